@@ -1,0 +1,391 @@
+// C ABI of the attention forward library: argument validation, workspace
+// layout, the decode split plan, TMA descriptor encoding and launches.
+//
+// The two-stage shape of the interface (size query, then a call that takes
+// a caller-owned workspace and a stream) follows aclnnIncreFlashAttention
+// guide §三 and §五; the checks mirror its §四 / §六 constraints
+// (numHeads a multiple of numKeyValueHeads, 0 meaning "same as numHeads",
+// lengths per batch) and the FlashAttn guide's layout and mask rules.
+// Every argument error is returned before any CUDA call is made.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+#include <vector>
+
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kMinChunk = 128;   // smallest chunk the split heuristic picks
+constexpr int kChunkQuant = 64;  // chunk sizes are multiples of this
+constexpr int kWaves = 4;        // heuristic target: about this many CTAs per SM
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// query heads per CTA in the decode stage-1 kernel (largest of 8/4/2/1 dividing g)
+int decode_heads_per_cta(int64_t g) {
+  return (g % 8 == 0) ? 8 : (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1;
+}
+
+struct DecodeWs {
+  size_t lens, items, part_lse, part_o, total;
+};
+
+DecodeWs decode_ws(int64_t B, int64_t Hq, int64_t D, int64_t max_chunks) {
+  DecodeWs w;
+  size_t off = kAlign;  // status word
+  w.lens = off;
+  off += align_up(sizeof(int32_t) * B);
+  w.items = off;
+  off += align_up(sizeof(int32_t) * 2 * B * max_chunks);
+  w.part_lse = off;
+  off += align_up(sizeof(float) * B * Hq * max_chunks);
+  w.part_o = off;
+  off += align_up(sizeof(float) * B * Hq * max_chunks * D);
+  w.total = off;
+  return w;
+}
+
+struct PrefillWs {
+  size_t lens, bits, total;
+};
+
+PrefillWs prefill_ws(int64_t B, int64_t S_kv) {
+  PrefillWs w;
+  size_t off = kAlign;  // status word
+  w.lens = off;
+  off += align_up(sizeof(int32_t) * B);
+  w.bits = off;
+  off += align_up(sizeof(uint32_t) * 4 * B * ceil_div(std::max<int64_t>(S_kv, 1), 128));
+  w.total = off;
+  return w;
+}
+
+int64_t chunk_for_splits(int64_t S_kv_max, int num_splits) {
+  int64_t c = ceil_div(S_kv_max, num_splits);
+  c = ceil_div(c, kChunkQuant) * kChunkQuant;
+  return std::max<int64_t>(c, kChunkQuant);
+}
+
+// ------------------------------------------------------------ driver entry
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+bool encode_bf16_map(CUtensorMap* map, const void* base, int layout, int64_t B, int64_t N,
+                     int64_t S, int64_t D, int box_d, int box_s, CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  // dimensions (D, S, N, B), innermost first; strides in bytes for dims 1..3
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+                              static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3];
+  if (layout == FA_LAYOUT_BNSD) {
+    strides[0] = static_cast<cuuint64_t>(D * 2);
+    strides[1] = static_cast<cuuint64_t>(S * D * 2);
+    strides[2] = static_cast<cuuint64_t>(N * S * D * 2);
+  } else {
+    strides[0] = static_cast<cuuint64_t>(N * D * 2);
+    strides[1] = static_cast<cuuint64_t>(D * 2);
+    strides[2] = static_cast<cuuint64_t>(S * N * D * 2);
+  }
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_d), static_cast<cuuint32_t>(box_s), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int device_sm_count() {
+  static std::mutex mu;
+  static std::vector<int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (static_cast<int>(cache.size()) <= dev) cache.resize(dev + 1, 0);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_abi_version(void) { return FA_ABI_VERSION; }
+
+const char* fa_status_string(int s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_NULLPTR: return "FA_ERR_NULLPTR: a required pointer is NULL";
+    case FA_ERR_PARAM_INVALID: return "FA_ERR_PARAM_INVALID: argument outside the contract";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be 64 or 128";
+    case FA_ERR_WORKSPACE_TOO_SMALL: return "FA_ERR_WORKSPACE_TOO_SMALL";
+    case FA_ERR_RUNTIME: return "FA_ERR_RUNTIME: a CUDA call failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT: a kernel wait expired";
+    default: return "unknown fa_status";
+  }
+}
+
+size_t fa_forward_workspace_size(int64_t B, int64_t S_q, int64_t S_kv, int64_t num_heads,
+                                 int64_t num_kv_heads, int64_t D) {
+  if (B < 0 || S_q < 0 || S_kv < 0 || num_heads < 0 || num_kv_heads < 0 || D < 0) return 0;
+  (void)S_q;
+  (void)num_heads;
+  (void)num_kv_heads;
+  (void)D;
+  return prefill_ws(B, S_kv).total;
+}
+
+fa_status fa_decode_plan(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t num_kv_heads,
+                         const int64_t* lens, int num_sms, int num_splits, int64_t* chunk_rows,
+                         int64_t* num_chunks, int64_t* max_chunks) {
+  if (lens == nullptr || chunk_rows == nullptr || num_chunks == nullptr || max_chunks == nullptr)
+    return FA_ERR_NULLPTR;
+  if (num_kv_heads == 0) num_kv_heads = num_heads;
+  if (B < 0 || S_kv_max < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+      num_heads % num_kv_heads != 0 || num_splits < 0 || num_sms <= 0 || S_kv_max > kMaxDim)
+    return FA_ERR_PARAM_INVALID;
+  int64_t total = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    if (lens[b] < 0 || lens[b] > S_kv_max) return FA_ERR_PARAM_INVALID;
+    total += lens[b];
+  }
+  int64_t chunk;
+  if (num_splits > 0) {
+    chunk = chunk_for_splits(std::max<int64_t>(S_kv_max, 1), num_splits);
+  } else {
+    // Spread the valid rows of every (batch, KV head, head group) over about
+    // kWaves CTAs per SM, in equal multiples of 64 rows.
+    const int64_t g = num_heads / num_kv_heads;
+    const int64_t per_row = num_kv_heads * (g / decode_heads_per_cta(g));
+    const int64_t target = static_cast<int64_t>(kWaves) * num_sms;
+    chunk = ceil_div(std::max<int64_t>(total * per_row, 1), target);
+    chunk = ceil_div(chunk, kChunkQuant) * kChunkQuant;
+    const int64_t cap = ceil_div(std::max<int64_t>(S_kv_max, 1), kChunkQuant) * kChunkQuant;
+    chunk = std::min(std::max<int64_t>(chunk, kMinChunk), std::max<int64_t>(cap, kMinChunk));
+  }
+  int64_t n = 0, mx = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t c = ceil_div(lens[b], chunk);
+    n += c;
+    mx = std::max(mx, c);
+  }
+  *chunk_rows = chunk;
+  *num_chunks = n;
+  *max_chunks = mx;
+  return FA_OK;
+}
+
+size_t fa_decode_workspace_size(int64_t B, int64_t S_kv_max, int64_t num_heads,
+                                int64_t num_kv_heads, int64_t D, int num_splits) {
+  if (num_kv_heads == 0) num_kv_heads = num_heads;
+  if (B < 0 || S_kv_max < 0 || num_heads < 0 || num_kv_heads < 0 || D < 0 || num_splits < 0)
+    return 0;
+  const int64_t S = std::max<int64_t>(S_kv_max, 1);
+  const int64_t chunk = num_splits > 0 ? chunk_for_splits(S, num_splits) : kMinChunk;
+  return decode_ws(B, num_heads, D, ceil_div(S, chunk)).total;
+}
+
+static fa_status check_common(int64_t B, int64_t S_q, int64_t S_kv, int64_t Hq, int64_t& Hkv,
+                              int64_t D, float scale, int layout) {
+  if (Hkv == 0) Hkv = Hq;
+  if (B < 0 || S_q < 0 || S_kv < 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return FA_ERR_PARAM_INVALID;
+  if (Hq % Hkv != 0) return FA_ERR_PARAM_INVALID;
+  if (layout != FA_LAYOUT_BNSD && layout != FA_LAYOUT_BSND) return FA_ERR_PARAM_INVALID;
+  if (!isfinite(scale)) return FA_ERR_PARAM_INVALID;
+  if (B > kMaxDim || S_q > kMaxDim || S_kv > kMaxDim || Hq > 65535) return FA_ERR_PARAM_INVALID;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa_status fa_forward(const void* q, const void* k, const void* v, int mask_mode,
+                     const uint8_t* key_mask, const int64_t* lens, int64_t B, int64_t S_q,
+                     int64_t S_kv, int64_t num_heads, int64_t num_kv_heads, int64_t D,
+                     float scale, int layout, void* out, float* lse, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || workspace == nullptr)
+    return FA_ERR_NULLPTR;
+  int64_t Hkv = num_kv_heads;
+  fa_status st = check_common(B, S_q, S_kv, num_heads, Hkv, D, scale, layout);
+  if (st != FA_OK) return st;
+  if (mask_mode != FA_MASK_NONE && mask_mode != FA_MASK_CAUSAL) return FA_ERR_PARAM_INVALID;
+  const bool causal = mask_mode == FA_MASK_CAUSAL;
+  if (causal && S_q != S_kv) return FA_ERR_PARAM_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
+    return FA_ERR_PARAM_INVALID;
+  if (lens != nullptr)
+    for (int64_t b = 0; b < B; ++b)
+      if (lens[b] < 0 || lens[b] > S_kv) return FA_ERR_PARAM_INVALID;
+  const PrefillWs ws = prefill_ws(B, S_kv);
+  if (workspace_bytes < ws.total) return FA_ERR_WORKSPACE_TOO_SMALL;
+  if (B == 0 || S_q == 0) return FA_OK;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char* wsb = static_cast<unsigned char*>(workspace);
+  // header: zeroed status word, then the lengths as int32 when given
+  std::vector<int32_t> blob(kAlign / 4 + (lens ? B : 0), 0);
+  if (lens)
+    for (int64_t b = 0; b < B; ++b) blob[kAlign / 4 + b] = static_cast<int32_t>(lens[b]);
+  if (cudaMemcpyAsync(wsb, blob.data(), blob.size() * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return FA_ERR_RUNTIME;
+  const uint32_t* bits = nullptr;
+  if ((key_mask != nullptr || lens != nullptr) && S_kv > 0) {
+    uint32_t* bits_dev = reinterpret_cast<uint32_t*>(wsb + ws.bits);
+    const int* lens_dev = lens ? reinterpret_cast<const int*>(wsb + ws.lens) : nullptr;
+    if (launch_tile_bits(key_mask, lens_dev, static_cast<int>(B), static_cast<int>(S_kv),
+                         bits_dev, s) != cudaSuccess)
+      return FA_ERR_RUNTIME;
+    bits = bits_dev;
+  }
+  PrefillLaunch x;
+  x.q = q;
+  x.k = k;
+  x.v = v;
+  x.B = static_cast<int>(B);
+  x.Hq = static_cast<int>(num_heads);
+  x.Hkv = static_cast<int>(Hkv);
+  x.S_q = static_cast<int>(S_q);
+  x.S_kv = static_cast<int>(S_kv);
+  x.D = static_cast<int>(D);
+  x.layout = layout;
+  x.causal = causal ? 1 : 0;
+  x.scale = scale;
+  x.tile_bits = bits;
+  x.out = out;
+  x.lse = lse;
+  x.status = reinterpret_cast<uint32_t*>(wsb);
+  x.timeout_ns = kDefaultTimeoutNs;
+  return launch_prefill(x, s) == cudaSuccess ? FA_OK : FA_ERR_RUNTIME;
+}
+
+fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                    const int64_t* lens, int64_t B, int64_t S_kv_max, int64_t num_heads,
+                    int64_t num_kv_heads, int64_t D, float scale, int layout, int num_splits,
+                    void* out, float* lse, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || workspace == nullptr ||
+      lens == nullptr)
+    return FA_ERR_NULLPTR;
+  int64_t Hkv = num_kv_heads;
+  fa_status st = check_common(B, 1, S_kv_max, num_heads, Hkv, D, scale, layout);
+  if (st != FA_OK) return st;
+  if (num_splits < 0) return FA_ERR_PARAM_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
+    return FA_ERR_PARAM_INVALID;
+  for (int64_t b = 0; b < B; ++b)
+    if (lens[b] < 0 || lens[b] > S_kv_max) return FA_ERR_PARAM_INVALID;
+  if (workspace_bytes < fa_decode_workspace_size(B, S_kv_max, num_heads, Hkv, D, num_splits))
+    return FA_ERR_WORKSPACE_TOO_SMALL;
+  if (B == 0) return FA_OK;
+
+  const int sms = device_sm_count();
+  if (sms <= 0) return FA_ERR_RUNTIME;
+  int64_t chunk = 0, n_items = 0, max_chunks = 0;
+  st = fa_decode_plan(B, S_kv_max, num_heads, Hkv, lens, sms, num_splits, &chunk, &n_items,
+                      &max_chunks);
+  if (st != FA_OK) return st;
+  const int64_t slots = std::max<int64_t>(max_chunks, 1);
+  const DecodeWs ws = decode_ws(B, num_heads, D, slots);
+  if (workspace_bytes < ws.total) return FA_ERR_WORKSPACE_TOO_SMALL;
+
+  // header blob: status word, lengths, work items (batch, chunk index)
+  std::vector<int32_t> blob(ws.items / 4 + 2 * n_items, 0);
+  for (int64_t b = 0; b < B; ++b) blob[ws.lens / 4 + b] = static_cast<int32_t>(lens[b]);
+  int64_t it = 0;
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t c = 0; c < ceil_div(lens[b], chunk); ++c, ++it) {
+      blob[ws.items / 4 + 2 * it] = static_cast<int32_t>(b);
+      blob[ws.items / 4 + 2 * it + 1] = static_cast<int32_t>(c);
+    }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char* wsb = static_cast<unsigned char*>(workspace);
+  if (cudaMemcpyAsync(wsb, blob.data(), blob.size() * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return FA_ERR_RUNTIME;
+
+  DecodeLaunch x;
+  x.q = q;
+  x.k = k;
+  x.v = v;
+  x.key_mask = key_mask;
+  x.B = static_cast<int>(B);
+  x.Hq = static_cast<int>(num_heads);
+  x.Hkv = static_cast<int>(Hkv);
+  x.S_kv = static_cast<int>(S_kv_max);
+  x.D = static_cast<int>(D);
+  x.layout = layout;
+  x.scale = scale;
+  x.chunk = static_cast<int>(chunk);
+  x.num_items = static_cast<int>(n_items);
+  x.max_chunks = static_cast<int>(slots);
+  x.lens_dev = reinterpret_cast<const int*>(wsb + ws.lens);
+  x.items_dev = reinterpret_cast<const int2*>(wsb + ws.items);
+  x.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
+  x.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
+  x.out = out;
+  x.lse = lse;
+  x.status = reinterpret_cast<uint32_t*>(wsb);
+  x.timeout_ns = kDefaultTimeoutNs;
+  return launch_decode(x, s) == cudaSuccess ? FA_OK : FA_ERR_RUNTIME;
+}
+
+fa_status fa_workspace_status(void* workspace, void* stream) {
+  if (workspace == nullptr) return FA_ERR_NULLPTR;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_RUNTIME;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FA_ERR_RUNTIME;
+  if (word != 0) {
+    if (cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return FA_ERR_RUNTIME;
+    return FA_ERR_DEVICE_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+fa_status fa_selftest_wait_timeout(void* workspace, uint64_t timeout_ns, void* stream) {
+  if (workspace == nullptr) return FA_ERR_NULLPTR;
+  if (timeout_ns == 0 || timeout_ns > 10000000000ull) return FA_ERR_PARAM_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return FA_ERR_RUNTIME;
+  return launch_wait_probe(static_cast<uint32_t*>(workspace), timeout_ns, s) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_RUNTIME;
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fa.h"
+
+namespace fa {
+
+// Encode a 4-D TMA map over a bf16 tensor stored BNSD or BSND, with
+// dimensions ordered (D, S, N, B) so that one box is `box_s` rows of
+// `box_d` elements of one (batch, head). Returns false on failure.
+bool encode_bf16_map(CUtensorMap* map, const void* base, int layout, int64_t B, int64_t N,
+                     int64_t S, int64_t D, int box_d, int box_s, CUtensorMapSwizzle swizzle);
+
+int device_sm_count();  // of the current device; 0 on failure
+
+struct DecodeLaunch {
+  const void* q;
+  const void* k;
+  const void* v;
+  const uint8_t* key_mask;
+  int B, Hq, Hkv, S_kv, D, layout;
+  float scale;
+  int chunk;       // KV rows per chunk
+  int num_items;   // (batch, chunk) work items
+  int max_chunks;  // chunk slots per (batch, head) in the partial buffers
+  const int* lens_dev;      // [B] in the workspace
+  const int2* items_dev;    // [num_items] in the workspace
+  float* part_o;            // [B, Hq, max_chunks, D]
+  float* part_lse;          // [B, Hq, max_chunks] (log2 domain)
+  void* out;
+  float* lse;
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream);
+
+struct PrefillLaunch {
+  const void* q;
+  const void* k;
+  const void* v;
+  int B, Hq, Hkv, S_q, S_kv, D, layout, causal;
+  float scale;
+  const uint32_t* tile_bits;  // [B][ceil(S_kv/128)][4] or null
+  void* out;
+  float* lse;
+  uint32_t* status;
+  uint64_t timeout_ns;
+};
+cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t stream);
+
+// Build the per-(batch, 128-key tile) validity bit table from an optional
+// key mask and optional device lengths.
+cudaError_t launch_tile_bits(const uint8_t* key_mask, const int* lens_dev, int B, int S_kv,
+                             uint32_t* bits, cudaStream_t stream);
+
+cudaError_t launch_wait_probe(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+
+// Default bounded-wait limit of the kernels (nanoseconds).
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+}  // namespace fa

@@ -1,0 +1,601 @@
+// Fused attention forward (prefill) for sm_103a on the 5th-generation
+// tensor cores.
+//
+// One CTA owns 256 consecutive query rows of one (batch, head) as two
+// 128-row tiles Q0, Q1 and walks the KV sequence in 128-key tiles
+// (FlashAttn guide, developer guide §3: tile the Q_S x KV_S matrix; never
+// store it). Per KV tile j and Q tile t:
+//     S_t   = Q_t K_j^T                          (tcgen05.mma, fp32 in TMEM)
+//     m'    = max(m, rowmax(scale*S_t)), P = 2^(scale*log2e*S_t - m')
+//     l     = l*2^(m-m') + rowsum(P),  O_t = O_t*2^(m-m') + P V_j  (tcgen05.mma)
+// and finally out = O_t / l, lse = ln2*(m + log2 l)  (aclnnIncreFlashAttention
+// guide §8.1: per-tile max/exp/sum refresh, division by the sum moved to
+// the end; FlashAttn guide §1.6 LSE and §1.7 invalid rows).
+//
+// Warp roles (384 threads, three warpgroups):
+//   warps 0-3  softmax of Q0 (thread i <-> query row i <-> TMEM lane i)
+//   warps 4-7  softmax of Q1
+//   warp 8     TMA producer: Q0/Q1 once, then K_j, V_j through a 4-slot ring
+//   warp 9     TMEM allocator and MMA issuer (one elected lane)
+//   warps 10-11 idle (they complete the third warpgroup for setmaxnreg)
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
+// P_t (bf16, two per column) overwrites the first 64 columns of S_t and is
+// the A operand of O_t += P_t V_j straight from TMEM.
+// The MMA warp interleaves the two tiles (S0 S1 | PV0 S0' | PV1 S1' | ...)
+// so that one tile's softmax runs while the tensor core works on the other.
+//
+// Causal (FlashAttn guide §1.5, mode 3): KV tiles above the diagonal are
+// never loaded or multiplied; only the diagonal tile and tiles that hold
+// masked or out-of-range keys pay for per-element predicates. Keys excluded
+// by the key mask or the actual length have their V rows zeroed in shared
+// memory before the P*V product, so whatever they hold cannot leak.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBM = 128;        // query rows per Q tile
+constexpr int kBN = 128;        // keys per KV tile
+constexpr int kRing = 4;        // K/V ring slots
+constexpr int kThreads = 384;   // three warpgroups
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;     // warps 10-11 only complete the third warpgroup
+// Register split (setmaxnreg): the launch gives 168 per thread (384 x 168 =
+// 64512); the softmax warpgroups take 224 each and the load/MMA warpgroup 56:
+// 128 x (224 + 224 + 56) = 64512.
+constexpr int kSoftmaxRegs = 224;
+constexpr int kControlRegs = 56;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when m grows by > 2^8
+
+template <int D>
+struct PCfg {
+  static constexpr int kTileBytes = kBM * D * 2;  // one Q, K or V tile
+  static constexpr int kSubBytes = kBM * 128;     // one 64-column swizzle slab (16 KB)
+  static constexpr int kQOff = 0;
+  static constexpr int kRingOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kRingOff + kRing * kTileBytes;
+  // barriers + alignment slack; at least 116 KB so that two CTAs never share
+  // an SM (each allocates all 512 TMEM columns)
+  static constexpr int kSmemBytes = (kBarOff + 256 + 1024) > 118784 ? (kBarOff + 256 + 1024) : 118784;
+};
+
+struct PrefillArgs {
+  __nv_bfloat16* out;
+  float* lse;
+  const uint32_t* tile_bits;  // [B][n_kv_tiles][4], bit set = key valid; or null
+  uint32_t* status;
+  uint64_t timeout_ns;
+  int B, Hq, Hkv, S_q, S_kv, causal;
+  int n_qpairs, n_kv_tiles;
+  long long out_row_stride, out_head_stride, out_batch_stride;  // elements
+  float scale_log2;
+};
+
+// Barrier slots (8 bytes each) after the tiles.
+enum : int {
+  kBarQ = 0,
+  kBarKvFull = 1,                 // + slot
+  kBarKvEmpty = kBarKvFull + kRing,
+  kBarSFull = kBarKvEmpty + kRing,  // + tile
+  kBarPReady = kBarSFull + 2,
+  kBarOFinal = kBarPReady + 2,
+  kBarFix = kBarOFinal + 2,
+  kBarDrain = kBarFix + 1,
+  kNumBars = kBarDrain + 1
+};
+
+struct TileSeq {
+  const uint32_t* bits;  // this batch's rows of the tile table, or null
+  int end;               // one past the last KV tile any Q tile of the CTA needs
+  __device__ __forceinline__ int next(int j) const {
+    for (; j < end; ++j) {
+      if (bits == nullptr) return j;
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(bits) + j);
+      if ((w.x | w.y | w.z | w.w) != 0u) return j;
+    }
+    return end;
+  }
+  __device__ __forceinline__ bool full(int j) const {
+    if (bits == nullptr) return true;
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(bits) + j);
+    return (w.x & w.y & w.z & w.w) == 0xFFFFFFFFu;
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
+  using C = PCfg<D>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto bar = [&](int i) -> uint32_t { return smem_u32(bars + i); };
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  // ---- work tile: heaviest (last) query pairs first
+  const int bh_count = a.B * a.Hq;
+  const int qp = a.n_qpairs - 1 - static_cast<int>(blockIdx.x) / bh_count;
+  const int bh = static_cast<int>(blockIdx.x) % bh_count;
+  const int b = bh / a.Hq;
+  const int h = bh % a.Hq;
+  const int kvh = h / (a.Hq / a.Hkv);
+  const int q_row0 = qp * 2 * kBM;
+  const bool has_t1 = q_row0 + kBM < a.S_q;
+  // KV tiles each Q tile needs (a prefix of the tile sequence)
+  int n_t[2];
+  for (int t = 0; t < 2; ++t) {
+    int n = a.n_kv_tiles;
+    if (a.causal) n = min(n, (q_row0 + t * kBM) / kBN + 1);
+    if (t == 1 && !has_t1) n = 0;
+    n_t[t] = n;
+  }
+  TileSeq seq;
+  seq.bits = a.tile_bits ? a.tile_bits + static_cast<size_t>(b) * a.n_kv_tiles * 4 : nullptr;
+  seq.end = max(n_t[0], n_t[1]);
+
+  if (tid == 0) {
+    for (int i = 0; i < kNumBars; ++i) {
+      uint32_t cnt = 1;
+      if (i == kBarPReady || i == kBarPReady + 1) cnt = kBM;
+      mbar_init(bar(i), cnt);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp >= 8) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
+  if (warp == kProducerWarp) {
+    // ================================================================ TMA
+    // Every lane waits on the same barriers and the warp votes on the result,
+    // so the warp always takes one path (also when a wait gives up).
+    if (lane == 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+      const int nq = has_t1 ? 2 : 1;
+      mbar_expect_tx(bar(kBarQ), nq * C::kTileBytes);
+      for (int t = 0; t < nq; ++t)
+        for (int s = 0; s < D / 64; ++s)
+          tma_load_4d(smem_u32(smem + C::kQOff + t * C::kTileBytes + s * C::kSubBytes), &tm_q,
+                      bar(kBarQ), s * 64, q_row0 + t * kBM, h, b);
+    }
+    __syncwarp();
+    int item = 0;  // ring items issued so far (K_j and V_j are one item each)
+    int fixes = 0;
+    bool ok = true;
+    for (int j = seq.next(0); ok && j < seq.end; j = seq.next(j + 1)) {
+      const bool fix_v = !seq.full(j);
+      for (int kv = 0; kv < 2; ++kv) {
+        const int slot = item % kRing;
+        const int use = item / kRing;
+        if (use > 0) {
+          ok = mbar_wait(bar(kBarKvEmpty + slot), (use - 1) & 1, a.timeout_ns, a.status,
+                         kDevTimeoutKvEmpty, abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+        }
+        const uint32_t dst = smem_u32(smem + C::kRingOff + slot * C::kTileBytes);
+        const CUtensorMap* map = kv == 0 ? &tm_k : &tm_v;
+        if (kv == 1 && fix_v) {
+          // land V on the side barrier, zero the rows of excluded keys, publish
+          if (lane == 0) {
+            mbar_expect_tx(bar(kBarFix), C::kTileBytes);
+            for (int s = 0; s < D / 64; ++s)
+              tma_load_4d(dst + s * C::kSubBytes, map, bar(kBarFix), s * 64, j * kBN, kvh, b);
+          }
+          ++item;
+          ok = mbar_wait(bar(kBarFix), fixes & 1, a.timeout_ns, a.status, kDevTimeoutKvFull,
+                         abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+          ++fixes;
+          if (!ok) break;
+          const uint4 w = __ldg(reinterpret_cast<const uint4*>(seq.bits) + j);
+          uint4* tile = reinterpret_cast<uint4*>(smem + C::kRingOff + slot * C::kTileBytes);
+          // 128 rows x (D/64 slabs) x 8 chunks of 16 B; a row of a slab is 128
+          // contiguous bytes whatever the swizzle
+          for (int idx = lane; idx < kBN * (D / 64) * 8; idx += 32) {
+            const int r = idx / ((D / 64) * 8);
+            const int rest = idx % ((D / 64) * 8);
+            const int s = rest / 8, ch = rest % 8;
+            const uint32_t word = r < 64 ? (r < 32 ? w.x : w.y) : (r < 96 ? w.z : w.w);
+            if (((word >> (r & 31)) & 1u) == 0u)
+              tile[(s * C::kSubBytes + r * 128) / 16 + ch] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarKvFull + slot));
+        } else {
+          if (lane == 0) {
+            mbar_expect_tx(bar(kBarKvFull + slot), C::kTileBytes);
+            for (int s = 0; s < D / 64; ++s)
+              tma_load_4d(dst + s * C::kSubBytes, map, bar(kBarKvFull + slot), s * 64, j * kBN,
+                          kvh, b);
+          }
+          ++item;
+        }
+        __syncwarp();
+      }
+    }
+    if (ok) {
+      // tail: wait until the MMA warp has released the last ring slots, so no
+      // asynchronous arrival can reach this CTA's shared memory after exit
+      for (int it = max(0, item - kRing); it < item && ok; ++it) {
+        ok = mbar_wait(bar(kBarKvEmpty + it % kRing), (it / kRing) & 1, a.timeout_ns, a.status,
+                       kDevTimeoutKvEmpty, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+    }
+    if (!ok && lane == 0) {
+      // let the copies this CTA started land before its shared memory is released
+      for (int it = max(0, item - kRing); it < item; ++it)
+        mbar_wait(bar(kBarKvFull + it % kRing), (it / kRing) & 1, a.timeout_ns, a.status,
+                  kDevTimeoutDrain, nullptr);
+      if (fixes > 0) mbar_wait(bar(kBarFix), (fixes - 1) & 1, a.timeout_ns, a.status,
+                               kDevTimeoutDrain, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ================================================================ MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, 0, 1);
+      const uint32_t q_base = smem_u32(smem + C::kQOff);
+      const uint32_t ring_base = smem_u32(smem + C::kRingOff);
+      bool ok = mbar_wait(bar(kBarQ), 0, a.timeout_ns, a.status, kDevTimeoutQ, abort_flag);
+      tc_fence_after();
+      auto issue_s = [&](int t, uint32_t k_addr) {
+        const uint32_t d_tmem = tmem + t * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::kSubBytes + (kk % 4) * 32;
+          umma_ss(d_tmem, smem_desc_sw128(q_base + t * C::kTileBytes + off, 16, 1024),
+                  smem_desc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(bar(kBarSFull + t));
+      };
+      auto issue_pv = [&](int t, uint32_t v_addr, bool first) {
+        const uint32_t d_tmem = tmem + 256 + t * 128;
+        const uint32_t p_tmem = tmem + t * 128;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_ts(d_tmem, p_tmem + kk * 8,
+                  smem_desc_sw128(v_addr + kk * 16 * 128, C::kSubBytes, 1024), idesc_pv,
+                  (first && kk == 0) ? 0u : 1u);
+      };
+      int item = 0;
+      int pv_count[2] = {0, 0};
+      int j = seq.next(0);
+      // prologue: S of the first tile
+      if (ok && j < seq.end) {
+        const int slot = item % kRing;
+        ok = mbar_wait(bar(kBarKvFull + slot), (item / kRing) & 1, a.timeout_ns, a.status,
+                       kDevTimeoutKvFull, abort_flag);
+        if (ok) {
+          tc_fence_after();
+          const uint32_t k_addr = ring_base + slot * C::kTileBytes;
+          for (int t = 0; t < 2; ++t)
+            if (j < n_t[t]) issue_s(t, k_addr);
+          umma_commit(bar(kBarKvEmpty + slot));
+        }
+      }
+      for (int t = 0; t < 2; ++t)  // a tile that sees no key at all
+        if ((t == 0 || has_t1) && !(j < n_t[t])) umma_commit(bar(kBarOFinal + t));
+      while (ok && j < seq.end) {
+        const int v_item = item + 1;
+        const int v_slot = v_item % kRing;
+        const int jn = seq.next(j + 1);
+        const int k_item = item + 2;
+        const int k_slot = k_item % kRing;
+        ok = mbar_wait(bar(kBarKvFull + v_slot), (v_item / kRing) & 1, a.timeout_ns, a.status,
+                       kDevTimeoutKvFull, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        bool k_ready = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!(j < n_t[t])) continue;
+          ok = mbar_wait(bar(kBarPReady + t), pv_count[t] & 1, a.timeout_ns, a.status,
+                         kDevTimeoutPReady, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, ring_base + v_slot * C::kTileBytes, pv_count[t] == 0);
+          ++pv_count[t];
+          if (jn < n_t[t]) {
+            if (!k_ready) {
+              ok = mbar_wait(bar(kBarKvFull + k_slot), (k_item / kRing) & 1, a.timeout_ns,
+                             a.status, kDevTimeoutKvFull, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_s(t, ring_base + k_slot * C::kTileBytes);
+          } else {
+            umma_commit(bar(kBarOFinal + t));
+          }
+        }
+        if (!ok) break;
+        umma_commit(bar(kBarKvEmpty + v_slot));
+        if (k_ready) umma_commit(bar(kBarKvEmpty + k_slot));
+        item += 2;
+        j = jn;
+      }
+    }
+    __syncwarp();
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+    // ============================================================ softmax
+    const int t = warp / 4;          // Q tile of this warpgroup
+    const int wl = warp % 4;         // TMEM lane quarter
+    const int row_in_tile = wl * 32 + lane;
+    const int row = q_row0 + t * kBM + row_in_tile;
+    const uint32_t lane_bits = static_cast<uint32_t>(wl * 32) << 16;
+    const uint32_t s_tmem = tmem + lane_bits + t * 128;
+    const uint32_t o_tmem = tmem + lane_bits + 256 + t * 128;
+    const float c = a.scale_log2;
+    float m_run = -INFINITY;  // reference max, log2 domain
+    float l_run = 0.f;
+    int k = 0;
+    bool ok = true;
+    for (int j = seq.next(0); j < n_t[t]; j = seq.next(j + 1), ++k) {
+      ok = mbar_wait(bar(kBarSFull + t), k & 1, a.timeout_ns, a.status, kDevTimeoutSFull,
+                     abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(s_tmem + q4 * 32, sr[q4]);
+      tmem_ld_wait();
+      const bool masked = (a.causal && j * kBN + kBN - 1 > q_row0 + t * kBM) ||
+                          ((j + 1) * kBN > a.S_kv) || !seq.full(j);
+      float tmax = -INFINITY;
+      if (masked) {
+        uint32_t words[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+        if (seq.bits != nullptr) {
+          const uint4 w = __ldg(reinterpret_cast<const uint4*>(seq.bits) + j);
+          words[0] = w.x; words[1] = w.y; words[2] = w.z; words[3] = w.w;
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int key = j * kBN + q4 * 32 + i;
+            const bool valid = ((words[q4] >> i) & 1u) && key < a.S_kv && (!a.causal || key <= row);
+            const float tv = valid ? __uint_as_float(sr[q4][i]) * c : -INFINITY;
+            sr[q4][i] = __float_as_uint(tv);
+            tmax = fmaxf(tmax, tv);
+          }
+        }
+      } else {
+        float smax = -INFINITY, smin = INFINITY;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            smax = fmaxf(smax, __uint_as_float(sr[q4][i]));
+            smin = fminf(smin, __uint_as_float(sr[q4][i]));
+          }
+        tmax = (c >= 0.f) ? smax * c : smin * c;
+      }
+      // conditional rescale: keep the reference max unless it grows by > 2^8
+      const float m_cand = fmaxf(m_run, tmax);
+      float alpha = 1.f;
+      const bool need = m_cand > m_run + kRescaleThreshold;
+      if (need) {
+        alpha = ex2(m_run - m_cand);  // 0 when m_run was -inf
+        m_run = m_cand;
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      float rsum = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+          const int q4 = half * 2 + qq;
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float p0, p1;
+            if (masked) {
+              p0 = ex2(__uint_as_float(sr[q4][i]) - m_use);
+              p1 = ex2(__uint_as_float(sr[q4][i + 1]) - m_use);
+            } else {
+              p0 = ex2(fmaf(__uint_as_float(sr[q4][i]), c, -m_use));
+              p1 = ex2(fmaf(__uint_as_float(sr[q4][i + 1]), c, -m_use));
+            }
+            rsum += p0 + p1;
+            pk[qq * 16 + i / 2] = pack_bf16x2(p0, p1);
+          }
+        }
+        tmem_st32(s_tmem + half * 32, pk);  // P overwrites S columns already read
+      }
+      l_run = l_run * alpha + rsum;
+      if (k > 0 && __any_sync(0xffffffffu, need)) {
+        // O_t was complete when S_t(j) landed (tcgen05 ops retire in order)
+#pragma unroll
+        for (int q4 = 0; q4 < D / 32; ++q4) {
+          uint32_t orr[32];
+          tmem_ld32(o_tmem + q4 * 32, orr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+          tmem_st32(o_tmem + q4 * 32, orr);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(kBarPReady + t));
+    }
+    // ---- epilogue: out = O / l, lse = ln2 * (m + log2 l)
+    if (ok && (t == 0 || has_t1)) {
+      ok = mbar_wait(bar(kBarOFinal + t), 0, a.timeout_ns, a.status, kDevTimeoutOFinal,
+                     abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        const bool row_ok = row < a.S_q;
+        const bool invalid = (l_run == 0.f);
+        const float inv_l = invalid ? 0.f : 1.f / l_run;
+        __nv_bfloat16* dst = a.out + static_cast<long long>(b) * a.out_batch_stride +
+                             static_cast<long long>(h) * a.out_head_stride +
+                             static_cast<long long>(row) * a.out_row_stride;
+#pragma unroll
+        for (int q4 = 0; q4 < D / 32; ++q4) {
+          uint32_t orr[32];
+          tmem_ld32(o_tmem + q4 * 32, orr);
+          tmem_ld_wait();
+          if (row_ok) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + q4 * 32);
+#pragma unroll
+            // an invalid row writes exact zeros: its O columns may never have
+            // been written by an MMA
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              orr[i] = invalid ? 0u : __float_as_uint(__uint_as_float(orr[i]) * inv_l);
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint4 u;
+              u.x = pack_bf16x2(__uint_as_float(orr[i]), __uint_as_float(orr[i + 1]));
+              u.y = pack_bf16x2(__uint_as_float(orr[i + 2]), __uint_as_float(orr[i + 3]));
+              u.z = pack_bf16x2(__uint_as_float(orr[i + 4]), __uint_as_float(orr[i + 5]));
+              u.w = pack_bf16x2(__uint_as_float(orr[i + 6]), __uint_as_float(orr[i + 7]));
+              d4[i / 8] = u;
+            }
+          }
+        }
+        if (row_ok && a.lse != nullptr)
+          a.lse[(static_cast<long long>(b) * a.Hq + h) * a.S_q + row] =
+              invalid ? INFINITY : (m_run + log2f(l_run)) * 0.69314718055994530942f;
+      }
+    }
+  }
+
+  // ---- teardown: every role is done with TMEM and shared memory
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    if (*abort_flag && lane == 0) {
+      // in-flight MMAs retire in order: one last commit covers all of them
+      umma_commit(bar(kBarDrain));
+      mbar_wait(bar(kBarDrain), 0, a.timeout_ns, a.status, kDevTimeoutDrain, nullptr);
+    }
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+__global__ void tile_bits_kernel(const uint8_t* __restrict__ key_mask, const int* __restrict__ lens,
+                                 int S_kv, int n_tiles, uint32_t* __restrict__ bits) {
+  const int tile = blockIdx.x;
+  const int b = blockIdx.y;
+  const int key = tile * kBN + threadIdx.x;
+  bool valid = key < S_kv;
+  if (valid && lens != nullptr) valid = key < lens[b];
+  if (valid && key_mask != nullptr) valid = key_mask[static_cast<size_t>(b) * S_kv + key] == 0;
+  const uint32_t word = __ballot_sync(0xffffffffu, valid);
+  if ((threadIdx.x & 31) == 0)
+    bits[(static_cast<size_t>(b) * n_tiles + tile) * 4 + (threadIdx.x >> 5)] = word;
+}
+
+__global__ void wait_probe_kernel(uint32_t* status, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar_storage;
+  const uint32_t b = smem_u32(&bar_storage);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // nothing ever arrives: the bounded wait must give up and record the error
+  if (threadIdx.x == 0) mbar_wait(b, 0, timeout_ns, status, kDevTimeoutProbe, nullptr);
+}
+
+template <int D>
+cudaError_t launch_prefill_d(const PrefillLaunch& x, cudaStream_t stream) {
+  using C = PCfg<D>;
+  static bool configured = false;  // benign race: idempotent attribute set
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  CUtensorMap mq, mk, mv;
+  const int64_t S_kv_map = x.S_kv > 0 ? x.S_kv : 1;
+  if (!encode_bf16_map(&mq, x.q, x.layout, x.B, x.Hq, x.S_q, D, 64, kBM,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_bf16_map(&mk, x.k, x.layout, x.B, x.Hkv, S_kv_map, D, 64, kBN,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_bf16_map(&mv, x.v, x.layout, x.B, x.Hkv, S_kv_map, D, 64, kBN,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  PrefillArgs pa;
+  pa.out = static_cast<__nv_bfloat16*>(x.out);
+  pa.lse = x.lse;
+  pa.tile_bits = x.tile_bits;
+  pa.status = x.status;
+  pa.timeout_ns = x.timeout_ns;
+  pa.B = x.B;
+  pa.Hq = x.Hq;
+  pa.Hkv = x.Hkv;
+  pa.S_q = x.S_q;
+  pa.S_kv = x.S_kv;
+  pa.causal = x.causal;
+  pa.n_qpairs = (x.S_q + 2 * kBM - 1) / (2 * kBM);
+  pa.n_kv_tiles = (x.S_kv + kBN - 1) / kBN;
+  if (x.layout == FA_LAYOUT_BNSD) {
+    pa.out_row_stride = D;
+    pa.out_head_stride = static_cast<long long>(x.S_q) * D;
+    pa.out_batch_stride = static_cast<long long>(x.Hq) * x.S_q * D;
+  } else {
+    pa.out_row_stride = static_cast<long long>(x.Hq) * D;
+    pa.out_head_stride = D;
+    pa.out_batch_stride = static_cast<long long>(x.S_q) * x.Hq * D;
+  }
+  pa.scale_log2 = x.scale * 1.4426950408889634f;
+  const long long grid = static_cast<long long>(pa.n_qpairs) * x.B * x.Hq;
+  prefill_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv,
+                                                                                      pa);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillLaunch& x, cudaStream_t stream) {
+  return x.D == 128 ? launch_prefill_d<128>(x, stream) : launch_prefill_d<64>(x, stream);
+}
+
+cudaError_t launch_tile_bits(const uint8_t* key_mask, const int* lens_dev, int B, int S_kv,
+                             uint32_t* bits, cudaStream_t stream) {
+  const int n_tiles = (S_kv + kBN - 1) / kBN;
+  tile_bits_kernel<<<dim3(n_tiles, B), kBN, 0, stream>>>(key_mask, lens_dev, S_kv, n_tiles, bits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_probe(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,177 @@
+"""Python binding of the C ABI (``include/fa.h``), same names as the C calls.
+
+Argument marshalling only: shapes are read from the tensors, outputs and the
+workspace are allocated with torch when not supplied, and every computation
+runs in the CUDA library on torch's current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import FaError, check  # noqa: F401
+
+LAYOUTS = {"BNSD": _lib.FA_LAYOUT_BNSD, "BSND": _lib.FA_LAYOUT_BSND, "BSH": _lib.FA_LAYOUT_BSND}
+MASK_MODES = {None: _lib.FA_MASK_NONE, "none": _lib.FA_MASK_NONE, 0: _lib.FA_MASK_NONE,
+              "causal": _lib.FA_MASK_CAUSAL, 3: _lib.FA_MASK_CAUSAL}
+
+
+def _layout_id(layout) -> int:
+    if isinstance(layout, int):
+        return layout
+    return LAYOUTS[layout.upper()]
+
+
+def _dims(x: torch.Tensor, layout_id: int):
+    """(B, N, S, D) of a 4-D tensor in the given layout."""
+    if x.dim() != 4:
+        raise ValueError("expected a 4-D tensor")
+    if layout_id == _lib.FA_LAYOUT_BNSD:
+        B, N, S, D = x.shape
+    else:
+        B, S, N, D = x.shape
+    return B, N, S, D
+
+
+def _check_tensor(x: torch.Tensor, name: str, dtype=torch.bfloat16):
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if x.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _lens_array(lens, B):
+    if lens is None:
+        return None, None
+    if isinstance(lens, torch.Tensor):
+        lens = lens.detach().cpu().tolist()
+    lens = [int(x) for x in lens]
+    if len(lens) != B:
+        raise ValueError("actual_seq_lengths must have B entries")
+    arr = (ctypes.c_int64 * max(B, 1))(*lens)
+    return arr, lens
+
+
+def fa_abi_version() -> int:
+    return _lib.load().fa_abi_version()
+
+
+def fa_status_string(status: int) -> str:
+    return _lib.load().fa_status_string(status).decode()
+
+
+def fa_forward_workspace_size(B, S_q, S_kv, num_heads, num_kv_heads, D) -> int:
+    return int(_lib.load().fa_forward_workspace_size(B, S_q, S_kv, num_heads, num_kv_heads, D))
+
+
+def fa_decode_workspace_size(B, S_kv_max, num_heads, num_kv_heads, D, num_splits=0) -> int:
+    return int(_lib.load().fa_decode_workspace_size(B, S_kv_max, num_heads, num_kv_heads, D,
+                                                    num_splits))
+
+
+def fa_decode_plan(actual_seq_lengths, S_kv_max, num_heads, num_kv_heads, num_sms, num_splits=0):
+    """(chunk_rows, num_chunks, max_chunks) of the decode split plan (host only)."""
+    B = len(actual_seq_lengths)
+    arr, _ = _lens_array(actual_seq_lengths, B)
+    c, n, m = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    st = _lib.load().fa_decode_plan(B, S_kv_max, num_heads, num_kv_heads, arr, num_sms,
+                                    num_splits, ctypes.byref(c), ctypes.byref(n), ctypes.byref(m))
+    check(st, "fa_decode_plan")
+    return c.value, n.value, m.value
+
+
+def fa_forward(q, k, v, *, mask_mode=None, key_mask=None, actual_seq_lengths=None, scale=1.0,
+               layout="BNSD", num_heads=None, num_kv_heads=None, out=None, lse=None,
+               return_lse=True, workspace=None, stream=None):
+    """Prefill attention. Returns (out, lse); lse is None unless requested."""
+    lid = _layout_id(layout)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n)
+    B, Hq, S_q, D = _dims(q, lid)
+    Bk, Hkv, S_kv, Dk = _dims(k, lid)
+    if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("q, k, v shapes disagree")
+    if num_heads is not None and num_heads != Hq:
+        raise ValueError("num_heads does not match q")
+    if num_kv_heads not in (None, 0) and num_kv_heads != Hkv:
+        raise ValueError("num_kv_heads does not match k")
+    if out is None:
+        out = torch.empty_like(q)
+    _check_tensor(out, "out")
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, S_q), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_tensor(lse, "lse", torch.float32)
+    if key_mask is not None:
+        _check_tensor(key_mask, "key_mask", torch.uint8)
+    need = fa_forward_workspace_size(B, S_q, S_kv, Hq, Hkv, D)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    lens_arr, _ = _lens_array(actual_seq_lengths, B)
+    st = _lib.load().fa_forward(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), MASK_MODES.get(mask_mode, mask_mode),
+        key_mask.data_ptr() if key_mask is not None else None, lens_arr, B, S_q, S_kv, Hq, Hkv,
+        D, float(scale), lid, out.data_ptr(), lse.data_ptr() if lse is not None else None,
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    check(st, "fa_forward")
+    return out, lse
+
+
+def fa_decode(q, k, v, actual_seq_lengths, *, key_mask=None, scale=1.0, layout="BNSD",
+              num_splits=0, num_heads=None, num_kv_heads=None, out=None, lse=None,
+              return_lse=True, workspace=None, stream=None):
+    """Decode (S_q = 1) attention with Split-KV. Returns (out, lse)."""
+    lid = _layout_id(layout)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n)
+    B, Hq, S_q, D = _dims(q, lid)
+    if S_q != 1:
+        raise ValueError("decode takes one query row per batch (S_q = 1)")
+    Bk, Hkv, S_kv, Dk = _dims(k, lid)
+    if (Bk, Dk) != (B, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("q, k, v shapes disagree")
+    if num_heads is not None and num_heads != Hq:
+        raise ValueError("num_heads does not match q")
+    if out is None:
+        out = torch.empty_like(q)
+    _check_tensor(out, "out")
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_tensor(lse, "lse", torch.float32)
+    if key_mask is not None:
+        _check_tensor(key_mask, "key_mask", torch.uint8)
+    need = fa_decode_workspace_size(B, S_kv, Hq, Hkv, D, num_splits)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    lens_arr, _ = _lens_array(actual_seq_lengths, B)
+    if lens_arr is None:
+        raise ValueError("actual_seq_lengths is required for decode")
+    st = _lib.load().fa_decode(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(),
+        key_mask.data_ptr() if key_mask is not None else None, lens_arr, B, S_kv, Hq, Hkv, D,
+        float(scale), lid, int(num_splits), out.data_ptr(),
+        lse.data_ptr() if lse is not None else None, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    check(st, "fa_decode")
+    return out, lse
+
+
+def fa_workspace_status(workspace, stream=None) -> int:
+    """Synchronise the stream and read/clear the workspace's device status word."""
+    return int(_lib.load().fa_workspace_status(workspace.data_ptr(), _stream_ptr(stream)))
+
+
+def fa_selftest_wait_timeout(workspace, timeout_ns: int, stream=None) -> int:
+    return int(_lib.load().fa_selftest_wait_timeout(workspace.data_ptr(), int(timeout_ns),
+                                                    _stream_ptr(stream)))

@@ -1,0 +1,169 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) fused attention forward library.
+ *
+ * What is computed (FlashAttn operator guide, functional description;
+ * aclnnIncreFlashAttention guide §1.2):
+ *
+ *     out = softmax(scale * Q K^T  [masked]) V,   lse = log sum_j exp(scale * q.k_j)
+ *
+ * row by row, tile by tile with a running max m and sum l, so the
+ * S_q x S_kv score matrix is never stored (FlashAttn guide, functional
+ * description and developer guide §3). Two regimes:
+ *   - prefill (fa_forward): S_q = S_kv rows, optional causal mask, optional
+ *     per-key mask, GQA;
+ *   - decode (fa_decode): S_q = 1 against a padded KV cache with per-batch
+ *     actual lengths, split along the keys into chunks (Split-KV) whose
+ *     partial results are merged by their log-sum-exp (FlashAttn guide §1.9
+ *     and §10; aclnnIncreFlashAttention guide §8.2-§8.3; FlashDecoding
+ *     tutorial §二-§三).
+ *
+ * Conventions shared by every entry point
+ *   - Tensors q, k, v, out are bf16, dense (contiguous), in one of two
+ *     layouts (FlashAttn guide, parameter layouts; aclnnIncreFlashAttention
+ *     guide §四 inputLayout): BNSD = [B, N, S, D] or BSND = [B, S, N, D]
+ *     (BSH is BSND memory). out has the shape and layout of q. The base
+ *     address of every tensor must be 16-byte aligned.
+ *   - lse (optional, may be NULL) is fp32 [B, num_heads, S_q], natural log
+ *     (FlashAttn guide §1.6).
+ *   - GQA: num_heads must be a multiple of num_kv_heads; query head h reads
+ *     KV head h / (num_heads / num_kv_heads) (FlashAttn guide §1.1).
+ *     num_kv_heads == 0 means num_kv_heads = num_heads
+ *     (aclnnIncreFlashAttention guide §四, numKeyValueHeads).
+ *   - key_mask (optional, may be NULL): device uint8 [B, S_kv], one flag per
+ *     key shared by all heads and query rows; nonzero = the key is excluded
+ *     (aclnnIncreFlashAttention guide §8.1: true positions are masked out).
+ *   - actual_seq_lengths: HOST int64 [B], valid KV length per batch; keys at
+ *     or past it are ignored entirely and may hold any bits, NaN included
+ *     (aclnnIncreFlashAttention guide §四 actualSeqLengths and §1.1).
+ *   - A query row with no valid key gets out = 0 and lse = +inf (FlashAttn
+ *     guide §1.7, row invalid).
+ *   - Head dimension D must be 64 or 128.
+ *   - Two-stage use as in aclnnIncreFlashAttention guide §三: ask for the
+ *     workspace size, allocate it on the device, then call. The caller owns
+ *     every buffer; the library allocates no device memory and keeps no
+ *     pointer after a call returns.
+ *   - All device work is enqueued on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and runs asynchronously. Argument errors are
+ *     detected and returned before anything is enqueued.
+ *   - Results are deterministic: no atomics, fixed reduction order.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FA_ABI_VERSION 1
+
+/* Status codes; the classes follow aclnnIncreFlashAttention guide §四
+ * (return values: null pointer, invalid parameter, runtime error). */
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_NULLPTR = 1,             /* a required pointer is NULL */
+  FA_ERR_PARAM_INVALID = 2,       /* a size, layout, mode or length is outside the contract */
+  FA_ERR_UNSUPPORTED = 3,         /* allowed by the pages but not built here (D not 64/128) */
+  FA_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes below the size query's answer */
+  FA_ERR_RUNTIME = 5,             /* a CUDA call failed (launch, copy, device query) */
+  FA_ERR_DEVICE_TIMEOUT = 6       /* a kernel's bounded wait expired; outputs are undefined */
+} fa_status;
+
+typedef enum { FA_LAYOUT_BNSD = 0, FA_LAYOUT_BSND = 1 } fa_layout;
+
+/* Mask modes, numbered as in FlashAttn guide §1.5 (0 = none, 3 = causal). */
+typedef enum { FA_MASK_NONE = 0, FA_MASK_CAUSAL = 3 } fa_mask_mode;
+
+/* Version of this ABI (FA_ABI_VERSION). */
+int fa_abi_version(void);
+
+/* Static text for a status code; never NULL. */
+const char* fa_status_string(int status);
+
+/* ---------------------------------------------------------------- prefill
+ * Workspace bytes fa_forward needs for these sizes (>= 256; holds the
+ * device status word and, when a key mask or lengths are given, a per-tile
+ * key-validity table). Pure host arithmetic; 0 when a size is negative. */
+size_t fa_forward_workspace_size(int64_t B, int64_t S_q, int64_t S_kv, int64_t num_heads,
+                                 int64_t num_kv_heads, int64_t D);
+
+/* Fused attention forward (prefill).
+ *   q    [B, num_heads, S_q, D] (BNSD) or [B, S_q, num_heads, D] (BSND), device bf16
+ *   k, v [B, num_kv_heads, S_kv, D] or [B, S_kv, num_kv_heads, D], device bf16
+ *   mask_mode           FA_MASK_NONE or FA_MASK_CAUSAL; causal keeps key j for
+ *                       query row i iff j <= i and requires S_q == S_kv
+ *   key_mask            NULL or device uint8 [B, S_kv] (nonzero = excluded)
+ *   actual_seq_lengths  NULL or HOST int64 [B], each in [0, S_kv]
+ *   scale               multiplies Q K^T before the softmax (finite)
+ *   out                 device bf16, shape and layout of q
+ *   lse                 NULL or device fp32 [B, num_heads, S_q]
+ *   workspace           device, >= fa_forward_workspace_size(...) bytes,
+ *                       256-byte aligned; contents need no initialisation
+ * B == 0 or S_q == 0 is a no-op returning FA_OK. S_kv == 0 makes every row
+ * invalid (out 0, lse +inf). */
+fa_status fa_forward(const void* q, const void* k, const void* v, int mask_mode,
+                     const uint8_t* key_mask, const int64_t* actual_seq_lengths, int64_t B,
+                     int64_t S_q, int64_t S_kv, int64_t num_heads, int64_t num_kv_heads,
+                     int64_t D, float scale, int layout, void* out, float* lse,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* ----------------------------------------------------------------- decode
+ * Workspace bytes fa_decode needs. num_splits as for fa_decode (0 = the
+ * split heuristic; the answer then covers any choice it can make).
+ * Pure host arithmetic; 0 when an argument is out of range. */
+size_t fa_decode_workspace_size(int64_t B, int64_t S_kv_max, int64_t num_heads,
+                                int64_t num_kv_heads, int64_t D, int num_splits);
+
+/* Incremental (decode) attention with Split-KV.
+ *   q    [B, num_heads, 1, D] (BNSD) or [B, 1, num_heads, D] (BSND): the same
+ *        memory either way, device bf16
+ *   k, v padded caches [B, num_kv_heads, S_kv_max, D] or [B, S_kv_max, num_kv_heads, D]
+ *   key_mask            NULL or device uint8 [B, S_kv_max] (nonzero = excluded)
+ *   actual_seq_lengths  HOST int64 [B], required, each in [0, S_kv_max]
+ *   num_splits          0: the library picks the KV chunk size from the SM
+ *                       count and the lengths; n > 0: chunks of
+ *                       ceil(S_kv_max / n) rows rounded up to a multiple of 64,
+ *                       so a full-length sequence is cut into about n chunks
+ *   out                 device bf16 [B, num_heads, D] (either layout)
+ *   lse                 NULL or device fp32 [B, num_heads]
+ *   workspace           device, >= fa_decode_workspace_size(..., num_splits)
+ *                       bytes, 256-byte aligned
+ * The lengths are read on the host during the call; a small table derived
+ * from them is copied into the workspace on `stream`. */
+fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                    const int64_t* actual_seq_lengths, int64_t B, int64_t S_kv_max,
+                    int64_t num_heads, int64_t num_kv_heads, int64_t D, float scale, int layout,
+                    int num_splits, void* out, float* lse, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/* The decode split plan for these arguments (pure host computation, no
+ * CUDA call): chunk_rows = KV rows per chunk, num_chunks = total (batch,
+ * chunk) work items, max_chunks = largest chunk count of any batch.
+ * num_sms is the SM count the plan is made for (fa_decode passes the
+ * device's). Aims at a few waves of equal chunks over the SMs, in the spirit
+ * of aclnnIncreFlashAttention guide §8.2 (split S2 when B*N2 is small) and
+ * §8.5 (balance by the actual lengths). */
+fa_status fa_decode_plan(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t num_kv_heads,
+                         const int64_t* actual_seq_lengths, int num_sms, int num_splits,
+                         int64_t* chunk_rows, int64_t* num_chunks, int64_t* max_chunks);
+
+/* ------------------------------------------------------------ diagnostics
+ * Synchronises `stream`, then reads and clears the device status word at
+ * the start of a workspace used by fa_forward / fa_decode. Returns FA_OK,
+ * FA_ERR_DEVICE_TIMEOUT (a bounded wait in a kernel expired) or
+ * FA_ERR_RUNTIME. */
+fa_status fa_workspace_status(void* workspace, void* stream);
+
+/* Self-test of the bounded-wait path: launches one CTA that waits on an
+ * mbarrier nothing ever arrives on, with a limit of timeout_ns. The kernel
+ * records FA_ERR_DEVICE_TIMEOUT's device code in the workspace's status
+ * word and returns; the context stays usable. Needs >= 256 workspace bytes. */
+fa_status fa_selftest_wait_timeout(void* workspace, uint64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,188 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads and
+exports every function include/fa.h declares, argument errors come back
+before any CUDA call, and the decode split plan behaves as documented."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from attention_forward_qk_gb300 import _lib
+from attention_forward_qk_gb300 import fa as F
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+# 16-byte aligned non-null stand-ins: validation must reject before touching them
+P = ctypes.c_void_p(0x10000)
+WS = ctypes.c_void_p(0x20000)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_forward_qk_gb300 import build as B
+    B.build()
+    return _lib.load()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_function(lib):
+    names = header_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_lib.SIGNATURES)
+
+
+def test_version_and_status_strings(lib):
+    assert lib.fa_abi_version() == 1
+    for s in range(7):
+        assert lib.fa_status_string(s)
+    assert b"unknown" in lib.fa_status_string(99)
+
+
+def test_workspace_sizes(lib):
+    a = lib.fa_forward_workspace_size(2, 8192, 8192, 64, 8, 128)
+    assert a >= 256 and a % 256 == 0
+    assert lib.fa_forward_workspace_size(-1, 1, 1, 1, 1, 64) == 0
+    d0 = lib.fa_decode_workspace_size(8, 8192, 32, 8, 128, 0)
+    d128 = lib.fa_decode_workspace_size(8, 8192, 32, 8, 128, 128)
+    d2 = lib.fa_decode_workspace_size(8, 8192, 32, 8, 128, 2)
+    assert d0 > 0 and d128 > 0 and d2 > 0
+    # partial outputs dominate: 8*32*splits*128 fp32
+    assert d128 >= 8 * 32 * 128 * 128 * 4
+    assert d2 < d128
+    assert lib.fa_decode_workspace_size(8, 8192, 32, 8, 128, -1) == 0
+
+
+def _fwd(lib, **kw):
+    args = dict(q=P, k=P, v=P, mask_mode=0, key_mask=None, lens=None, B=1, S_q=128, S_kv=128,
+                Hq=2, Hkv=2, D=64, scale=0.125, layout=0, out=P, lse=None, ws=WS,
+                ws_bytes=1 << 20, stream=None)
+    args.update(kw)
+    lens = args["lens"]
+    if lens is not None:
+        lens = (ctypes.c_int64 * len(lens))(*lens)
+    return lib.fa_forward(args["q"], args["k"], args["v"], args["mask_mode"], args["key_mask"],
+                          lens, args["B"], args["S_q"], args["S_kv"], args["Hq"], args["Hkv"],
+                          args["D"], args["scale"], args["layout"], args["out"], args["lse"],
+                          args["ws"], args["ws_bytes"], args["stream"])
+
+
+def _dec(lib, **kw):
+    args = dict(q=P, k=P, v=P, key_mask=None, lens=[100, 7], B=2, S=128, Hq=8, Hkv=2, D=128,
+                scale=0.1, layout=0, splits=0, out=P, lse=None, ws=WS, ws_bytes=1 << 22,
+                stream=None)
+    args.update(kw)
+    lens = args["lens"]
+    if lens is not None:
+        lens = (ctypes.c_int64 * max(len(lens), 1))(*lens)
+    return lib.fa_decode(args["q"], args["k"], args["v"], args["key_mask"], lens, args["B"],
+                         args["S"], args["Hq"], args["Hkv"], args["D"], args["scale"],
+                         args["layout"], args["splits"], args["out"], args["lse"], args["ws"],
+                         args["ws_bytes"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), _lib.FA_ERR_NULLPTR),
+    (dict(out=None), _lib.FA_ERR_NULLPTR),
+    (dict(ws=None), _lib.FA_ERR_NULLPTR),
+    (dict(Hq=3, Hkv=2), _lib.FA_ERR_PARAM_INVALID),
+    (dict(D=96), _lib.FA_ERR_UNSUPPORTED),
+    (dict(D=256), _lib.FA_ERR_UNSUPPORTED),
+    (dict(layout=2), _lib.FA_ERR_PARAM_INVALID),
+    (dict(mask_mode=4), _lib.FA_ERR_PARAM_INVALID),
+    (dict(mask_mode=3, S_q=64, S_kv=128), _lib.FA_ERR_PARAM_INVALID),
+    (dict(B=-1), _lib.FA_ERR_PARAM_INVALID),
+    (dict(scale=float("nan")), _lib.FA_ERR_PARAM_INVALID),
+    (dict(q=ctypes.c_void_p(0x10008)), _lib.FA_ERR_PARAM_INVALID),
+    (dict(ws=ctypes.c_void_p(0x20010)), _lib.FA_ERR_PARAM_INVALID),
+    (dict(lens=[129]), _lib.FA_ERR_PARAM_INVALID),
+    (dict(lens=[-1]), _lib.FA_ERR_PARAM_INVALID),
+    (dict(ws_bytes=16), _lib.FA_ERR_WORKSPACE_TOO_SMALL),
+])
+def test_forward_rejects_before_any_cuda_call(lib, kw, expect):
+    assert _fwd(lib, **kw) == expect
+
+
+def test_forward_noop_shapes_return_ok(lib):
+    assert _fwd(lib, B=0) == _lib.FA_OK
+    assert _fwd(lib, S_q=0, S_kv=5) == _lib.FA_OK
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(lens=None), _lib.FA_ERR_NULLPTR),
+    (dict(v=None), _lib.FA_ERR_NULLPTR),
+    (dict(Hq=8, Hkv=3), _lib.FA_ERR_PARAM_INVALID),
+    (dict(D=32), _lib.FA_ERR_UNSUPPORTED),
+    (dict(lens=[129, 1]), _lib.FA_ERR_PARAM_INVALID),
+    (dict(splits=-2), _lib.FA_ERR_PARAM_INVALID),
+    (dict(ws_bytes=1024), _lib.FA_ERR_WORKSPACE_TOO_SMALL),
+    (dict(layout=7), _lib.FA_ERR_PARAM_INVALID),
+])
+def test_decode_rejects_before_any_cuda_call(lib, kw, expect):
+    assert _dec(lib, **kw) == expect
+
+
+def test_decode_zero_batch_is_noop(lib):
+    assert _dec(lib, B=0, lens=[]) == _lib.FA_OK
+
+
+def _plan(lens, S, Hq, Hkv, sms=152, splits=0):
+    return F.fa_decode_plan(lens, S, Hq, Hkv, sms, splits)
+
+
+def test_plan_covers_every_row_with_equal_chunks(lib):
+    import random
+    rng = random.Random(5)
+    for _ in range(50):
+        B = rng.randint(1, 16)
+        S = rng.randint(1, 20000)
+        lens = [rng.randint(0, S) for _ in range(B)]
+        Hkv = rng.choice([1, 2, 8, 32])
+        Hq = Hkv * rng.choice([1, 2, 4, 8])
+        chunk, n, mx = _plan(lens, S, Hq, Hkv)
+        assert chunk % 64 == 0 and chunk >= 128
+        assert n == sum(math.ceil(L / chunk) for L in lens)
+        assert mx == max(math.ceil(L / chunk) for L in lens)
+        assert mx <= math.ceil(S / 128)  # fits the size query's bound
+
+
+def test_plan_targets_a_few_waves():
+    # GQA decode workload shape: 8 x 8 KV heads, lengths ~U[1024, 8192]
+    lens = [1024, 8192, 4000, 6000, 3000, 7777, 2048, 5000]
+    chunk, n, _ = _plan(lens, 8192, 32, 8)
+    ctas = n * 8
+    assert 2 * 152 <= ctas <= 8 * 152
+    # one long sequence, 32 heads: split so every SM gets work
+    chunk, n, _ = _plan([131072], 131072, 32, 32)
+    assert n * 32 >= 152 * 2
+
+
+def test_plan_with_forced_splits():
+    chunk, n, mx = _plan([131072], 131072, 32, 32, splits=128)
+    assert (chunk, n, mx) == (1024, 128, 128)
+    chunk, n, mx = _plan([131072], 131072, 32, 32, splits=1024)
+    assert (chunk, n, mx) == (128, 1024, 1024)
+    chunk, n, mx = _plan([1000, 0], 1000, 4, 4, splits=3)
+    assert chunk == 384 and n == 3 and mx == 3
+
+
+def test_plan_zero_lengths():
+    chunk, n, mx = _plan([0, 0, 0], 4096, 8, 8)
+    assert n == 0 and mx == 0
+
+
+def test_plan_rejects_bad_args(lib):
+    with pytest.raises(_lib.FaError):
+        _plan([5], 4, 8, 8)          # length above the cache
+    with pytest.raises(_lib.FaError):
+        _plan([5], 8, 8, 3)          # heads not a multiple
+    with pytest.raises(_lib.FaError):
+        _plan([5], 8, 8, 8, sms=0)
