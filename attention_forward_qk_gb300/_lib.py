@@ -45,6 +45,8 @@ SIGNATURES = {
                                       ctypes.POINTER(_i64)]),
     "fa_workspace_status": (ctypes.c_int, [_vp, _vp]),
     "fa_selftest_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_uint64, _vp]),
+    "fa_set_main_kernel_events": (None, [_vp, _vp]),
+    "fa_kernel_launch_count": (ctypes.c_uint64, []),
 }
 
 _lock = threading.Lock()

@@ -13,6 +13,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -123,6 +124,20 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int layout, int64_t B, 
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
+thread_local cudaEvent_t tl_before = nullptr;
+thread_local cudaEvent_t tl_after = nullptr;
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+void main_kernel_begin(cudaStream_t stream) {
+  if (tl_before != nullptr && tl_after != nullptr) cudaEventRecord(tl_before, stream);
+}
+void main_kernel_end(cudaStream_t stream) {
+  if (tl_before != nullptr && tl_after != nullptr) cudaEventRecord(tl_after, stream);
+}
+void count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
 
 int device_sm_count() {
   static std::mutex mu;
@@ -270,6 +285,7 @@ fa_status fa_forward(const void* q, const void* k, const void* v, int mask_mode,
     if (launch_tile_bits(key_mask, lens_dev, static_cast<int>(B), static_cast<int>(S_kv),
                          bits_dev, s) != cudaSuccess)
       return FA_ERR_RUNTIME;
+    count_launches(1);
     bits = bits_dev;
   }
   PrefillLaunch x;
@@ -290,7 +306,12 @@ fa_status fa_forward(const void* q, const void* k, const void* v, int mask_mode,
   x.lse = lse;
   x.status = reinterpret_cast<uint32_t*>(wsb);
   x.timeout_ns = kDefaultTimeoutNs;
-  return launch_prefill(x, s) == cudaSuccess ? FA_OK : FA_ERR_RUNTIME;
+  main_kernel_begin(s);
+  const cudaError_t e = launch_prefill(x, s);
+  main_kernel_end(s);
+  if (e != cudaSuccess) return FA_ERR_RUNTIME;
+  count_launches(1);
+  return FA_OK;
 }
 
 fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* key_mask,
@@ -383,9 +404,17 @@ fa_status fa_selftest_wait_timeout(void* workspace, uint64_t timeout_ns, void* s
   if (timeout_ns == 0 || timeout_ns > 10000000000ull) return FA_ERR_PARAM_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return FA_ERR_RUNTIME;
-  return launch_wait_probe(static_cast<uint32_t*>(workspace), timeout_ns, s) == cudaSuccess
-             ? FA_OK
-             : FA_ERR_RUNTIME;
+  if (launch_wait_probe(static_cast<uint32_t*>(workspace), timeout_ns, s) != cudaSuccess)
+    return FA_ERR_RUNTIME;
+  count_launches(1);
+  return FA_OK;
 }
+
+void fa_set_main_kernel_events(void* before, void* after) {
+  tl_before = static_cast<cudaEvent_t>(before);
+  tl_after = static_cast<cudaEvent_t>(after);
+}
+
+uint64_t fa_kernel_launch_count(void) { return g_launches.load(); }
 
 }  // extern "C"

@@ -427,9 +427,12 @@ cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
     da.max_chunks = x.max_chunks;
     da.head_groups = g_total / G;
     da.scale_log2 = x.scale * 1.4426950408889634f;
+    main_kernel_begin(stream);
     cudaError_t e = (x.D == 128) ? launch_chunks_g<128>(G, x, mk, mv, da, stream)
                                  : launch_chunks_g<64>(G, x, mk, mv, da, stream);
+    main_kernel_end(stream);
     if (e != cudaSuccess) return e;
+    count_launches(1);
   }
   MergeArgs ma;
   ma.part_o = x.part_o;
@@ -444,7 +447,9 @@ cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
     decode_merge_kernel<128><<<x.B * x.Hq, kMergeThreads, 0, stream>>>(ma);
   else
     decode_merge_kernel<64><<<x.B * x.Hq, kMergeThreads, 0, stream>>>(ma);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launches(1);
+  return e;
 }
 
 }  // namespace fa

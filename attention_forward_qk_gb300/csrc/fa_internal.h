@@ -59,6 +59,12 @@ cudaError_t launch_tile_bits(const uint8_t* key_mask, const int* lens_dev, int B
 
 cudaError_t launch_wait_probe(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 
+// Diagnostics: events recorded around the main kernel (thread-local, may be
+// null) and a process-wide count of kernel launches.
+void main_kernel_begin(cudaStream_t stream);
+void main_kernel_end(cudaStream_t stream);
+void count_launches(int n);
+
 // Default bounded-wait limit of the kernels (nanoseconds).
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 

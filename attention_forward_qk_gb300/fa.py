@@ -175,3 +175,18 @@ def fa_workspace_status(workspace, stream=None) -> int:
 def fa_selftest_wait_timeout(workspace, timeout_ns: int, stream=None) -> int:
     return int(_lib.load().fa_selftest_wait_timeout(workspace.data_ptr(), int(timeout_ns),
                                                     _stream_ptr(stream)))
+
+
+def fa_set_main_kernel_events(before, after) -> None:
+    """Record torch.cuda.Event `before`/`after` around the main kernel of every
+    later call from this thread (None, None turns it off). Each event must
+    have been recorded once by torch so that its handle exists."""
+    if before is None or after is None:
+        _lib.load().fa_set_main_kernel_events(None, None)
+        return
+    _lib.load().fa_set_main_kernel_events(ctypes.c_void_p(before.cuda_event),
+                                          ctypes.c_void_p(after.cuda_event))
+
+
+def fa_kernel_launch_count() -> int:
+    return int(_lib.load().fa_kernel_launch_count())

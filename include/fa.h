@@ -162,6 +162,18 @@ fa_status fa_workspace_status(void* workspace, void* stream);
  * word and returns; the context stays usable. Needs >= 256 workspace bytes. */
 fa_status fa_selftest_wait_timeout(void* workspace, uint64_t timeout_ns, void* stream);
 
+/* Diagnostics for measurement. When both handles are non-NULL, every later
+ * fa_forward / fa_decode call made from this host thread records `before`
+ * (a cudaEvent_t) on its stream immediately before launching its main
+ * kernel (the prefill kernel, or the decode stage-1 kernel) and `after`
+ * immediately after it, so the pair times that kernel alone on the stream it
+ * runs on. Passing NULL, NULL turns the hooks off. The events stay owned by
+ * the caller. */
+void fa_set_main_kernel_events(void* before, void* after);
+
+/* Number of kernels this library has launched in this process so far. */
+uint64_t fa_kernel_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif
