@@ -40,7 +40,7 @@ SIGNATURES = {
     "fa_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                                  ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _sz,
                                  _vp]),
-    "fa_decode_plan": (ctypes.c_int, [_i64, _i64, _i64, _i64, _vp, ctypes.c_int, ctypes.c_int,
+    "fa_decode_plan": (ctypes.c_int, [_i64, _i64, _i64, _i64, _i64, _vp, ctypes.c_int, ctypes.c_int,
                                       ctypes.POINTER(_i64), ctypes.POINTER(_i64),
                                       ctypes.POINTER(_i64)]),
     "fa_workspace_status": (ctypes.c_int, [_vp, _vp]),

@@ -33,11 +33,6 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// query heads per CTA in the decode stage-1 kernel (largest of 8/4/2/1 dividing g)
-int decode_heads_per_cta(int64_t g) {
-  return (g % 8 == 0) ? 8 : (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1;
-}
-
 struct DecodeWs {
   size_t lens, items, part_lse, part_o, total;
 };
@@ -186,14 +181,15 @@ size_t fa_forward_workspace_size(int64_t B, int64_t S_q, int64_t S_kv, int64_t n
 }
 
 fa_status fa_decode_plan(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t num_kv_heads,
-                         const int64_t* lens, int num_sms, int num_splits, int64_t* chunk_rows,
-                         int64_t* num_chunks, int64_t* max_chunks) {
+                         int64_t D, const int64_t* lens, int num_sms, int num_splits,
+                         int64_t* chunk_rows, int64_t* num_chunks, int64_t* max_chunks) {
   if (lens == nullptr || chunk_rows == nullptr || num_chunks == nullptr || max_chunks == nullptr)
     return FA_ERR_NULLPTR;
   if (num_kv_heads == 0) num_kv_heads = num_heads;
   if (B < 0 || S_kv_max < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
       num_heads % num_kv_heads != 0 || num_splits < 0 || num_sms <= 0 || S_kv_max > kMaxDim)
     return FA_ERR_PARAM_INVALID;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
   int64_t total = 0;
   for (int64_t b = 0; b < B; ++b) {
     if (lens[b] < 0 || lens[b] > S_kv_max) return FA_ERR_PARAM_INVALID;
@@ -206,7 +202,7 @@ fa_status fa_decode_plan(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t
     // Spread the valid rows of every (batch, KV head, head group) over about
     // kWaves CTAs per SM, in equal multiples of 64 rows.
     const int64_t g = num_heads / num_kv_heads;
-    const int64_t per_row = num_kv_heads * (g / decode_heads_per_cta(g));
+    const int64_t per_row = num_kv_heads * (g / decode_heads_per_cta(g, D));
     const int64_t target = static_cast<int64_t>(kWaves) * num_sms;
     chunk = ceil_div(std::max<int64_t>(total * per_row, 1), target);
     chunk = ceil_div(chunk, kChunkQuant) * kChunkQuant;
@@ -338,7 +334,7 @@ fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* 
   const int sms = device_sm_count();
   if (sms <= 0) return FA_ERR_RUNTIME;
   int64_t chunk = 0, n_items = 0, max_chunks = 0;
-  st = fa_decode_plan(B, S_kv_max, num_heads, Hkv, lens, sms, num_splits, &chunk, &n_items,
+  st = fa_decode_plan(B, S_kv_max, num_heads, Hkv, D, lens, sms, num_splits, &chunk, &n_items,
                       &max_chunks);
   if (st != FA_OK) return st;
   const int64_t slots = std::max<int64_t>(max_chunks, 1);

@@ -3,8 +3,9 @@
 // Stage 1 (decode_chunk_kernel): one CTA per (batch, chunk of KV rows,
 // KV head [, group of query heads]). A producer warp streams the chunk's K
 // and V rows through a 4-stage shared-memory ring with TMA tensor loads;
-// eight consumer warps compute q.k with 128-bit shared loads and butterfly
-// shuffles (every query head of the GQA group reuses the same K/V row), keep
+// seven consumer warps compute q.k with 128-bit shared loads, packed f32x2
+// FMAs and butterfly shuffles over the 8 lanes that share a row (every query
+// head of the GQA group reuses the same K/V row), keep
 // an online softmax (running max m and sum l, exp2 domain) per head and
 // accumulate p*v. The chunk's normalised partial output o/l and its
 // log-sum-exp are written to the workspace. This is the FlashDecoding
@@ -30,18 +31,21 @@
 namespace fa {
 namespace {
 
-constexpr int kDecWarps = 8;                       // consumer warps
+// 7 consumer warps + 1 producer warp: 256 threads keeps the per-thread
+// register budget at 255 (larger CTAs are capped at 168).
+constexpr int kDecWarps = 7;                       // consumer warps
 constexpr int kDecThreads = (kDecWarps + 1) * 32;  // + one producer warp
 constexpr int kDecStages = 4;
-constexpr int kDecStageBytes = 32768;              // K rows + V rows of one stage
+constexpr int kDecStageBytes = 28672;              // K rows + V rows of one stage
 constexpr int kDecSmemBytes = kDecStages * kDecStageBytes + 256;
 constexpr int kMergeThreads = 256;
 
 template <int D>
 struct DecCfg {
-  static constexpr int LPR = D / 8;                     // lanes per row: 16 B of the row each
+  static constexpr int LPR = 8;                         // lanes per K/V row
+  static constexpr int NCH = D / 64;                    // 16-byte chunks of a row per lane
   static constexpr int RPW = 32 / LPR;                  // rows per warp per step
-  static constexpr int R = kDecStageBytes / (2 * D * 2);  // rows per stage
+  static constexpr int R = kDecStageBytes / (2 * D * 2);  // rows per stage (56 or 112)
   static constexpr int RPWS = R / kDecWarps;            // rows per warp per stage
   static constexpr int STEPS = RPWS / RPW;
   static constexpr int TILE_BYTES = R * D * 2;
@@ -59,17 +63,6 @@ struct DecodeArgs {
   int Hq, Hkv, S_kv, chunk, max_chunks, head_groups;
   float scale_log2;
 };
-
-__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
-  f[0] = bf16lo_to_f32(u.x);
-  f[1] = bf16hi_to_f32(u.x);
-  f[2] = bf16lo_to_f32(u.y);
-  f[3] = bf16hi_to_f32(u.y);
-  f[4] = bf16lo_to_f32(u.z);
-  f[5] = bf16hi_to_f32(u.z);
-  f[6] = bf16lo_to_f32(u.w);
-  f[7] = bf16hi_to_f32(u.w);
-}
 
 template <int D, int G>
 __global__ void __launch_bounds__(kDecThreads, 1)
@@ -110,16 +103,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   }
   __syncthreads();
 
-  // per-lane softmax state (consumers)
-  float m[G], l[G], o[G][8];
+  // per-lane softmax state (consumers); o holds this lane's 8*NCH elements
+  // of every head's output as fp32 pairs
+  constexpr int NP = 4 * C::NCH;  // fp32 pairs per lane
+  float m[G], l[G];
+  uint64_t o[G][NP];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     m[h] = -INFINITY;
     l[h] = 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) o[h][k] = 0.f;
+    for (int k = 0; k < NP; ++k) o[h][k] = 0ull;
   }
-  const int sub = lane % C::LPR;  // which 8 elements of a row this lane owns
+  const int sub = lane % C::LPR;  // this lane owns 16-byte chunks sub, sub+8, ... of a row
   const int rg = lane / C::LPR;   // row group within a warp step
 
   if (warp == kDecWarps) {
@@ -150,14 +146,21 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
   } else {
     // ----------------------------------------------------------- consumers
-    float qf[G][8];
+    uint64_t qp[G][NP];  // q * scale * log2(e), as fp32 pairs
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const uint4 u =
-          *reinterpret_cast<const uint4*>(a.q + (static_cast<size_t>(b) * a.Hq + h0 + h) * D + sub * 8);
-      unpack8(u, qf[h]);
+      const __nv_bfloat16* qh = a.q + (static_cast<size_t>(b) * a.Hq + h0 + h) * D;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) qf[h][k] *= a.scale_log2;
+      for (int ch = 0; ch < C::NCH; ++ch) {
+        const uint4 u = *reinterpret_cast<const uint4*>(qh + (sub + 8 * ch) * 8);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float lo = bf16lo_to_f32(w4[k]) * a.scale_log2;
+          const float hi = bf16hi_to_f32(w4[k]) * a.scale_log2;
+          qp[h][ch * 4 + k] = pair_f32(lo, hi);
+        }
+      }
     }
     const uint8_t* mask_row =
         a.key_mask ? a.key_mask + static_cast<size_t>(b) * a.S_kv : nullptr;
@@ -181,14 +184,22 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         bool ok = gr < row_end;
         if (ok && mask_row != nullptr) ok = mask_row[gr] == 0;
         valid[i] = ok;
-        const uint4 u = *reinterpret_cast<const uint4*>(Ks + r * D + sub * 8);
-        float kf[8];
-        unpack8(u, kf);
+        uint64_t kp[NP];
+#pragma unroll
+        for (int ch = 0; ch < C::NCH; ++ch) {
+          const uint4 u = *reinterpret_cast<const uint4*>(Ks + r * D + (sub + 8 * ch) * 8);
+          kp[ch * 4 + 0] = bf16x2_pair(u.x);
+          kp[ch * 4 + 1] = bf16x2_pair(u.y);
+          kp[ch * 4 + 2] = bf16x2_pair(u.z);
+          kp[ch * 4 + 3] = bf16x2_pair(u.w);
+        }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          float acc = 0.f;
+          uint64_t acc2 = 0ull;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) acc = fmaf(qf[h][k], kf[k], acc);
+          for (int k = 0; k < NP; ++k) acc2 = ffma2(qp[h][k], kp[k], acc2);
+          const float2 a2 = unpair(acc2);
+          float acc = a2.x + a2.y;
 #pragma unroll
           for (int off = C::LPR / 2; off > 0; off >>= 1)
             acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -206,8 +217,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const float alpha = ex2(m[h] - m_use);  // 0 when m was -inf
         m[h] = mn;
         l[h] *= alpha;
+        const uint64_t a2 = pair_f32(alpha, alpha);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) o[h][k] *= alpha;
+        for (int k = 0; k < NP; ++k) o[h][k] = ffma2(o[h][k], a2, 0ull);
 #pragma unroll
         for (int i = 0; i < C::STEPS; ++i) {
           s[i][h] = ex2(s[i][h] - m_use);  // -inf -> 0
@@ -217,14 +229,22 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
       for (int i = 0; i < C::STEPS; ++i) {
         const int r = warp * C::RPWS + i * C::RPW + rg;
-        uint4 u = *reinterpret_cast<const uint4*>(Vs + r * D + sub * 8);
-        if (!valid[i]) u = make_uint4(0u, 0u, 0u, 0u);  // stale rows never enter a product
-        float vf[8];
-        unpack8(u, vf);
+        uint64_t vp[NP];
 #pragma unroll
-        for (int h = 0; h < G; ++h)
+        for (int ch = 0; ch < C::NCH; ++ch) {
+          uint4 u = *reinterpret_cast<const uint4*>(Vs + r * D + (sub + 8 * ch) * 8);
+          if (!valid[i]) u = make_uint4(0u, 0u, 0u, 0u);  // stale rows never enter a product
+          vp[ch * 4 + 0] = bf16x2_pair(u.x);
+          vp[ch * 4 + 1] = bf16x2_pair(u.y);
+          vp[ch * 4 + 2] = bf16x2_pair(u.z);
+          vp[ch * 4 + 3] = bf16x2_pair(u.w);
+        }
 #pragma unroll
-          for (int k = 0; k < 8; ++k) o[h][k] = fmaf(s[i][h], vf[k], o[h][k]);
+        for (int h = 0; h < G; ++h) {
+          const uint64_t p2 = pair_f32(s[i][h], s[i][h]);
+#pragma unroll
+          for (int k = 0; k < NP; ++k) o[h][k] = ffma2(p2, vp[k], o[h][k]);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * slot);
@@ -243,9 +263,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const float a2 = ex2(m2 - m_use);
         l[h] = l[h] * a1 + l2 * a2;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float o2 = __shfl_xor_sync(0xffffffffu, o[h][k], off);
-          o[h][k] = o[h][k] * a1 + o2 * a2;
+        for (int k = 0; k < NP; ++k) {
+          const float2 mine = unpair(o[h][k]);
+          const float ox = __shfl_xor_sync(0xffffffffu, mine.x, off);
+          const float oy = __shfl_xor_sync(0xffffffffu, mine.y, off);
+          o[h][k] = pair_f32(mine.x * a1 + ox * a2, mine.y * a1 + oy * a2);
         }
         m[h] = mn;
       }
@@ -265,7 +287,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         sm_l[warp * G + h] = l[h];
       }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) sm_o[(warp * G + h) * D + sub * 8 + k] = o[h][k];
+      for (int ch = 0; ch < C::NCH; ++ch)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 v2 = unpair(o[h][ch * 4 + k]);
+          float* dst = sm_o + (warp * G + h) * D + (sub + 8 * ch) * 8 + 2 * k;
+          dst[0] = v2.x;
+          dst[1] = v2.y;
+        }
     }
   }
   __syncthreads();
@@ -391,7 +420,9 @@ template <int D>
 cudaError_t launch_chunks_g(int G, const DecodeLaunch& x, const CUtensorMap& mk,
                             const CUtensorMap& mv, const DecodeArgs& da, cudaStream_t s) {
   switch (G) {
-    case 8: return launch_chunks<D, 8>(x, mk, mv, da, s);
+    case 8:
+      if constexpr (D == 64) return launch_chunks<D, 8>(x, mk, mv, da, s);
+      return cudaErrorInvalidValue;
     case 4: return launch_chunks<D, 4>(x, mk, mv, da, s);
     case 2: return launch_chunks<D, 2>(x, mk, mv, da, s);
     default: return launch_chunks<D, 1>(x, mk, mv, da, s);
@@ -402,7 +433,7 @@ cudaError_t launch_chunks_g(int G, const DecodeLaunch& x, const CUtensorMap& mk,
 
 cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
   const int g_total = x.Hq / x.Hkv;
-  const int G = (g_total % 8 == 0) ? 8 : (g_total % 4 == 0) ? 4 : (g_total % 2 == 0) ? 2 : 1;
+  const int G = decode_heads_per_cta(g_total, x.D);
   if (x.num_items > 0) {
     CUtensorMap mk, mv;
     const int R = (x.D == 128) ? DecCfg<128>::R : DecCfg<64>::R;

@@ -17,6 +17,13 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int layout, int64_t B, 
 
 int device_sm_count();  // of the current device; 0 on failure
 
+// Query heads one decode stage-1 CTA handles: the largest of 8/4/2/1 that
+// divides the GQA group size g (at most 4 for D = 128, to stay in registers).
+inline int decode_heads_per_cta(int64_t g, int64_t D) {
+  if (D == 64 && g % 8 == 0) return 8;
+  return (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1;
+}
+
 struct DecodeLaunch {
   const void* q;
   const void* k;

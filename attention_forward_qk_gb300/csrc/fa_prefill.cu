@@ -123,13 +123,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  // ---- work tile: heaviest (last) query pairs first
-  const int bh_count = a.B * a.Hq;
-  const int qp = a.n_qpairs - 1 - static_cast<int>(blockIdx.x) / bh_count;
-  const int bh = static_cast<int>(blockIdx.x) % bh_count;
-  const int b = bh / a.Hq;
-  const int h = bh % a.Hq;
-  const int kvh = h / (a.Hq / a.Hkv);
+  // ---- work tile. Consecutive CTAs share one (batch, KV head): all query
+  // pairs of its g query heads, heaviest (last) pairs first, heads innermost,
+  // so the CTAs resident at any time read the same K/V tiles out of L2.
+  const int g = a.Hq / a.Hkv;
+  const int per_kv = a.n_qpairs * g;
+  const int bkv = static_cast<int>(blockIdx.x) / per_kv;
+  const int rem = static_cast<int>(blockIdx.x) % per_kv;
+  const int qp = a.n_qpairs - 1 - rem / g;
+  const int b = bkv / a.Hkv;
+  const int kvh = bkv % a.Hkv;
+  const int h = kvh * g + rem % g;
   const int q_row0 = qp * 2 * kBM;
   const bool has_t1 = q_row0 + kBM < a.S_q;
   // KV tiles each Q tile needs (a prefix of the tile sequence)
@@ -386,16 +390,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmax = fmaxf(tmax, tv);
           }
         }
-      } else {
-        float smax = -INFINITY, smin = INFINITY;
+      } else if (c >= 0.f) {
+        float mx = -INFINITY;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            smax = fmaxf(smax, __uint_as_float(sr[q4][i]));
-            smin = fminf(smin, __uint_as_float(sr[q4][i]));
-          }
-        tmax = (c >= 0.f) ? smax * c : smin * c;
+          for (int i = 0; i < 32; i += 2)
+            mx = fmax3(mx, __uint_as_float(sr[q4][i]), __uint_as_float(sr[q4][i + 1]));
+        tmax = mx * c;
+      } else {
+        float mn = INFINITY;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int i = 0; i < 32; i += 2)
+            mn = fmin3(mn, __uint_as_float(sr[q4][i]), __uint_as_float(sr[q4][i + 1]));
+        tmax = mn * c;
       }
       // conditional rescale: keep the reference max unless it grows by > 2^8
       const float m_cand = fmaxf(m_run, tmax);
@@ -406,7 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_run = m_cand;
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      float rsum = 0.f;
+      // p = 2^(s*c - m): packed f32x2 FMA, then ex2; row sum in two packed lanes
+      uint64_t rs2 = 0ull;
+      const uint64_t c2 = masked ? pair_f32(1.f, 1.f) : pair_f32(c, c);
+      const uint64_t nm2 = pair_f32(-m_use, -m_use);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
@@ -415,20 +428,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int q4 = half * 2 + qq;
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            float p0, p1;
-            if (masked) {
-              p0 = ex2(__uint_as_float(sr[q4][i]) - m_use);
-              p1 = ex2(__uint_as_float(sr[q4][i + 1]) - m_use);
-            } else {
-              p0 = ex2(fmaf(__uint_as_float(sr[q4][i]), c, -m_use));
-              p1 = ex2(fmaf(__uint_as_float(sr[q4][i + 1]), c, -m_use));
-            }
-            rsum += p0 + p1;
+            const float2 t2 = unpair(ffma2(pair_u32(sr[q4][i], sr[q4][i + 1]), c2, nm2));
+            const float p0 = ex2(t2.x);
+            const float p1 = ex2(t2.y);
+            rs2 = fadd2(rs2, pair_f32(p0, p1));
             pk[qq * 16 + i / 2] = pack_bf16x2(p0, p1);
           }
         }
         tmem_st32(s_tmem + half * 32, pk);  // P overwrites S columns already read
       }
+      const float2 rsp = unpair(rs2);
+      const float rsum = rsp.x + rsp.y;
       l_run = l_run * alpha + rsum;
       if (k > 0 && __any_sync(0xffffffffu, need)) {
         // O_t was complete when S_t(j) landed (tcgen05 ops retire in order)

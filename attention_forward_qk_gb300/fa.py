@@ -79,12 +79,13 @@ def fa_decode_workspace_size(B, S_kv_max, num_heads, num_kv_heads, D, num_splits
                                                     num_splits))
 
 
-def fa_decode_plan(actual_seq_lengths, S_kv_max, num_heads, num_kv_heads, num_sms, num_splits=0):
+def fa_decode_plan(actual_seq_lengths, S_kv_max, num_heads, num_kv_heads, D, num_sms,
+                   num_splits=0):
     """(chunk_rows, num_chunks, max_chunks) of the decode split plan (host only)."""
     B = len(actual_seq_lengths)
     arr, _ = _lens_array(actual_seq_lengths, B)
     c, n, m = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
-    st = _lib.load().fa_decode_plan(B, S_kv_max, num_heads, num_kv_heads, arr, num_sms,
+    st = _lib.load().fa_decode_plan(B, S_kv_max, num_heads, num_kv_heads, D, arr, num_sms,
                                     num_splits, ctypes.byref(c), ctypes.byref(n), ctypes.byref(m))
     check(st, "fa_decode_plan")
     return c.value, n.value, m.value

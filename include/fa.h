@@ -146,8 +146,9 @@ fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* 
  * of aclnnIncreFlashAttention guide §8.2 (split S2 when B*N2 is small) and
  * §8.5 (balance by the actual lengths). */
 fa_status fa_decode_plan(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t num_kv_heads,
-                         const int64_t* actual_seq_lengths, int num_sms, int num_splits,
-                         int64_t* chunk_rows, int64_t* num_chunks, int64_t* max_chunks);
+                         int64_t D, const int64_t* actual_seq_lengths, int num_sms,
+                         int num_splits, int64_t* chunk_rows, int64_t* num_chunks,
+                         int64_t* max_chunks);
 
 /* ------------------------------------------------------------ diagnostics
  * Synchronises `stream`, then reads and clears the device status word at

@@ -134,8 +134,8 @@ def test_decode_zero_batch_is_noop(lib):
     assert _dec(lib, B=0, lens=[]) == _lib.FA_OK
 
 
-def _plan(lens, S, Hq, Hkv, sms=152, splits=0):
-    return F.fa_decode_plan(lens, S, Hq, Hkv, sms, splits)
+def _plan(lens, S, Hq, Hkv, sms=152, splits=0, D=128):
+    return F.fa_decode_plan(lens, S, Hq, Hkv, D, sms, splits)
 
 
 def test_plan_covers_every_row_with_equal_chunks(lib):
@@ -147,7 +147,7 @@ def test_plan_covers_every_row_with_equal_chunks(lib):
         lens = [rng.randint(0, S) for _ in range(B)]
         Hkv = rng.choice([1, 2, 8, 32])
         Hq = Hkv * rng.choice([1, 2, 4, 8])
-        chunk, n, mx = _plan(lens, S, Hq, Hkv)
+        chunk, n, mx = _plan(lens, S, Hq, Hkv, D=rng.choice([64, 128]))
         assert chunk % 64 == 0 and chunk >= 128
         assert n == sum(math.ceil(L / chunk) for L in lens)
         assert mx == max(math.ceil(L / chunk) for L in lens)
@@ -186,3 +186,5 @@ def test_plan_rejects_bad_args(lib):
         _plan([5], 8, 8, 3)          # heads not a multiple
     with pytest.raises(_lib.FaError):
         _plan([5], 8, 8, 8, sms=0)
+    with pytest.raises(_lib.FaError):
+        _plan([5], 8, 8, 8, D=96)
