@@ -23,9 +23,7 @@ namespace fa {
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int kMinChunk = 128;   // smallest chunk the split heuristic picks
-constexpr int kChunkQuant = 64;  // chunk sizes are multiples of this
-constexpr int kWaves = 4;        // heuristic target: about this many CTAs per SM
+constexpr int kChunkQuant = 64;  // forced-split chunk sizes are multiples of this
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -33,23 +31,36 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+int64_t chunk_for_splits(int64_t S_kv_max, int num_splits) {
+  int64_t c = ceil_div(S_kv_max, num_splits);
+  c = ceil_div(c, kChunkQuant) * kChunkQuant;
+  return std::max<int64_t>(c, kChunkQuant);
+}
+
 struct DecodeWs {
-  size_t lens, items, part_lse, part_o, total;
+  size_t prefix, part_lse, part_o, total;
 };
 
-DecodeWs decode_ws(int64_t B, int64_t Hq, int64_t D, int64_t max_chunks) {
+// [status | pad][length prefix sums, large batches only][partial lse][partial o]
+DecodeWs decode_ws(int64_t B, int64_t Hq, int64_t D, int64_t max_slots) {
   DecodeWs w;
   size_t off = kAlign;  // status word
-  w.lens = off;
-  off += align_up(sizeof(int32_t) * B);
-  w.items = off;
-  off += align_up(sizeof(int32_t) * 2 * B * max_chunks);
+  w.prefix = off;
+  off += align_up(sizeof(int64_t) * (B + 1));
   w.part_lse = off;
-  off += align_up(sizeof(float) * B * Hq * max_chunks);
+  off += align_up(sizeof(float) * B * Hq * max_slots);
   w.part_o = off;
-  off += align_up(sizeof(float) * B * Hq * max_chunks * D);
+  off += align_up(sizeof(float) * B * Hq * max_slots * D);
   w.total = off;
   return w;
+}
+
+// Upper bound of the pieces one sequence is cut into, for the size query.
+int64_t max_slots_bound(int64_t S_kv_max, int num_splits) {
+  const int64_t S = std::max<int64_t>(S_kv_max, 1);
+  const int64_t rc = num_splits > 0 ? chunk_for_splits(S, num_splits)
+                                    : static_cast<int64_t>(kDecodeMinRowsPerCta);
+  return ceil_div(S, rc) + 1;
 }
 
 struct PrefillWs {
@@ -67,11 +78,6 @@ PrefillWs prefill_ws(int64_t B, int64_t S_kv) {
   return w;
 }
 
-int64_t chunk_for_splits(int64_t S_kv_max, int num_splits) {
-  int64_t c = ceil_div(S_kv_max, num_splits);
-  c = ceil_div(c, kChunkQuant) * kChunkQuant;
-  return std::max<int64_t>(c, kChunkQuant);
-}
 
 // ------------------------------------------------------------ driver entry
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -190,33 +196,35 @@ fa_status fa_decode_plan(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t
       num_heads % num_kv_heads != 0 || num_splits < 0 || num_sms <= 0 || S_kv_max > kMaxDim)
     return FA_ERR_PARAM_INVALID;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
-  int64_t total = 0;
+  int64_t sum = 0;
   for (int64_t b = 0; b < B; ++b) {
     if (lens[b] < 0 || lens[b] > S_kv_max) return FA_ERR_PARAM_INVALID;
-    total += lens[b];
+    sum += lens[b];
   }
-  int64_t chunk;
+  // work space: every (batch, KV head, head group) unit of L_b rows, end to end
+  const int64_t g = num_heads / num_kv_heads;
+  const int64_t KH = num_kv_heads * (g / decode_heads_per_cta(g, D));
+  const int64_t total = KH * sum;
+  int64_t rc;
   if (num_splits > 0) {
-    chunk = chunk_for_splits(std::max<int64_t>(S_kv_max, 1), num_splits);
+    rc = chunk_for_splits(std::max<int64_t>(S_kv_max, 1), num_splits);
   } else {
-    // Spread the valid rows of every (batch, KV head, head group) over about
-    // kWaves CTAs per SM, in equal multiples of 64 rows.
-    const int64_t g = num_heads / num_kv_heads;
-    const int64_t per_row = num_kv_heads * (g / decode_heads_per_cta(g, D));
-    const int64_t target = static_cast<int64_t>(kWaves) * num_sms;
-    chunk = ceil_div(std::max<int64_t>(total * per_row, 1), target);
-    chunk = ceil_div(chunk, kChunkQuant) * kChunkQuant;
-    const int64_t cap = ceil_div(std::max<int64_t>(S_kv_max, 1), kChunkQuant) * kChunkQuant;
-    chunk = std::min(std::max<int64_t>(chunk, kMinChunk), std::max<int64_t>(cap, kMinChunk));
+    // one equal share per SM (at least a couple of stages each)
+    rc = std::max<int64_t>(ceil_div(std::max<int64_t>(total, 1), num_sms), kDecodeMinRowsPerCta);
   }
-  int64_t n = 0, mx = 0;
+  int64_t mx = 0, prefix = 0;
   for (int64_t b = 0; b < B; ++b) {
-    const int64_t c = ceil_div(lens[b], chunk);
-    n += c;
-    mx = std::max(mx, c);
+    const int64_t L = lens[b];
+    if (L > 0) {
+      for (int64_t kh = 0; kh < KH; ++kh) {
+        const int64_t u0 = KH * prefix + kh * L;
+        mx = std::max(mx, (u0 + L - 1) / rc - u0 / rc + 1);
+      }
+    }
+    prefix += L;
   }
-  *chunk_rows = chunk;
-  *num_chunks = n;
+  *chunk_rows = rc;
+  *num_chunks = ceil_div(total, rc);
   *max_chunks = mx;
   return FA_OK;
 }
@@ -226,9 +234,7 @@ size_t fa_decode_workspace_size(int64_t B, int64_t S_kv_max, int64_t num_heads,
   if (num_kv_heads == 0) num_kv_heads = num_heads;
   if (B < 0 || S_kv_max < 0 || num_heads < 0 || num_kv_heads < 0 || D < 0 || num_splits < 0)
     return 0;
-  const int64_t S = std::max<int64_t>(S_kv_max, 1);
-  const int64_t chunk = num_splits > 0 ? chunk_for_splits(S, num_splits) : kMinChunk;
-  return decode_ws(B, num_heads, D, ceil_div(S, chunk)).total;
+  return decode_ws(B, num_heads, D, max_slots_bound(S_kv_max, num_splits)).total;
 }
 
 static fa_status check_common(int64_t B, int64_t S_q, int64_t S_kv, int64_t Hq, int64_t& Hkv,
@@ -333,26 +339,32 @@ fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* 
 
   const int sms = device_sm_count();
   if (sms <= 0) return FA_ERR_RUNTIME;
-  int64_t chunk = 0, n_items = 0, max_chunks = 0;
-  st = fa_decode_plan(B, S_kv_max, num_heads, Hkv, D, lens, sms, num_splits, &chunk, &n_items,
-                      &max_chunks);
+  int64_t rc = 0, n_ctas = 0, max_slots = 0;
+  st = fa_decode_plan(B, S_kv_max, num_heads, Hkv, D, lens, sms, num_splits, &rc, &n_ctas,
+                      &max_slots);
   if (st != FA_OK) return st;
-  const int64_t slots = std::max<int64_t>(max_chunks, 1);
+  const int64_t slots = std::max<int64_t>(max_slots, 1);
+  if (slots > max_slots_bound(S_kv_max, num_splits)) return FA_ERR_RUNTIME;  // cannot happen
   const DecodeWs ws = decode_ws(B, num_heads, D, slots);
   if (workspace_bytes < ws.total) return FA_ERR_WORKSPACE_TOO_SMALL;
 
-  // header blob: status word, lengths, work items (batch, chunk index)
-  std::vector<int32_t> blob(ws.items / 4 + 2 * n_items, 0);
-  for (int64_t b = 0; b < B; ++b) blob[ws.lens / 4 + b] = static_cast<int32_t>(lens[b]);
-  int64_t it = 0;
-  for (int64_t b = 0; b < B; ++b)
-    for (int64_t c = 0; c < ceil_div(lens[b], chunk); ++c, ++it) {
-      blob[ws.items / 4 + 2 * it] = static_cast<int32_t>(b);
-      blob[ws.items / 4 + 2 * it + 1] = static_cast<int32_t>(c);
-    }
+  std::vector<long long> prefix(B + 1, 0);
+  bool has_empty = false;
+  for (int64_t b = 0; b < B; ++b) {
+    prefix[b + 1] = prefix[b] + lens[b];
+    has_empty = has_empty || lens[b] == 0;
+  }
+  const int64_t g = num_heads / Hkv;
+  const int64_t KH = Hkv * (g / decode_heads_per_cta(g, D));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned char* wsb = static_cast<unsigned char*>(workspace);
-  if (cudaMemcpyAsync(wsb, blob.data(), blob.size() * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+  const bool in_params = B <= kDecodeParamBatches;
+  if (!in_params && cudaMemcpyAsync(wsb + ws.prefix, prefix.data(), prefix.size() * sizeof(long long),
+                                    cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return FA_ERR_RUNTIME;
+  const int64_t total = KH * prefix[B];
+  // the main kernel clears the status word when it starts; without one, clear it here
+  if (total == 0 && cudaMemsetAsync(wsb, 0, sizeof(uint32_t), s) != cudaSuccess)
     return FA_ERR_RUNTIME;
 
   DecodeLaunch x;
@@ -367,11 +379,12 @@ fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* 
   x.D = static_cast<int>(D);
   x.layout = layout;
   x.scale = scale;
-  x.chunk = static_cast<int>(chunk);
-  x.num_items = static_cast<int>(n_items);
-  x.max_chunks = static_cast<int>(slots);
-  x.lens_dev = reinterpret_cast<const int*>(wsb + ws.lens);
-  x.items_dev = reinterpret_cast<const int2*>(wsb + ws.items);
+  x.total = total;
+  x.rows_per_cta = rc;
+  x.max_slots = static_cast<int>(slots);
+  x.needs_merge = has_empty || max_slots > 1;
+  x.prefix_host = prefix.data();
+  x.prefix_dev = in_params ? nullptr : reinterpret_cast<const long long*>(wsb + ws.prefix);
   x.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
   x.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
   x.out = out;

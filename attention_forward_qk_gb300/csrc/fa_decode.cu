@@ -1,29 +1,46 @@
 // Split-KV decode (S_q = 1) for sm_103a.
 //
-// Stage 1 (decode_chunk_kernel): one CTA per (batch, chunk of KV rows,
-// KV head [, group of query heads]). A producer warp streams the chunk's K
-// and V rows through a 4-stage shared-memory ring with TMA tensor loads;
-// seven consumer warps compute q.k with 128-bit shared loads, packed f32x2
-// FMAs and butterfly shuffles over the 8 lanes that share a row (every query
-// head of the GQA group reuses the same K/V row), keep
-// an online softmax (running max m and sum l, exp2 domain) per head and
-// accumulate p*v. The chunk's normalised partial output o/l and its
-// log-sum-exp are written to the workspace. This is the FlashDecoding
-// tutorial's stage 1 (§3.2) and the FlashAttn guide's FA phase of
-// FlashDecode (§1.9), with the scale and the length mask applied.
+// Work space. Every (batch b, KV head, group of G query heads) is a unit of
+// L_b key rows; the units are laid end to end in one global row space of
+// T = KH * sum_b L_b rows (KH = KV heads x head groups), and CTA i takes the
+// rows [i*Rc, (i+1)*Rc): every CTA gets the same amount of K/V to stream,
+// and a CTA's range is cut into pieces only where it crosses a unit boundary
+// (the load-balancing idea of the FlashAttn guide §4, SectionStreamK: split
+// the KV axis so that all cores carry equal cost, and merge the split rows
+// afterwards, FlashAttn guide §1.9).
 //
-// Stage 2 (decode_merge_kernel): one CTA per (batch, query head) merges the
-// chunks by their log-sum-exp with the largest value factored out:
+// Stage 1 (decode_kernel): the producer warp streams each piece's K and V
+// rows (112-row stages; a piece's last, partial stage with 16-row boxes)
+// through one 168 KB shared-memory ring with TMA tensor loads, without a
+// break between pieces; q arrives with a piece's first stage. Seven consumer
+// warps compute q.k with 128-bit shared loads, packed f32x2 FMAs and
+// butterfly shuffles over the 8 lanes that share a row (the G query heads of
+// a GQA group reuse each K/V row), keep an online softmax per head (running
+// max m and sum l, exp2 domain) and accumulate p*v. This is the FlashDecoding
+// tutorial's stage 1 (§3.2) with the scale and the length mask applied.
+// At the end of a piece every warp parks its (m, l, o) in a double-buffered
+// scratch slot and goes on; the last warp to arrive combines the seven
+// states into the piece's normalised partial o/l and log-sum-exp (or, when
+// the piece is the whole unit, into the final output).
+//
+// Stage 2 (decode_merge_kernel), launched with programmatic dependent launch
+// so that it is resident as soon as stage 1 drains, merges the pieces of
+// every (batch, query head) by their log-sum-exp with the largest value
+// factored out, in piece order:
 //   M = max_c lse_c, w_c = 2^(lse_c - M), out = sum_c w_c o_c / sum_c w_c,
 //   lse = M + log2(sum_c w_c)  (reported as natural log)
 // which is aclnnIncreFlashAttention guide §8.3's combine() and the FlashAttn
-// guide §10 formula written for normalised partials.
+// guide §10 formula written for normalised partials (FlashDecoding tutorial
+// §3.3). A sequence of length 0 gets out = 0, lse = +inf (FlashAttn guide
+// §1.7).
 //
-// Rows at or past a batch's length are never read by any arithmetic (they
-// may be loaded into shared memory with the rest of a box, and are skipped),
-// so stale cache contents, NaN included, cannot reach the output.
+// Rows at or past a batch's length are never used by any arithmetic (they
+// may land in shared memory with the rest of a box and are skipped), so
+// stale cache contents, NaN included, cannot reach the output.
 #include <cuda_bf16.h>
 #include <math.h>
+
+#include <algorithm>
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
@@ -35,146 +52,265 @@ namespace {
 // register budget at 255 (larger CTAs are capped at 168).
 constexpr int kDecWarps = 7;                       // consumer warps
 constexpr int kDecThreads = (kDecWarps + 1) * 32;  // + one producer warp
-constexpr int kDecStages = 4;
-constexpr int kDecStageBytes = 28672;              // K rows + V rows of one stage
-constexpr int kDecSmemBytes = kDecStages * kDecStageBytes + 256;
-constexpr int kMergeThreads = 256;
+constexpr int kRingBytes = 172032;                 // K/V ring (168 KB)
+constexpr int kQBytes = 1024;                      // q of one piece (G * D * 2 <= 1 KB)
+constexpr int kMaxStages = 6;
+constexpr int kTailBox = 16;  // rows per box of a piece's last, partial stage
+constexpr float kLn2 = 0.69314718055994530942f;
 
-template <int D>
+template <int D, int G>
 struct DecCfg {
-  static constexpr int LPR = 8;                         // lanes per K/V row
-  static constexpr int NCH = D / 64;                    // 16-byte chunks of a row per lane
-  static constexpr int RPW = 32 / LPR;                  // rows per warp per step
-  static constexpr int R = kDecStageBytes / (2 * D * 2);  // rows per stage (56 or 112)
-  static constexpr int RPWS = R / kDecWarps;            // rows per warp per stage
-  static constexpr int STEPS = RPWS / RPW;
+  static constexpr int LPR = 8;                     // lanes per K/V row
+  static constexpr int NCH = D / 64;                // 16-byte chunks of a row per lane
+  static constexpr int RPW = 32 / LPR;              // rows per warp per step
+  static constexpr int R = kDecodeStageRows;        // rows per stage (112)
+  static constexpr int RPWS = R / kDecWarps;        // rows per warp per stage (16)
+  static constexpr int STEPS = RPWS / RPW;          // 4
   static constexpr int TILE_BYTES = R * D * 2;
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int NST = kRingBytes / STAGE_BYTES;  // 3 (D = 128) or 6 (D = 64)
+  static constexpr int NP = 4 * NCH;                // fp32 pairs per lane per head
+  // one scratch buffer: m[warps][G] and l[warps][G], each padded to a
+  // multiple of 4 floats so that o[warps][G][D] and the next buffer stay
+  // 16-byte aligned for the float4 accesses
+  static constexpr int MG = (kDecWarps * G + 3) / 4 * 4;
+  static constexpr int SCRATCH_FLOATS = 2 * MG + kDecWarps * G * D;
+  static constexpr int SMEM = kRingBytes + 2 * SCRATCH_FLOATS * 4 + kMaxStages * kQBytes + 1024;
+  static_assert(SCRATCH_FLOATS % 4 == 0, "scratch alignment");
+  static_assert(NST <= kMaxStages, "ring slots");
+  static_assert(R % (kDecWarps * RPW) == 0, "stage rows");
+};
+
+// Where the length prefix sums live: launch parameters for small batches,
+// else the workspace.
+struct Prefix {
+  const long long* global;  // [B + 1] or null
+  long long local[kDecodeParamBatches + 1];
+  __device__ __forceinline__ long long operator[](int i) const {
+    return global != nullptr ? global[i] : local[i];
+  }
 };
 
 struct DecodeArgs {
   const __nv_bfloat16* q;
   const uint8_t* key_mask;
-  const int* lens;
-  const int2* items;
-  float* part_o;
-  float* part_lse;
+  float* part_o;     // [B][Hq][max_slots][D]
+  float* part_lse;   // [B][Hq][max_slots], log2 domain
+  __nv_bfloat16* out;
+  float* lse;
   uint32_t* status;
   uint64_t timeout_ns;
-  int Hq, Hkv, S_kv, chunk, max_chunks, head_groups;
+  long long total;         // rows of the work space
+  long long rows_per_cta;  // Rc
+  int B, Hq, Hkv, S_kv, max_slots, head_groups, G;
   float scale_log2;
+  Prefix prefix;           // prefix[b] = sum of lengths of batches < b
+};
+
+// Largest b with KH * prefix[b] <= r (the batch whose rows hold r; batches
+// of length 0 own no row and are passed over).
+__device__ __forceinline__ int find_batch(const Prefix& p, int B, long long KH, long long r) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (KH * p[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Per-slot header the producer writes before the slot's loads, so consumers
+// need no global lookups.
+struct SlotHeader {
+  int piece;   // piece counter of this CTA, -1 = no more work
+  int stage;   // stage index within the piece
+  int nstage;  // stages of the piece
+  int b, kh, row0, rows, slot, nsp, pad;
 };
 
 template <int D, int G>
 __global__ void __launch_bounds__(kDecThreads, 1)
-    decode_chunk_kernel(const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
-  using C = DecCfg<D>;
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_k16,
+                  const __grid_constant__ CUtensorMap tm_v16,
+                  const __grid_constant__ DecodeArgs a) {
+  using C = DecCfg<D, G>;
+  constexpr int NP = C::NP;
+  constexpr int NST = C::NST;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDecStages * kDecStageBytes);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kDecStages);
+  float* scratch = reinterpret_cast<float*>(smem + kRingBytes);  // 2 buffers
+  unsigned char* qbuf = smem + kRingBytes + 2 * C::SCRATCH_FLOATS * 4;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qbuf + kMaxStages * kQBytes);
+  // bars: full[kMaxStages], empty[kMaxStages], scratch_free[2]
+  SlotHeader* hdr = reinterpret_cast<SlotHeader*>(bars + 2 * kMaxStages + 2);
+  int* arrivals = reinterpret_cast<int*>(hdr + kMaxStages);  // [2] warps done per buffer
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(arrivals + 2);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-
-  const int2 item = a.items[blockIdx.x];
-  const int b = item.x;
-  const int c = item.y;
-  const int kvh = blockIdx.y / a.head_groups;
-  const int hg = blockIdx.y % a.head_groups;
+  const long long KH = static_cast<long long>(a.Hkv) * a.head_groups;
   const int g_total = a.Hq / a.Hkv;
-  const int h0 = kvh * g_total + hg * G;  // first query head of this CTA
-  const int L = a.lens[b];
-  const int row_begin = c * a.chunk;
-  const int row_end = min(row_begin + a.chunk, L);
-  const int nstage = (row_end - row_begin + C::R - 1) / C::R;
 
   const uint32_t full0 = smem_u32(bars);
-  const uint32_t empty0 = smem_u32(bars + kDecStages);
+  const uint32_t empty0 = smem_u32(bars + kMaxStages);
+  const uint32_t sfree0 = smem_u32(bars + 2 * kMaxStages);
   if (tid == 0) {
-    for (int s = 0; s < kDecStages; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, kDecWarps);
     }
+    mbar_init(sfree0, 1);
+    mbar_init(sfree0 + 8, 1);
+    arrivals[0] = 0;
+    arrivals[1] = 0;
     *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
-
-  // per-lane softmax state (consumers); o holds this lane's 8*NCH elements
-  // of every head's output as fp32 pairs
-  constexpr int NP = 4 * C::NCH;  // fp32 pairs per lane
-  float m[G], l[G];
-  uint64_t o[G][NP];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    m[h] = -INFINITY;
-    l[h] = 0.f;
-#pragma unroll
-    for (int k = 0; k < NP; ++k) o[h][k] = 0ull;
-  }
-  const int sub = lane % C::LPR;  // this lane owns 16-byte chunks sub, sub+8, ... of a row
-  const int rg = lane / C::LPR;   // row group within a warp step
+  // launched with programmatic dependent launch: wait until the work that
+  // precedes this kernel on the stream (which may produce q, K, V) is done
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // a timeout needs timeout_ns to fire, long after this clear
+  if (tid == 0 && blockIdx.x == 0) *a.status = 0;
+  // the merge kernel may be scheduled as soon as SMs free up; it waits for
+  // this grid's completion before it reads any partial
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == kDecWarps) {
-    // ------------------------------------------------------------ producer
+    // ================================================================ producer
     if (lane == 0) {
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
-      int issued = 0;
-      for (int st = 0; st < nstage; ++st) {
-        const int slot = st % kDecStages;
-        const int use = st / kDecStages;
-        if (use > 0 && !mbar_wait(empty0 + 8 * slot, (use - 1) & 1, a.timeout_ns, a.status,
-                                  kDevTimeoutDecodeEmpty, abort_flag))
-          break;
-        const uint32_t dst = smem_u32(smem + slot * kDecStageBytes);
-        mbar_expect_tx(full0 + 8 * slot, 2 * C::TILE_BYTES);
-        tma_load_4d(dst, &tm_k, full0 + 8 * slot, 0, row_begin + st * C::R, kvh, b);
-        tma_load_4d(dst + C::TILE_BYTES, &tm_v, full0 + 8 * slot, 0, row_begin + st * C::R, kvh,
-                    b);
-        issued = st + 1;
+      tma_prefetch_map(&tm_k16);
+      tma_prefetch_map(&tm_v16);
+      const long long Rc = a.rows_per_cta;
+      long long r = static_cast<long long>(blockIdx.x) * Rc;
+      const long long r1 = min(r + Rc, a.total);
+      int st = 0;  // stages issued by this CTA
+      bool ok = true;
+      for (int piece = 0; ok; ++piece) {
+        const bool done = r >= r1;
+        SlotHeader h{-1, 0, 1, 0, 0, 0, 0, 0, 0, 0};
+        int kvh = 0, hg = 0;
+        if (!done) {
+          const int b = find_batch(a.prefix, a.B, KH, r);
+          const long long base = KH * a.prefix[b];
+          const long long L = a.prefix[b + 1] - a.prefix[b];
+          const long long kh = (r - base) / L;
+          const long long u0 = base + kh * L;  // the unit's first row in the work space
+          const long long u1 = u0 + L;
+          const long long rows = min(u1, r1) - r;
+          h.piece = piece;
+          h.b = b;
+          h.kh = static_cast<int>(kh);
+          h.row0 = static_cast<int>(r - u0);
+          h.rows = static_cast<int>(rows);
+          h.slot = static_cast<int>(blockIdx.x - u0 / Rc);
+          h.nsp = static_cast<int>((u1 - 1) / Rc - u0 / Rc + 1);
+          h.nstage = static_cast<int>((rows + C::R - 1) / C::R);
+          kvh = h.kh / a.head_groups;
+          hg = h.kh % a.head_groups;
+          r += rows;
+        }
+        for (int s = 0; s < h.nstage; ++s, ++st) {
+          const int slot = st % NST;
+          const int use = st / NST;
+          if (use > 0 && !mbar_wait(empty0 + 8 * slot, (use - 1) & 1, a.timeout_ns, a.status,
+                                    kDevTimeoutDecodeEmpty, abort_flag)) {
+            ok = false;
+            break;
+          }
+          h.stage = s;
+          hdr[slot] = h;
+          if (done) {
+            mbar_arrive(full0 + 8 * slot);  // end marker: no data
+            ok = false;
+            ++st;
+            break;
+          }
+          const uint32_t dst = smem_u32(smem + slot * C::STAGE_BYTES);
+          const int row = h.row0 + s * C::R;
+          const int rows_here = min(C::R, h.rows - s * C::R);
+          const uint32_t q_bytes = s == 0 ? G * D * 2 : 0;
+          if (rows_here == C::R) {
+            mbar_expect_tx(full0 + 8 * slot, C::STAGE_BYTES + q_bytes);
+            tma_load_4d(dst, &tm_k, full0 + 8 * slot, 0, row, kvh, h.b);
+            tma_load_4d(dst + C::TILE_BYTES, &tm_v, full0 + 8 * slot, 0, row, kvh, h.b);
+          } else {
+            // partial last stage: 16-row boxes, only as many as the piece needs
+            const int nb = (rows_here + kTailBox - 1) / kTailBox;
+            mbar_expect_tx(full0 + 8 * slot, 2 * nb * kTailBox * D * 2 + q_bytes);
+            for (int t = 0; t < nb; ++t) {
+              tma_load_4d(dst + t * kTailBox * D * 2, &tm_k16, full0 + 8 * slot, 0,
+                          row + t * kTailBox, kvh, h.b);
+              tma_load_4d(dst + C::TILE_BYTES + t * kTailBox * D * 2, &tm_v16, full0 + 8 * slot,
+                          0, row + t * kTailBox, kvh, h.b);
+            }
+          }
+          if (s == 0) {
+            const __nv_bfloat16* qsrc =
+                a.q + (static_cast<size_t>(h.b) * a.Hq + kvh * g_total + hg * G) * D;
+            bulk_load(smem_u32(qbuf + slot * kQBytes), qsrc, q_bytes, full0 + 8 * slot);
+          }
+        }
       }
       if (*abort_flag) {
         // let every copy this CTA started land before shared memory is released
-        for (int st = max(0, issued - kDecStages); st < issued; ++st)
-          mbar_wait(full0 + 8 * (st % kDecStages), (st / kDecStages) & 1, a.timeout_ns, a.status,
+        for (int s = max(0, st - NST); s < st; ++s)
+          mbar_wait(full0 + 8 * (s % NST), (s / NST) & 1, a.timeout_ns, a.status,
                     kDevTimeoutDrain, nullptr);
       }
     }
   } else {
-    // ----------------------------------------------------------- consumers
+    // ================================================================ consumers
+    const int sub = lane % C::LPR;  // this lane owns 16-byte chunks sub, sub+8 of a row
+    const int rg = lane / C::LPR;   // row group within a warp step
+    float m[G], l[G];
+    uint64_t o[G][NP];
     uint64_t qp[G][NP];  // q * scale * log2(e), as fp32 pairs
+    int row_begin = 0, row_end = 0, piece_seq = -1;
+    const uint8_t* mask_row = nullptr;
+
+    for (int st = 0;; ++st) {
+      const int slot = st % NST;
+      bool got = mbar_wait(full0 + 8 * slot, (st / NST) & 1, a.timeout_ns, a.status,
+                           kDevTimeoutDecodeFull, abort_flag);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) break;
+      const SlotHeader hd = hdr[slot];
+      if (hd.piece < 0) break;
+
+      if (hd.stage == 0) {
+        // ---- a new piece: q landed with this stage; fresh softmax state
+        ++piece_seq;
+        row_begin = hd.row0;
+        row_end = hd.row0 + hd.rows;
+        mask_row = a.key_mask ? a.key_mask + static_cast<size_t>(hd.b) * a.S_kv : nullptr;
+        const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(qbuf + slot * kQBytes);
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const __nv_bfloat16* qh = a.q + (static_cast<size_t>(b) * a.Hq + h0 + h) * D;
+        for (int h = 0; h < G; ++h) {
+          m[h] = -INFINITY;
+          l[h] = 0.f;
 #pragma unroll
-      for (int ch = 0; ch < C::NCH; ++ch) {
-        const uint4 u = *reinterpret_cast<const uint4*>(qh + (sub + 8 * ch) * 8);
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+          for (int k = 0; k < NP; ++k) o[h][k] = 0ull;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float lo = bf16lo_to_f32(w4[k]) * a.scale_log2;
-          const float hi = bf16hi_to_f32(w4[k]) * a.scale_log2;
-          qp[h][ch * 4 + k] = pair_f32(lo, hi);
+          for (int ch = 0; ch < C::NCH; ++ch) {
+            const uint4 u = *reinterpret_cast<const uint4*>(qs + h * D + (sub + 8 * ch) * 8);
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              qp[h][ch * 4 + k] = pair_f32(bf16lo_to_f32(w4[k]) * a.scale_log2,
+                                           bf16hi_to_f32(w4[k]) * a.scale_log2);
+          }
         }
       }
-    }
-    const uint8_t* mask_row =
-        a.key_mask ? a.key_mask + static_cast<size_t>(b) * a.S_kv : nullptr;
 
-    for (int st = 0; st < nstage; ++st) {
-      const int slot = st % kDecStages;
-      if (!mbar_wait(full0 + 8 * slot, (st / kDecStages) & 1, a.timeout_ns, a.status,
-                     kDevTimeoutDecodeFull, abort_flag))
-        break;
-      const __nv_bfloat16* Ks =
-          reinterpret_cast<const __nv_bfloat16*>(smem + slot * kDecStageBytes);
+      // ---- one stage: R rows of K and V
+      const __nv_bfloat16* Ks = reinterpret_cast<const __nv_bfloat16*>(smem + slot * C::STAGE_BYTES);
       const __nv_bfloat16* Vs = Ks + C::R * D;
-      const int stage_row0 = row_begin + st * C::R;
-
+      const int stage_row0 = row_begin + hd.stage * C::R;
       float s[C::STEPS][G];
       bool valid[C::STEPS];
 #pragma unroll
@@ -195,18 +331,22 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          uint64_t acc2 = 0ull;
+          // two accumulator pairs: half the dependent-FMA chain length
+          uint64_t acc_a = 0ull, acc_b = 0ull;
 #pragma unroll
-          for (int k = 0; k < NP; ++k) acc2 = ffma2(qp[h][k], kp[k], acc2);
-          const float2 a2 = unpair(acc2);
-          float acc = a2.x + a2.y;
+          for (int k = 0; k < NP; k += 2) {
+            acc_a = ffma2(qp[h][k], kp[k], acc_a);
+            acc_b = ffma2(qp[h][k + 1], kp[k + 1], acc_b);
+          }
+          const float2 a2 = unpair(acc_a);
+          const float2 b2 = unpair(acc_b);
+          float acc = (a2.x + a2.y) + (b2.x + b2.y);
 #pragma unroll
           for (int off = C::LPR / 2; off > 0; off >>= 1)
             acc += __shfl_xor_sync(0xffffffffu, acc, off);
           s[i][h] = ok ? acc : -INFINITY;
         }
       }
-      // online softmax update for this stage's rows (exp2 domain)
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         float mx = s[0][h];
@@ -219,7 +359,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         l[h] *= alpha;
         const uint64_t a2 = pair_f32(alpha, alpha);
 #pragma unroll
-        for (int k = 0; k < NP; ++k) o[h][k] = ffma2(o[h][k], a2, 0ull);
+        for (int k = 0; k < NP; ++k) o[h][k] = fmul2(o[h][k], a2);
 #pragma unroll
         for (int i = 0; i < C::STEPS; ++i) {
           s[i][h] = ex2(s[i][h] - m_use);  // -inf -> 0
@@ -248,184 +388,249 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * slot);
-    }
+      if (hd.stage != hd.nstage - 1) continue;
 
-    // merge the row groups of this warp (lanes with equal `sub`)
+      // ================================================= end of the piece
+      // 1) merge the row groups of this warp (lanes with equal `sub`)
 #pragma unroll
-    for (int off = C::LPR; off < 32; off <<= 1) {
+      for (int off = C::LPR; off < 32; off <<= 1) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, m[h], off);
+          const float l2 = __shfl_xor_sync(0xffffffffu, l[h], off);
+          const float mn = fmaxf(m[h], m2);
+          const float m_use = (mn == -INFINITY) ? 0.f : mn;
+          const float a1 = ex2(m[h] - m_use);
+          const float a2 = ex2(m2 - m_use);
+          l[h] = l[h] * a1 + l2 * a2;
+#pragma unroll
+          for (int k = 0; k < NP; ++k) {
+            const float2 mine = unpair(o[h][k]);
+            const float ox = __shfl_xor_sync(0xffffffffu, mine.x, off);
+            const float oy = __shfl_xor_sync(0xffffffffu, mine.y, off);
+            o[h][k] = pair_f32(mine.x * a1 + ox * a2, mine.y * a1 + oy * a2);
+          }
+          m[h] = mn;
+        }
+      }
+      // 2) park this warp's state in scratch buffer (piece_seq & 1); wait
+      //    until the combiner of the piece two back has released it
+      const int buf = piece_seq & 1;
+      if (piece_seq >= 2) {
+        bool fr = mbar_wait(sfree0 + 8 * buf, ((piece_seq >> 1) - 1) & 1, a.timeout_ns, a.status,
+                            kDevTimeoutDecodeFull, abort_flag);
+        fr = __all_sync(0xffffffffu, fr);
+        if (!fr) break;
+      }
+      float* sb = scratch + buf * C::SCRATCH_FLOATS;
+      float* sm_m = sb;              // [warps][G]
+      float* sm_l = sb + C::MG;      // [warps][G]
+      float* sm_o = sb + 2 * C::MG;  // [warps][G][D], 16-byte aligned
+      if (lane < C::LPR) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          if (lane == 0) {
+            sm_m[warp * G + h] = m[h];
+            sm_l[warp * G + h] = l[h];
+          }
+#pragma unroll
+          for (int ch = 0; ch < C::NCH; ++ch)
+#pragma unroll
+            for (int k = 0; k < 4; k += 2) {
+              const float2 v0 = unpair(o[h][ch * 4 + k]);
+              const float2 v1 = unpair(o[h][ch * 4 + k + 1]);
+              *reinterpret_cast<float4*>(sm_o + (warp * G + h) * D + (sub + 8 * ch) * 8 + 2 * k) =
+                  make_float4(v0.x, v0.y, v1.x, v1.y);
+            }
+        }
+      }
+      // 3) the last warp to finish this piece combines it
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) {
+        __threadfence_block();
+        last = (atomicAdd(arrivals + buf, 1) == kDecWarps - 1) ? 1 : 0;
+        if (last) {
+          arrivals[buf] = 0;
+          __threadfence_block();
+        }
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (!last) continue;
+
+      // ---- combiner warp: 7 warp states -> the piece's result
+      const int kvh = hd.kh / a.head_groups;
+      const int hg = hd.kh % a.head_groups;
+      const size_t bh0 = static_cast<size_t>(hd.b) * a.Hq + kvh * g_total + hg * G;
+      float Mh[G], Lh[G], fw[G][kDecWarps];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m[h], off);
-        const float l2 = __shfl_xor_sync(0xffffffffu, l[h], off);
-        const float mn = fmaxf(m[h], m2);
-        const float m_use = (mn == -INFINITY) ? 0.f : mn;
-        const float a1 = ex2(m[h] - m_use);
-        const float a2 = ex2(m2 - m_use);
-        l[h] = l[h] * a1 + l2 * a2;
+        float M = -INFINITY;
 #pragma unroll
-        for (int k = 0; k < NP; ++k) {
-          const float2 mine = unpair(o[h][k]);
-          const float ox = __shfl_xor_sync(0xffffffffu, mine.x, off);
-          const float oy = __shfl_xor_sync(0xffffffffu, mine.y, off);
-          o[h][k] = pair_f32(mine.x * a1 + ox * a2, mine.y * a1 + oy * a2);
+        for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sm_m[w * G + h]);
+        float Ls = 0.f;
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) {
+          fw[h][w] = (M == -INFINITY) ? 0.f : ex2(sm_m[w * G + h] - M);
+          Ls = fmaf(sm_l[w * G + h], fw[h][w], Ls);
         }
-        m[h] = mn;
+        Mh[h] = M;
+        Lh[h] = Ls;
       }
-    }
-  }
-
-  __syncthreads();  // every stage consumed: the ring becomes merge scratch
-  const bool aborted = *abort_flag != 0;
-  float* sm_m = reinterpret_cast<float*>(smem);          // [warps][G]
-  float* sm_l = sm_m + kDecWarps * G;                    // [warps][G]
-  float* sm_o = sm_l + kDecWarps * G;                    // [warps][G][D]
-  if (warp < kDecWarps && lane < C::LPR) {
+      // lane handles elements lane*4 .. lane*4+3 of every 128-element block
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      if (lane == 0) {
-        sm_m[warp * G + h] = m[h];
-        sm_l[warp * G + h] = l[h];
-      }
+      for (int h = 0; h < G; ++h) {
+        const bool empty = (Mh[h] == -INFINITY);
+        const float inv = empty ? 0.f : 1.f / Lh[h];
 #pragma unroll
-      for (int ch = 0; ch < C::NCH; ++ch)
+        for (int d0 = 0; d0 < D; d0 += 128) {
+          const int d = d0 + lane * 4;
+          if (d < D) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 v2 = unpair(o[h][ch * 4 + k]);
-          float* dst = sm_o + (warp * G + h) * D + (sub + 8 * ch) * 8 + 2 * k;
-          dst[0] = v2.x;
-          dst[1] = v2.y;
+            for (int w = 0; w < kDecWarps; ++w) {
+              const float4 v = *reinterpret_cast<const float4*>(sm_o + (w * G + h) * D + d);
+              acc.x = fmaf(v.x, fw[h][w], acc.x);
+              acc.y = fmaf(v.y, fw[h][w], acc.y);
+              acc.z = fmaf(v.z, fw[h][w], acc.z);
+              acc.w = fmaf(v.w, fw[h][w], acc.w);
+            }
+            acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            if (hd.nsp == 1) {
+              __nv_bfloat16* dst = a.out + (bh0 + h) * D + d;
+              *reinterpret_cast<uint2*>(dst) =
+                  make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+            } else {
+              *reinterpret_cast<float4*>(a.part_o + ((bh0 + h) * a.max_slots + hd.slot) * D + d) =
+                  acc;
+            }
+          }
         }
+        if (lane == 0) {
+          if (hd.nsp == 1) {
+            if (a.lse != nullptr)
+              a.lse[bh0 + h] = empty ? INFINITY : (Mh[h] + log2f(Lh[h])) * kLn2;
+          } else {
+            a.part_lse[(bh0 + h) * a.max_slots + hd.slot] =
+                empty ? -INFINITY : Mh[h] + log2f(Lh[h]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sfree0 + 8 * buf);  // scratch buffer free again
     }
   }
   __syncthreads();
-  if (aborted) return;
-  for (int idx = tid; idx < G * D; idx += kDecThreads) {
-    const int h = idx / D;
-    const int d = idx % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sm_m[w * G + h]);
-    float Lsum = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) {
-        const float f = ex2(sm_m[w * G + h] - M);
-        Lsum = fmaf(sm_l[w * G + h], f, Lsum);
-        O = fmaf(sm_o[(w * G + h) * D + d], f, O);
-      }
-    }
-    const size_t slot = (static_cast<size_t>(b) * a.Hq + h0 + h) * a.max_chunks + c;
-    a.part_o[slot * D + d] = (M != -INFINITY) ? O / Lsum : 0.f;
-    if (d == 0) a.part_lse[slot] = (M != -INFINITY) ? M + log2f(Lsum) : -INFINITY;
-  }
 }
 
-struct MergeArgs {
-  const float* part_o;
-  const float* part_lse;
-  const int* lens;
-  __nv_bfloat16* out;
-  float* lse;
-  int Hq, chunk, max_chunks;
-};
-
+// One warp per (batch, query head). Recomputes the piece count of its unit
+// from the same prefix sums; a unit cut into one piece was written by stage
+// 1, a batch of length 0 gets out = 0 and lse = +inf, the rest are merged
+// with all loads of a batch of pieces issued before any is used.
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const MergeArgs a) {
+__global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant__ DecodeArgs a) {
   constexpr int EPL = D / 32;  // output elements per lane
-  constexpr int NW = kMergeThreads / 32;
-  __shared__ float red[NW];
-  __shared__ float sm_w[NW];
-  __shared__ float sm_o[NW][D];
-  const int bh = blockIdx.x;
-  const int b = bh / a.Hq;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int L = a.lens[b];
-  const int nsp = L > 0 ? (L + a.chunk - 1) / a.chunk : 0;
-  const float* pl = a.part_lse + static_cast<size_t>(bh) * a.max_chunks;
-  const float* po = a.part_o + static_cast<size_t>(bh) * a.max_chunks * D;
-
-  // 1) M = max over chunks of lse_c
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (row >= a.B * a.Hq) return;
+  const int b = row / a.Hq;
+  const int h = row % a.Hq;
+  const int g_total = a.Hq / a.Hkv;
+  const long long KH = static_cast<long long>(a.Hkv) * a.head_groups;
+  const long long kh = static_cast<long long>(h / g_total) * a.head_groups + (h % g_total) / a.G;
+  const long long L = a.prefix[b + 1] - a.prefix[b];
+  __nv_bfloat16* dst = a.out + static_cast<size_t>(row) * D + lane * EPL;
+  if (L == 0) {
+    if constexpr (EPL == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
+    else *reinterpret_cast<uint32_t*>(dst) = 0u;
+    if (lane == 0 && a.lse != nullptr) a.lse[row] = INFINITY;
+    return;
+  }
+  const long long u0 = KH * a.prefix[b] + kh * L;
+  const int nsp = static_cast<int>((u0 + L - 1) / a.rows_per_cta - u0 / a.rows_per_cta + 1);
+  if (nsp <= 1) return;
+  const float* pl = a.part_lse + static_cast<size_t>(row) * a.max_slots;
+  const float* po = a.part_o + static_cast<size_t>(row) * a.max_slots * D + lane * EPL;
   float M = -INFINITY;
-  for (int c = tid; c < nsp; c += kMergeThreads) M = fmaxf(M, pl[c]);
+  for (int k = lane; k < nsp; k += 32) M = fmaxf(M, __ldcg(pl + k));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  if (lane == 0) red[warp] = M;
-  __syncthreads();
-  M = red[0];
+  const bool invalid = (M == -INFINITY);
+  float acc[EPL], W = 0.f;
 #pragma unroll
-  for (int w = 1; w < NW; ++w) M = fmaxf(M, red[w]);
-
-  // 2) each warp sums w_c * o_c over its chunks
-  float W = 0.f, O[EPL];
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+  if (!invalid) {
+    for (int k0 = 0; k0 < nsp; k0 += 8) {
+      // all loads of up to 8 pieces in flight before any is used
+      float lk[8], v[8][EPL];
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) O[e] = 0.f;
-  if (M != -INFINITY) {
-#pragma unroll 4
-    for (int c = warp; c < nsp; c += NW) {
-      const float w = ex2(pl[c] - M);  // empty chunk: lse -inf -> 0
-      const float* src = po + static_cast<size_t>(c) * D + lane * EPL;
-      if constexpr (EPL == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        O[0] = fmaf(w, v.x, O[0]);
-        O[1] = fmaf(w, v.y, O[1]);
-        O[2] = fmaf(w, v.z, O[2]);
-        O[3] = fmaf(w, v.w, O[3]);
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        O[0] = fmaf(w, v.x, O[0]);
-        O[1] = fmaf(w, v.y, O[1]);
+      for (int u = 0; u < 8; ++u) {
+        const bool in = k0 + u < nsp;
+        lk[u] = in ? __ldcg(pl + k0 + u) : -INFINITY;
+        if constexpr (EPL == 4) {
+          const float4 t = in ? __ldcg(reinterpret_cast<const float4*>(po + static_cast<size_t>(k0 + u) * D))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+        } else {
+          const float2 t = in ? __ldcg(reinterpret_cast<const float2*>(po + static_cast<size_t>(k0 + u) * D))
+                              : make_float2(0.f, 0.f);
+          v[u][0] = t.x; v[u][1] = t.y;
+        }
       }
-      W += w;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float wk = ex2(lk[u] - M);  // empty or absent piece: 0
+        W += wk;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wk, v[u][e], acc[e]);
+      }
     }
   }
-  if (lane == 0) sm_w[warp] = W;
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) sm_o[warp][lane * EPL + e] = O[e];
-  __syncthreads();
-  if (warp == 0) {
-    float Wt = 0.f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) Wt += sm_w[w];
-    const bool invalid = (M == -INFINITY);
-    __nv_bfloat16* dst = a.out + static_cast<size_t>(bh) * D + lane * EPL;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      float acc = 0.f;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) acc += sm_o[w][lane * EPL + e];
-      dst[e] = __float2bfloat16_rn(invalid ? 0.f : acc / Wt);
-    }
-    if (lane == 0 && a.lse != nullptr)
-      a.lse[bh] = invalid ? INFINITY : (M + log2f(Wt)) * 0.69314718055994530942f;
+  const float inv = invalid ? 0.f : 1.f / W;
+  if constexpr (EPL == 4) {
+    *reinterpret_cast<uint2*>(dst) =
+        make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
   }
+  if (lane == 0 && a.lse != nullptr) a.lse[row] = invalid ? INFINITY : (M + log2f(W)) * kLn2;
 }
 
 template <int D, int G>
-cudaError_t launch_chunks(const DecodeLaunch& x, const CUtensorMap& mk, const CUtensorMap& mv,
-                          const DecodeArgs& da, cudaStream_t stream) {
+cudaError_t launch_decode_dg(int grid, const CUtensorMap* m, const DecodeArgs& da,
+                             cudaStream_t stream) {
   static bool configured = false;  // benign race: idempotent attribute set
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_chunk_kernel<D, G>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kDecSmemBytes + 1024);
+                                         DecCfg<D, G>::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(x.num_items, x.Hkv * da.head_groups);
-  decode_chunk_kernel<D, G><<<grid, kDecThreads, kDecSmemBytes + 1024, stream>>>(mk, mv, da);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = DecCfg<D, G>::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, G>, m[0], m[1], m[2], m[3], da);
 }
 
 template <int D>
-cudaError_t launch_chunks_g(int G, const DecodeLaunch& x, const CUtensorMap& mk,
-                            const CUtensorMap& mv, const DecodeArgs& da, cudaStream_t s) {
+cudaError_t launch_decode_d(int G, int grid, const CUtensorMap* m, const DecodeArgs& da,
+                            cudaStream_t s) {
   switch (G) {
     case 8:
-      if constexpr (D == 64) return launch_chunks<D, 8>(x, mk, mv, da, s);
+      if constexpr (D == 64) return launch_decode_dg<D, 8>(grid, m, da, s);
       return cudaErrorInvalidValue;
-    case 4: return launch_chunks<D, 4>(x, mk, mv, da, s);
-    case 2: return launch_chunks<D, 2>(x, mk, mv, da, s);
-    default: return launch_chunks<D, 1>(x, mk, mv, da, s);
+    case 4: return launch_decode_dg<D, 4>(grid, m, da, s);
+    case 2: return launch_decode_dg<D, 2>(grid, m, da, s);
+    default: return launch_decode_dg<D, 1>(grid, m, da, s);
   }
 }
 
@@ -434,51 +639,63 @@ cudaError_t launch_chunks_g(int G, const DecodeLaunch& x, const CUtensorMap& mk,
 cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
   const int g_total = x.Hq / x.Hkv;
   const int G = decode_heads_per_cta(g_total, x.D);
-  if (x.num_items > 0) {
-    CUtensorMap mk, mv;
-    const int R = (x.D == 128) ? DecCfg<128>::R : DecCfg<64>::R;
-    if (!encode_bf16_map(&mk, x.k, x.layout, x.B, x.Hkv, x.S_kv, x.D, x.D, R,
+  DecodeArgs da;
+  da.q = static_cast<const __nv_bfloat16*>(x.q);
+  da.key_mask = x.key_mask;
+  da.part_o = x.part_o;
+  da.part_lse = x.part_lse;
+  da.out = static_cast<__nv_bfloat16*>(x.out);
+  da.lse = x.lse;
+  da.status = x.status;
+  da.timeout_ns = x.timeout_ns;
+  da.total = x.total;
+  da.rows_per_cta = x.rows_per_cta;
+  da.B = x.B;
+  da.Hq = x.Hq;
+  da.Hkv = x.Hkv;
+  da.S_kv = std::max(x.S_kv, 1);
+  da.max_slots = x.max_slots;
+  da.head_groups = g_total / G;
+  da.G = G;
+  da.scale_log2 = x.scale * 1.4426950408889634f;
+  da.prefix.global = x.prefix_dev;
+  if (x.prefix_dev == nullptr)
+    for (int b = 0; b <= x.B; ++b) da.prefix.local[b] = x.prefix_host[b];
+
+  if (x.total > 0) {
+    CUtensorMap maps[4];  // K, V with 112-row boxes; K, V with 16-row boxes
+    const int S_map = std::max(x.S_kv, 1);
+    if (!encode_bf16_map(&maps[0], x.k, x.layout, x.B, x.Hkv, S_map, x.D, x.D, kDecodeStageRows,
                          CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_bf16_map(&mv, x.v, x.layout, x.B, x.Hkv, x.S_kv, x.D, x.D, R,
+        !encode_bf16_map(&maps[1], x.v, x.layout, x.B, x.Hkv, S_map, x.D, x.D, kDecodeStageRows,
+                         CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_bf16_map(&maps[2], x.k, x.layout, x.B, x.Hkv, S_map, x.D, x.D, kTailBox,
+                         CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_bf16_map(&maps[3], x.v, x.layout, x.B, x.Hkv, S_map, x.D, x.D, kTailBox,
                          CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
-    DecodeArgs da;
-    da.q = static_cast<const __nv_bfloat16*>(x.q);
-    da.key_mask = x.key_mask;
-    da.lens = x.lens_dev;
-    da.items = x.items_dev;
-    da.part_o = x.part_o;
-    da.part_lse = x.part_lse;
-    da.status = x.status;
-    da.timeout_ns = x.timeout_ns;
-    da.Hq = x.Hq;
-    da.Hkv = x.Hkv;
-    da.S_kv = x.S_kv;
-    da.chunk = x.chunk;
-    da.max_chunks = x.max_chunks;
-    da.head_groups = g_total / G;
-    da.scale_log2 = x.scale * 1.4426950408889634f;
+    const int grid = static_cast<int>((x.total + x.rows_per_cta - 1) / x.rows_per_cta);
     main_kernel_begin(stream);
-    cudaError_t e = (x.D == 128) ? launch_chunks_g<128>(G, x, mk, mv, da, stream)
-                                 : launch_chunks_g<64>(G, x, mk, mv, da, stream);
+    const cudaError_t e = (x.D == 128) ? launch_decode_d<128>(G, grid, maps, da, stream)
+                                       : launch_decode_d<64>(G, grid, maps, da, stream);
     main_kernel_end(stream);
     if (e != cudaSuccess) return e;
     count_launches(1);
   }
-  MergeArgs ma;
-  ma.part_o = x.part_o;
-  ma.part_lse = x.part_lse;
-  ma.lens = x.lens_dev;
-  ma.out = static_cast<__nv_bfloat16*>(x.out);
-  ma.lse = x.lse;
-  ma.Hq = x.Hq;
-  ma.chunk = x.chunk;
-  ma.max_chunks = x.max_chunks;
-  if (x.D == 128)
-    decode_merge_kernel<128><<<x.B * x.Hq, kMergeThreads, 0, stream>>>(ma);
-  else
-    decode_merge_kernel<64><<<x.B * x.Hq, kMergeThreads, 0, stream>>>(ma);
-  const cudaError_t e = cudaGetLastError();
+  if (!x.needs_merge) return cudaSuccess;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((x.B * x.Hq + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = (x.D == 128) ? cudaLaunchKernelEx(&cfg, decode_merge_kernel<128>, da)
+                                     : cudaLaunchKernelEx(&cfg, decode_merge_kernel<64>, da);
   if (e == cudaSuccess) count_launches(1);
   return e;
 }

@@ -24,6 +24,13 @@ inline int decode_heads_per_cta(int64_t g, int64_t D) {
   return (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1;
 }
 
+// Decode stage height in rows, and the batch count up to which the length
+// prefix sums travel as launch parameters (larger batches use the workspace).
+constexpr int kDecodeStageRows = 112;
+constexpr int kDecodeParamBatches = 1024;
+// Smallest share of the work space one decode CTA is given.
+constexpr int kDecodeMinRowsPerCta = 224;
+
 struct DecodeLaunch {
   const void* q;
   const void* k;
@@ -31,13 +38,14 @@ struct DecodeLaunch {
   const uint8_t* key_mask;
   int B, Hq, Hkv, S_kv, D, layout;
   float scale;
-  int chunk;       // KV rows per chunk
-  int num_items;   // (batch, chunk) work items
-  int max_chunks;  // chunk slots per (batch, head) in the partial buffers
-  const int* lens_dev;      // [B] in the workspace
-  const int2* items_dev;    // [num_items] in the workspace
-  float* part_o;            // [B, Hq, max_chunks, D]
-  float* part_lse;          // [B, Hq, max_chunks] (log2 domain)
+  long long total;            // rows of the work space (KV heads x head groups x sum L_b)
+  long long rows_per_cta;     // contiguous share of each CTA
+  int max_slots;              // piece slots per (batch, head) in the partial buffers
+  bool needs_merge;           // some sequence has more than one piece, or length 0
+  const long long* prefix_host;  // [B + 1] prefix sums of the lengths
+  const long long* prefix_dev;   // the same in the workspace, or null (then in params)
+  float* part_o;            // [B, Hq, max_slots, D]
+  float* part_lse;          // [B, Hq, max_slots] (log2 domain)
   void* out;
   float* lse;
   uint32_t* status;

@@ -40,8 +40,8 @@ import workloads  # noqa: E402
 
 METRIC = "prefill attn TFLOP/s & decode KV-read GB/s on 1 GB300, as % of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-FLUSH_BYTES = 512 * 1024 * 1024
-MAIN_KERNEL = {"decode": "decode_chunk_kernel", "prefill": "prefill_kernel"}
+FLUSH_BYTES = 512 * 1024 * 1024  # written, then half as much read: both above L2 (126 MB)
+MAIN_KERNEL = {"decode": "decode_kernel", "prefill": "prefill_kernel"}
 KERNEL_SOURCE = {"decode": "attention_forward_qk_gb300/csrc/fa_decode.cu",
                  "prefill": "attention_forward_qk_gb300/csrc/fa_prefill.cu"}
 
@@ -250,6 +250,24 @@ class Runner:
         return self.out.numel() * self.out.element_size() + self.lse.numel() * 4
 
 
+class L2Flush:
+    """Evicts the step's inputs from L2 between steps: a 512 MB write, then a
+    256 MB read, so that L2 is left holding clean lines of the flush buffers
+    (the write-back of the flush's own dirty lines is not charged to the
+    timed step)."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.ones(FLUSH_BYTES // 8, dtype=torch.float32, device=dev)
+        self.sink = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        import torch
+        self.w.fill_(1.0)
+        torch.sum(self.r, dim=0, keepdim=True, out=self.sink)
+
+
 def time_steps(runner, steps, warmup, flush, fn=None):
     """Per-step CUDA-event times (ms) of `fn` (default runner.step) and of the
     main kernel inside it; L2 flushed before every step, outside the events."""
@@ -257,7 +275,7 @@ def time_steps(runner, steps, warmup, flush, fn=None):
     F = runner.F
     fn = fn or runner.step
     for _ in range(warmup):
-        flush.fill_(1.0)
+        flush()
         fn()
     torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
@@ -267,7 +285,7 @@ def time_steps(runner, steps, warmup, flush, fn=None):
     torch.cuda.synchronize()
     l0 = F.fa_kernel_launch_count()
     for e in evs:
-        flush.fill_(1.0)
+        flush()
         F.fa_set_main_kernel_events(e[2], e[3])
         e[0].record()
         fn()
@@ -366,7 +384,7 @@ def run_gpu(args):
     torch.cuda.set_device(dev)
     from attention_forward_qk_gb300 import build as B
     B.build()
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     main = Runner(w, dev, host_copy=True)
 
     sampler = ClockSampler(local)
@@ -440,7 +458,7 @@ def run_gpu(args):
             "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16; stale cache rows are random bf16 bits)",
             "config": {"workload": w.name, "shape": w.note, "l2": "flushed between steps "
-                       "(512 MB write, outside the timed events)",
+                       "(512 MB write then 256 MB read, outside the timed events)",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
             "roofline": roofline(w.kind, main.units["main"], kms, peaks, peak_kind, w.name),
             "cpu_baseline": cpu,

@@ -122,10 +122,10 @@ size_t fa_decode_workspace_size(int64_t B, int64_t S_kv_max, int64_t num_heads,
  *   k, v padded caches [B, num_kv_heads, S_kv_max, D] or [B, S_kv_max, num_kv_heads, D]
  *   key_mask            NULL or device uint8 [B, S_kv_max] (nonzero = excluded)
  *   actual_seq_lengths  HOST int64 [B], required, each in [0, S_kv_max]
- *   num_splits          0: the library picks the KV chunk size from the SM
- *                       count and the lengths; n > 0: chunks of
- *                       ceil(S_kv_max / n) rows rounded up to a multiple of 64,
- *                       so a full-length sequence is cut into about n chunks
+ *   num_splits          0: one equal share of all K/V rows per SM (see
+ *                       fa_decode_plan); n > 0: shares of ceil(S_kv_max / n)
+ *                       rows rounded up to a multiple of 64, so a
+ *                       full-length sequence is cut into about n pieces
  *   out                 device bf16 [B, num_heads, D] (either layout)
  *   lse                 NULL or device fp32 [B, num_heads]
  *   workspace           device, >= fa_decode_workspace_size(..., num_splits)
@@ -139,12 +139,19 @@ fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* 
                     size_t workspace_bytes, void* stream);
 
 /* The decode split plan for these arguments (pure host computation, no
- * CUDA call): chunk_rows = KV rows per chunk, num_chunks = total (batch,
- * chunk) work items, max_chunks = largest chunk count of any batch.
+ * CUDA call). Every (batch, KV head, group of query heads handled together)
+ * is a unit of L_b key rows; the units are laid end to end and cut into
+ * equal contiguous shares, one per CTA (the load-balancing idea of the
+ * FlashAttn guide §4, SectionStreamK; splitting S2 when B*N2 is small,
+ * aclnnIncreFlashAttention guide §8.2). A unit crossed by share boundaries
+ * is computed in pieces that are merged by their log-sum-exp.
+ *   chunk_rows  rows per share: with num_splits = 0, the total divided by
+ *               num_sms (at least 224); with n > 0, ceil(S_kv_max / n)
+ *               rounded up to a multiple of 64
+ *   num_chunks  number of shares (CTAs)
+ *   max_chunks  largest number of pieces of one unit
  * num_sms is the SM count the plan is made for (fa_decode passes the
- * device's). Aims at a few waves of equal chunks over the SMs, in the spirit
- * of aclnnIncreFlashAttention guide §8.2 (split S2 when B*N2 is small) and
- * §8.5 (balance by the actual lengths). */
+ * device's). */
 fa_status fa_decode_plan(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t num_kv_heads,
                          int64_t D, const int64_t* actual_seq_lengths, int num_sms,
                          int num_splits, int64_t* chunk_rows, int64_t* num_chunks,

@@ -138,44 +138,66 @@ def _plan(lens, S, Hq, Hkv, sms=152, splits=0, D=128):
     return F.fa_decode_plan(lens, S, Hq, Hkv, D, sms, splits)
 
 
-def test_plan_covers_every_row_with_equal_chunks(lib):
+def _heads_per_cta(g, D):
+    if D == 64 and g % 8 == 0:
+        return 8
+    return 4 if g % 4 == 0 else 2 if g % 2 == 0 else 1
+
+
+def _pieces(lens, Hq, Hkv, D, rc):
+    """Brute force: pieces per (batch, KV head, head group) unit when the
+    units are laid end to end and cut every rc rows."""
+    g = Hq // Hkv
+    KH = Hkv * (g // _heads_per_cta(g, D))
+    out, pos = [], 0
+    for L in lens:
+        for _ in range(KH):
+            if L:
+                out.append(len(range(pos // rc, (pos + L - 1) // rc + 1)))
+            pos += L
+    return out, pos
+
+
+def test_plan_cuts_equal_shares(lib):
     import random
     rng = random.Random(5)
-    for _ in range(50):
+    for _ in range(60):
         B = rng.randint(1, 16)
         S = rng.randint(1, 20000)
         lens = [rng.randint(0, S) for _ in range(B)]
         Hkv = rng.choice([1, 2, 8, 32])
         Hq = Hkv * rng.choice([1, 2, 4, 8])
-        chunk, n, mx = _plan(lens, S, Hq, Hkv, D=rng.choice([64, 128]))
-        assert chunk % 64 == 0 and chunk >= 128
-        assert n == sum(math.ceil(L / chunk) for L in lens)
-        assert mx == max(math.ceil(L / chunk) for L in lens)
-        assert mx <= math.ceil(S / 128)  # fits the size query's bound
+        D = rng.choice([64, 128])
+        rc, n, mx = _plan(lens, S, Hq, Hkv, D=D)
+        pieces, total = _pieces(lens, Hq, Hkv, D, rc)
+        assert rc >= 224 and n == math.ceil(total / rc) and n <= 152
+        assert mx == (max(pieces) if pieces else 0)
+        assert mx <= math.ceil(S / 224) + 1  # fits the size query's bound
 
 
-def test_plan_targets_a_few_waves():
-    # GQA decode workload shape: 8 x 8 KV heads, lengths ~U[1024, 8192]
+def test_plan_one_share_per_sm():
+    # GQA decode workload shape: 8 batches x 8 KV heads, lengths ~U[1024, 8192]
     lens = [1024, 8192, 4000, 6000, 3000, 7777, 2048, 5000]
-    chunk, n, _ = _plan(lens, 8192, 32, 8)
-    ctas = n * 8
-    assert 2 * 152 <= ctas <= 8 * 152
-    # one long sequence, 32 heads: split so every SM gets work
-    chunk, n, _ = _plan([131072], 131072, 32, 32)
-    assert n * 32 >= 152 * 2
+    rc, n, mx = _plan(lens, 8192, 32, 8)
+    assert n == 152 and rc * 152 >= 8 * sum(lens) > rc * 151
+    # one long sequence, 32 heads: every SM streams an equal share
+    rc, n, mx = _plan([131072], 131072, 32, 32)
+    assert n == 152 and mx == max(_pieces([131072], 32, 32, 128, rc)[0])
+    assert mx <= math.ceil(131072 / rc) + 1
 
 
 def test_plan_with_forced_splits():
-    chunk, n, mx = _plan([131072], 131072, 32, 32, splits=128)
-    assert (chunk, n, mx) == (1024, 128, 128)
-    chunk, n, mx = _plan([131072], 131072, 32, 32, splits=1024)
-    assert (chunk, n, mx) == (128, 1024, 1024)
-    chunk, n, mx = _plan([1000, 0], 1000, 4, 4, splits=3)
-    assert chunk == 384 and n == 3 and mx == 3
+    rc, n, mx = _plan([131072], 131072, 32, 32, splits=128)
+    assert (rc, n, mx) == (1024, 32 * 128, 128)
+    rc, n, mx = _plan([131072], 131072, 32, 32, splits=1024)
+    assert (rc, n, mx) == (128, 32 * 1024, 1024)
+    rc, n, mx = _plan([1000, 0], 1000, 4, 4, splits=3)
+    assert (rc, n) == (384, math.ceil(4000 / 384))
+    assert mx == max(_pieces([1000, 0], 4, 4, 128, 384)[0])
 
 
 def test_plan_zero_lengths():
-    chunk, n, mx = _plan([0, 0, 0], 4096, 8, 8)
+    rc, n, mx = _plan([0, 0, 0], 4096, 8, 8)
     assert n == 0 and mx == 0
 
 
