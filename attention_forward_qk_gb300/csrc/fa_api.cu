@@ -348,7 +348,16 @@ fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* 
   const DecodeWs ws = decode_ws(B, num_heads, D, slots);
   if (workspace_bytes < ws.total) return FA_ERR_WORKSPACE_TOO_SMALL;
 
-  std::vector<long long> prefix(B + 1, 0);
+  // length prefix sums: on the stack for batches that travel in the launch
+  // parameters, on the heap only for larger ones
+  long long prefix_small[kDecodeParamBatches + 1];
+  std::vector<long long> prefix_big;
+  long long* prefix = prefix_small;
+  if (B > kDecodeParamBatches) {
+    prefix_big.resize(B + 1);
+    prefix = prefix_big.data();
+  }
+  prefix[0] = 0;
   bool has_empty = false;
   for (int64_t b = 0; b < B; ++b) {
     prefix[b + 1] = prefix[b] + lens[b];
@@ -359,7 +368,7 @@ fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned char* wsb = static_cast<unsigned char*>(workspace);
   const bool in_params = B <= kDecodeParamBatches;
-  if (!in_params && cudaMemcpyAsync(wsb + ws.prefix, prefix.data(), prefix.size() * sizeof(long long),
+  if (!in_params && cudaMemcpyAsync(wsb + ws.prefix, prefix, (B + 1) * sizeof(long long),
                                     cudaMemcpyHostToDevice, s) != cudaSuccess)
     return FA_ERR_RUNTIME;
   const int64_t total = KH * prefix[B];
@@ -383,7 +392,7 @@ fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* 
   x.rows_per_cta = rc;
   x.max_slots = static_cast<int>(slots);
   x.needs_merge = has_empty || max_slots > 1;
-  x.prefix_host = prefix.data();
+  x.prefix_host = prefix;
   x.prefix_dev = in_params ? nullptr : reinterpret_cast<const long long*>(wsb + ws.prefix);
   x.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
   x.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
