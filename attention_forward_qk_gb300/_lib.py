@@ -45,6 +45,9 @@ SIGNATURES = {
                                       ctypes.POINTER(_i64)]),
     "fa_workspace_status": (ctypes.c_int, [_vp, _vp]),
     "fa_selftest_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_uint64, _vp]),
+    "fa_decode_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                         ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp, _vp,
+                                         _vp]),
     "fa_set_main_kernel_events": (None, [_vp, _vp]),
     "fa_kernel_launch_count": (ctypes.c_uint64, []),
 }

@@ -168,6 +168,29 @@ def fa_decode(q, k, v, actual_seq_lengths, *, key_mask=None, scale=1.0, layout="
     return out, lse
 
 
+def fa_decode_noalloc(q, k, v, actual_seq_lengths, *, key_mask=None, scale=1.0, layout="BNSD",
+                      num_splits=0, out=None, lse=None, return_lse=True, stream=None):
+    """fa_decode on the library's own device scratch (no workspace argument):
+    for callers that cannot allocate device memory. Returns (out, lse)."""
+    lid = _layout_id(layout)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n)
+    B, Hq, S_q, D = _dims(q, lid)
+    _, Hkv, S_kv, _ = _dims(k, lid)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=q.device)
+    lens_arr, _ = _lens_array(actual_seq_lengths, B)
+    st = _lib.load().fa_decode_noalloc(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(),
+        key_mask.data_ptr() if key_mask is not None else None, lens_arr, B, S_kv, Hq, Hkv, D,
+        float(scale), lid, int(num_splits), out.data_ptr(),
+        lse.data_ptr() if lse is not None else None, _stream_ptr(stream))
+    check(st, "fa_decode_noalloc")
+    return out, lse
+
+
 def fa_workspace_status(workspace, stream=None) -> int:
     """Synchronise the stream and read/clear the workspace's device status word."""
     return int(_lib.load().fa_workspace_status(workspace.data_ptr(), _stream_ptr(stream)))

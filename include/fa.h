@@ -157,6 +157,33 @@ fa_status fa_decode_plan(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t
                          int num_splits, int64_t* chunk_rows, int64_t* num_chunks,
                          int64_t* max_chunks);
 
+/* ------------------------------------------------------- decode, no alloc
+ * fa_decode for callers that cannot allocate device memory: for example a
+ * runtime that must not call cudaMalloc (allocation is forbidden while a
+ * stream is being captured into a CUDA graph), a plugin that may not touch
+ * its host framework's memory pool, or an embedded loader with no device
+ * allocator at all. It takes the same arguments as fa_decode minus the
+ * workspace; its scratch is one array of FA_NOALLOC_SCRATCH_BYTES in device
+ * global memory that the library owns: every GPU that loads the library
+ * holds that array until the process exits. This entry point has no
+ * counterpart on the pages; it is a packaging variant of fa_decode.
+ *   - Limits: the scratch fa_decode_workspace_size(...) reports must fit in
+ *     FA_NOALLOC_SCRATCH_BYTES, else FA_ERR_WORKSPACE_TOO_SMALL; B must be
+ *     at most 1024, else FA_ERR_PARAM_INVALID. Nothing is enqueued then.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls on a device share the one array: calls whose GPU work
+ *     overlaps (other streams, other threads) race and must be serialised by
+ *     the caller. Each call clears the part of the array it needs cleared.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call,
+ *     and no host heap allocation. */
+#define FA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+fa_status fa_decode_noalloc(const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                            const int64_t* actual_seq_lengths, int64_t B, int64_t S_kv_max,
+                            int64_t num_heads, int64_t num_kv_heads, int64_t D, float scale,
+                            int layout, int num_splits, void* out, float* lse, void* stream);
+
 /* ------------------------------------------------------------ diagnostics
  * Synchronises `stream`, then reads and clears the device status word at
  * the start of a workspace used by fa_forward / fa_decode. Returns FA_OK,
