@@ -15,9 +15,10 @@
 // Warp roles (384 threads, three warpgroups):
 //   warps 0-3  softmax of Q0 (thread i <-> query row i <-> TMEM lane i)
 //   warps 4-7  softmax of Q1
-//   warp 8     TMA producer: Q0/Q1 once, then K_j, V_j through a 4-slot ring
-//   warp 9     TMEM allocator and MMA issuer (one elected lane)
-//   warps 10-11 idle (they complete the third warpgroup for setmaxnreg)
+//   warp 8     TMA producer: Q0/Q1 once, then K_j, V_j through a 5-slot ring
+//   warp 9     TMEM allocator and MMA issue stream of Q0 (one lane)
+//   warp 10    MMA issue stream of Q1 (the two streams take turns)
+//   warp 11    idle (it completes the third warpgroup for setmaxnreg)
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
 // P_t (bf16, two per column) overwrites the first 64 columns of S_t and is
 // the A operand of O_t += P_t V_j straight from TMEM.
@@ -40,15 +41,15 @@ namespace {
 
 constexpr int kBM = 128;        // query rows per Q tile
 constexpr int kBN = 128;        // keys per KV tile
-constexpr int kRing = 4;        // K/V ring slots
+constexpr int kRing = 5;        // K/V ring slots (tiles of K or V)
 constexpr int kThreads = 384;   // three warpgroups
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;     // warps 10-11 only complete the third warpgroup
+constexpr int kMmaWarp = 9;     // MMA issue for Q0 (warp 10 for Q1); warp 11 idle
 // Register split (setmaxnreg): the launch gives 168 per thread (384 x 168 =
-// 64512); the softmax warpgroups take 224 each and the load/MMA warpgroup 56:
-// 128 x (224 + 224 + 56) = 64512.
-constexpr int kSoftmaxRegs = 224;
-constexpr int kControlRegs = 56;
+// 64512); the softmax warpgroups take 216 each and the load/MMA warpgroup 72:
+// 128 x (216 + 216 + 72) = 64512.
+constexpr int kSoftmaxRegs = 216;
+constexpr int kControlRegs = 72;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when m grows by > 2^8
 
 template <int D>
@@ -84,8 +85,8 @@ enum : int {
   kBarPReady = kBarSFull + 2,
   kBarOFinal = kBarPReady + 2,
   kBarFix = kBarOFinal + 2,
-  kBarDrain = kBarFix + 1,
-  kNumBars = kBarDrain + 1
+  kBarDrain = kBarFix + 1,         // + issue stream
+  kNumBars = kBarDrain + 2
 };
 
 struct TileSeq {
@@ -117,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* turn = reinterpret_cast<volatile int*>(tmem_slot + 2);  // MMA issue turn
   auto bar = [&](int i) -> uint32_t { return smem_u32(bars + i); };
 
   const int tid = threadIdx.x;
@@ -152,9 +154,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t cnt = 1;
       if (i == kBarPReady || i == kBarPReady + 1) cnt = kBM;
+      if (i >= kBarKvEmpty && i < kBarKvEmpty + kRing) cnt = 2;  // both issue streams
       mbar_init(bar(i), cnt);
     }
     *abort_flag = 0;
+    *turn = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -258,8 +262,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                kDevTimeoutDrain, nullptr);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ================================================================ MMA
+    // Two issue streams, one per Q tile, that take turns: stream t issues
+    // PV_t(j) then S_t(j+1) and hands the turn to the other. One thread
+    // cannot issue 128x128x16 MMAs much faster than the tensor core retires
+    // them, so a barrier wait inside a single stream leaves the pipe idle;
+    // here each stream does its waits (V_j, P_t(j), K_j+1) while the other
+    // one is issuing. The turn order keeps the pipe order of one stream
+    // (S0 S1 | PV0 S0' | PV1 S1' | ...), so one tile's softmax still runs
+    // while the tensor core works on the other tile. Each stream is in
+    // order, which keeps S_t(j+1) behind the P_t(j) V_j product that reads
+    // the aliased columns; the streams share no TMEM. Both streams wait for
+    // and release every ring item (kv_empty counts two arrivals), so neither
+    // runs a full ring ahead of the other.
+    const int t = warp - kMmaWarp;
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, 0, 1);
@@ -267,44 +284,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ring_base = smem_u32(smem + C::kRingOff);
       bool ok = mbar_wait(bar(kBarQ), 0, a.timeout_ns, a.status, kDevTimeoutQ, abort_flag);
       tc_fence_after();
-      auto issue_s = [&](int t, uint32_t k_addr) {
-        const uint32_t d_tmem = tmem + t * 128;
+      // Descriptor bases built once; an MMA adds a constant to the 14-bit
+      // address field (addresses stay below 256 KB, so the add never carries
+      // out of the field). K-major tiles advance 32 B per 16-element k-step
+      // inside a 128-byte swizzle row and 16 KB per 64-column slab; the
+      // MN-major V operand advances 16 keys = 2 KB per k-step.
+      const uint64_t dq = smem_desc_sw128(q_base + t * C::kTileBytes, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(ring_base, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(ring_base, C::kSubBytes, 1024);
+      constexpr uint32_t kSlotStep = C::kTileBytes >> 4;
+      const uint32_t s_tmem = tmem + t * 128;
+      const uint32_t o_tmem = tmem + 256 + t * 128;
+      auto issue_s = [&](int slot) {
+        const uint64_t bk = dk0 + static_cast<uint64_t>(slot) * kSlotStep;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::kSubBytes + (kk % 4) * 32;
-          umma_ss(d_tmem, smem_desc_sw128(q_base + t * C::kTileBytes + off, 16, 1024),
-                  smem_desc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk / 4) * C::kSubBytes + (kk % 4) * 32) >> 4;
+          umma_ss(s_tmem, dq + off, bk + off, idesc_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar(kBarSFull + t));
       };
-      auto issue_pv = [&](int t, uint32_t v_addr, bool first) {
-        const uint32_t d_tmem = tmem + 256 + t * 128;
-        const uint32_t p_tmem = tmem + t * 128;
+      auto issue_pv = [&](int slot, bool first) {
+        const uint64_t bv = dv0 + static_cast<uint64_t>(slot) * kSlotStep;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts(d_tmem, p_tmem + kk * 8,
-                  smem_desc_sw128(v_addr + kk * 16 * 128, C::kSubBytes, 1024), idesc_pv,
+          umma_ts(o_tmem, s_tmem + kk * 8, bv + ((kk * 16 * 128) >> 4), idesc_pv,
                   (first && kk == 0) ? 0u : 1u);
       };
+      // bounded wait for this stream's turn (turn 2r + t in round r)
+      auto take_turn = [&](int want) -> bool {
+        if (*turn == want) return true;
+        const uint64_t t0 = globaltimer_ns();
+        while (*turn != want) {
+          if (*abort_flag) return false;
+          if (globaltimer_ns() - t0 > a.timeout_ns) {
+            record_error(a.status, kDevTimeoutTurn);
+            *abort_flag = 1;
+            return false;
+          }
+        }
+        return true;
+      };
+      const int n = n_t[t];
       int item = 0;
-      int pv_count[2] = {0, 0};
+      int pv_count = 0;
       int j = seq.next(0);
-      // prologue: S of the first tile
+      // round 0: S of the first tile
       if (ok && j < seq.end) {
-        const int slot = item % kRing;
-        ok = mbar_wait(bar(kBarKvFull + slot), (item / kRing) & 1, a.timeout_ns, a.status,
-                       kDevTimeoutKvFull, abort_flag);
+        ok = mbar_wait(bar(kBarKvFull), 0, a.timeout_ns, a.status, kDevTimeoutKvFull, abort_flag);
+        if (ok) ok = take_turn(t);
         if (ok) {
           tc_fence_after();
-          const uint32_t k_addr = ring_base + slot * C::kTileBytes;
-          for (int t = 0; t < 2; ++t)
-            if (j < n_t[t]) issue_s(t, k_addr);
-          umma_commit(bar(kBarKvEmpty + slot));
+          if (j < n) issue_s(0);
+          *turn = t + 1;
+          if (j < n) umma_commit(bar(kBarSFull + t));
+          umma_commit(bar(kBarKvEmpty));
         }
       }
-      for (int t = 0; t < 2; ++t)  // a tile that sees no key at all
-        if ((t == 0 || has_t1) && !(j < n_t[t])) umma_commit(bar(kBarOFinal + t));
-      while (ok && j < seq.end) {
+      if ((t == 0 || has_t1) && !(j < n)) umma_commit(bar(kBarOFinal + t));  // sees no key
+      for (int r = 1; ok && j < seq.end; ++r) {
         const int v_item = item + 1;
         const int v_slot = v_item % kRing;
         const int jn = seq.next(j + 1);
@@ -312,33 +349,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int k_slot = k_item % kRing;
         ok = mbar_wait(bar(kBarKvFull + v_slot), (v_item / kRing) & 1, a.timeout_ns, a.status,
                        kDevTimeoutKvFull, abort_flag);
+        if (ok && j < n)
+          ok = mbar_wait(bar(kBarPReady + t), pv_count & 1, a.timeout_ns, a.status,
+                         kDevTimeoutPReady, abort_flag);
+        if (ok && jn < seq.end)
+          ok = mbar_wait(bar(kBarKvFull + k_slot), (k_item / kRing) & 1, a.timeout_ns, a.status,
+                         kDevTimeoutKvFull, abort_flag);
+        if (ok) ok = take_turn(2 * r + t);
         if (!ok) break;
         tc_fence_after();
-        bool k_ready = false;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (!(j < n_t[t])) continue;
-          ok = mbar_wait(bar(kBarPReady + t), pv_count[t] & 1, a.timeout_ns, a.status,
-                         kDevTimeoutPReady, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(t, ring_base + v_slot * C::kTileBytes, pv_count[t] == 0);
-          ++pv_count[t];
-          if (jn < n_t[t]) {
-            if (!k_ready) {
-              ok = mbar_wait(bar(kBarKvFull + k_slot), (k_item / kRing) & 1, a.timeout_ns,
-                             a.status, kDevTimeoutKvFull, abort_flag);
-              if (!ok) break;
-              tc_fence_after();
-              k_ready = true;
-            }
-            issue_s(t, ring_base + k_slot * C::kTileBytes);
-          } else {
-            umma_commit(bar(kBarOFinal + t));
-          }
-        }
-        if (!ok) break;
+        if (j < n) issue_pv(v_slot, pv_count == 0);
+        if (jn < n) issue_s(k_slot);
+        *turn = 2 * r + t + 1;
+        if (j < n) ++pv_count;
+        if (jn < n) umma_commit(bar(kBarSFull + t));
+        if (j < n && !(jn < n)) umma_commit(bar(kBarOFinal + t));
         umma_commit(bar(kBarKvEmpty + v_slot));
-        if (k_ready) umma_commit(bar(kBarKvEmpty + k_slot));
+        if (jn < seq.end) umma_commit(bar(kBarKvEmpty + k_slot));
         item += 2;
         j = jn;
       }
@@ -367,18 +394,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       uint32_t sr[4][32];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(s_tmem + q4 * 32, sr[q4]);
-      tmem_ld_wait();
+      // per-element path: masked tiles, and a negative scale (whose row max is
+      // the scale times the row min)
       const bool masked = (a.causal && j * kBN + kBN - 1 > q_row0 + t * kBM) ||
-                          ((j + 1) * kBN > a.S_kv) || !seq.full(j);
+                          ((j + 1) * kBN > a.S_kv) || !seq.full(j) || c < 0.f;
       float tmax = -INFINITY;
       if (masked) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(s_tmem + q4 * 32, sr[q4]);
+        tmem_ld_wait();
         uint32_t words[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
         if (seq.bits != nullptr) {
           const uint4 w = __ldg(reinterpret_cast<const uint4*>(seq.bits) + j);
           words[0] = w.x; words[1] = w.y; words[2] = w.z; words[3] = w.w;
         }
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
 #pragma unroll
@@ -387,10 +417,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool valid = ((words[q4] >> i) & 1u) && key < a.S_kv && (!a.causal || key <= row);
             const float tv = valid ? __uint_as_float(sr[q4][i]) * c : -INFINITY;
             sr[q4][i] = __float_as_uint(tv);
-            tmax = fmaxf(tmax, tv);
+            mx[q4] = fmaxf(mx[q4], tv);
           }
         }
-      } else if (c >= 0.f) {
+        tmax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      } else {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(s_tmem + q4 * 32, sr[q4]);
+        tmem_ld_wait();
         float mx = -INFINITY;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
@@ -398,14 +432,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; i += 2)
             mx = fmax3(mx, __uint_as_float(sr[q4][i]), __uint_as_float(sr[q4][i + 1]));
         tmax = mx * c;
-      } else {
-        float mn = INFINITY;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-          for (int i = 0; i < 32; i += 2)
-            mn = fmin3(mn, __uint_as_float(sr[q4][i]), __uint_as_float(sr[q4][i + 1]));
-        tmax = mn * c;
       }
       // conditional rescale: keep the reference max unless it grows by > 2^8
       const float m_cand = fmaxf(m_run, tmax);
@@ -435,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[qq * 16 + i / 2] = pack_bf16x2(p0, p1);
           }
         }
-        tmem_st32(s_tmem + half * 32, pk);  // P overwrites S columns already read
+        tmem_st32(s_tmem + half * 32, pk);
       }
       const float2 rsp = unpair(rs2);
       const float rsum = rsp.x + rsp.y;
@@ -469,27 +495,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         __nv_bfloat16* dst = a.out + static_cast<long long>(b) * a.out_batch_stride +
                              static_cast<long long>(h) * a.out_head_stride +
                              static_cast<long long>(row) * a.out_row_stride;
+        // the whole O row in one round of TMEM loads
+        uint32_t orr[D / 32][32];
 #pragma unroll
-        for (int q4 = 0; q4 < D / 32; ++q4) {
-          uint32_t orr[32];
-          tmem_ld32(o_tmem + q4 * 32, orr);
-          tmem_ld_wait();
-          if (row_ok) {
+        for (int q4 = 0; q4 < D / 32; ++q4) tmem_ld32(o_tmem + q4 * 32, orr[q4]);
+        tmem_ld_wait();
+        if (row_ok) {
+#pragma unroll
+          for (int q4 = 0; q4 < D / 32; ++q4) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + q4 * 32);
-#pragma unroll
             // an invalid row writes exact zeros: its O columns may never have
             // been written by an MMA
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              orr[i] = invalid ? 0u : __float_as_uint(__uint_as_float(orr[i]) * inv_l);
-#pragma unroll
             for (int i = 0; i < 32; i += 8) {
-              uint4 u;
-              u.x = pack_bf16x2(__uint_as_float(orr[i]), __uint_as_float(orr[i + 1]));
-              u.y = pack_bf16x2(__uint_as_float(orr[i + 2]), __uint_as_float(orr[i + 3]));
-              u.z = pack_bf16x2(__uint_as_float(orr[i + 4]), __uint_as_float(orr[i + 5]));
-              u.w = pack_bf16x2(__uint_as_float(orr[i + 6]), __uint_as_float(orr[i + 7]));
-              d4[i / 8] = u;
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                f[e] = invalid ? 0.f : __uint_as_float(orr[q4][i + e]) * inv_l;
+              d4[i / 8] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                     pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
             }
           }
         }
@@ -503,15 +527,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- teardown: every role is done with TMEM and shared memory
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     tc_fence_after();
     if (*abort_flag && lane == 0) {
-      // in-flight MMAs retire in order: one last commit covers all of them
-      umma_commit(bar(kBarDrain));
-      mbar_wait(bar(kBarDrain), 0, a.timeout_ns, a.status, kDevTimeoutDrain, nullptr);
+      // in-flight MMAs of this stream retire in order: one commit covers them
+      const int t = warp - kMmaWarp;
+      umma_commit(bar(kBarDrain + t));
+      mbar_wait(bar(kBarDrain + t), 0, a.timeout_ns, a.status, kDevTimeoutDrain, nullptr);
     }
     __syncwarp();
-    tmem_dealloc(tmem, 512);
+    asm volatile("bar.sync 1, 64;" ::: "memory");  // both streams drained
+    if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
   }
 }
 

@@ -23,6 +23,7 @@ enum DeviceError : uint32_t {
   kDevTimeoutPReady = 0x105,
   kDevTimeoutOFinal = 0x106,
   kDevTimeoutDrain = 0x107,
+  kDevTimeoutTurn = 0x108,
   kDevTimeoutDecodeFull = 0x201,
   kDevTimeoutDecodeEmpty = 0x202,
   kDevTimeoutProbe = 0x301,
