@@ -422,16 +422,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
       } else {
+        // row max with 8 independent accumulators; the first half's max runs
+        // while the second half is still being read out of TMEM
+        float mx[8];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(s_tmem + q4 * 32, sr[q4]);
+        for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+        tmem_ld32(s_tmem, sr[0]);
+        tmem_ld32(s_tmem + 32, sr[1]);
         tmem_ld_wait();
-        float mx = -INFINITY;
+        tmem_ld32(s_tmem + 64, sr[2]);
+        tmem_ld32(s_tmem + 96, sr[3]);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
+        for (int q4 = 0; q4 < 2; ++q4)
 #pragma unroll
           for (int i = 0; i < 32; i += 2)
-            mx = fmax3(mx, __uint_as_float(sr[q4][i]), __uint_as_float(sr[q4][i + 1]));
-        tmax = mx * c;
+            mx[(q4 * 16 + i / 2) % 8] = fmax3(mx[(q4 * 16 + i / 2) % 8], __uint_as_float(sr[q4][i]),
+                                              __uint_as_float(sr[q4][i + 1]));
+        tmem_ld_wait();
+#pragma unroll
+        for (int q4 = 2; q4 < 4; ++q4)
+#pragma unroll
+          for (int i = 0; i < 32; i += 2)
+            mx[(q4 * 16 + i / 2) % 8] = fmax3(mx[(q4 * 16 + i / 2) % 8], __uint_as_float(sr[q4][i]),
+                                              __uint_as_float(sr[q4][i + 1]));
+        tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * c;
       }
       // conditional rescale: keep the reference max unless it grows by > 2^8
       const float m_cand = fmaxf(m_run, tmax);
@@ -443,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       // p = 2^(s*c - m): packed f32x2 FMA, then ex2; row sum in two packed lanes
-      uint64_t rs2 = 0ull;
+      uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};  // independent row-sum chains
       const uint64_t c2 = masked ? pair_f32(1.f, 1.f) : pair_f32(c, c);
       const uint64_t nm2 = pair_f32(-m_use, -m_use);
 #pragma unroll
@@ -457,14 +471,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float2 t2 = unpair(ffma2(pair_u32(sr[q4][i], sr[q4][i + 1]), c2, nm2));
             const float p0 = ex2(t2.x);
             const float p1 = ex2(t2.y);
-            rs2 = fadd2(rs2, pair_f32(p0, p1));
+            rs2[(i / 2) % 4] = fadd2(rs2[(i / 2) % 4], pair_f32(p0, p1));
             pk[qq * 16 + i / 2] = pack_bf16x2(p0, p1);
           }
         }
         tmem_st32(s_tmem + half * 32, pk);
       }
-      const float2 rsp = unpair(rs2);
-      const float rsum = rsp.x + rsp.y;
+      const float2 rsa = unpair(fadd2(rs2[0], rs2[1]));
+      const float2 rsb = unpair(fadd2(rs2[2], rs2[3]));
+      const float rsum = (rsa.x + rsa.y) + (rsb.x + rsb.y);
       l_run = l_run * alpha + rsum;
       if (k > 0 && __any_sync(0xffffffffu, need)) {
         // O_t was complete when S_t(j) landed (tcgen05 ops retire in order)
