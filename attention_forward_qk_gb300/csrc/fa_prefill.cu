@@ -33,6 +33,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <algorithm>
+
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
 
@@ -71,21 +73,23 @@ struct PrefillArgs {
   uint32_t* status;
   uint64_t timeout_ns;
   int B, Hq, Hkv, S_q, S_kv, causal;
-  int n_qpairs, n_kv_tiles;
+  int n_qpairs, n_kv_tiles, n_items;
   long long out_row_stride, out_head_stride, out_batch_stride;  // elements
   float scale_log2;
 };
 
 // Barrier slots (8 bytes each) after the tiles.
 enum : int {
-  kBarQ = 0,
-  kBarKvFull = 1,                 // + slot
+  kBarQ = 0,                        // Q tiles of the current work item landed
+  kBarQFree = 1,                    // both streams' S products of the item done
+  kBarKvFull = 2,                   // + slot
   kBarKvEmpty = kBarKvFull + kRing,
   kBarSFull = kBarKvEmpty + kRing,  // + tile
-  kBarPReady = kBarSFull + 2,
-  kBarOFinal = kBarPReady + 2,
-  kBarFix = kBarOFinal + 2,
-  kBarDrain = kBarFix + 1,         // + issue stream
+  kBarPReady = kBarSFull + 2,       // + tile
+  kBarOFinal = kBarPReady + 2,      // + tile
+  kBarODrained = kBarOFinal + 2,    // + tile: the epilogue has read O_t
+  kBarFix = kBarODrained + 2,
+  kBarDrain = kBarFix + 1,          // + issue stream
   kNumBars = kBarDrain + 2
 };
 
@@ -107,6 +111,41 @@ struct TileSeq {
   }
 };
 
+// One work item: 256 consecutive query rows (two 128-row tiles) of one
+// (batch, query head). Items are numbered KV-head-major: all query pairs of
+// the g query heads of one (batch, KV head) are consecutive, heaviest (last)
+// pairs first and heads innermost, so the items in flight at any time read
+// the same K/V tiles out of L2.
+struct WorkItem {
+  int b, kvh, h, q_row0;
+  bool has_t1;
+  int n_t[2];  // KV tiles each Q tile needs (a prefix of the tile sequence)
+  TileSeq seq;
+};
+
+__device__ __forceinline__ WorkItem work_item(const PrefillArgs& a, int w) {
+  WorkItem it;
+  const int g = a.Hq / a.Hkv;
+  const int per_kv = a.n_qpairs * g;
+  const int bkv = w / per_kv;
+  const int rem = w % per_kv;
+  const int qp = a.n_qpairs - 1 - rem / g;
+  it.b = bkv / a.Hkv;
+  it.kvh = bkv % a.Hkv;
+  it.h = it.kvh * g + rem % g;
+  it.q_row0 = qp * 2 * kBM;
+  it.has_t1 = it.q_row0 + kBM < a.S_q;
+  for (int t = 0; t < 2; ++t) {
+    int n = a.n_kv_tiles;
+    if (a.causal) n = min(n, (it.q_row0 + t * kBM) / kBN + 1);
+    if (t == 1 && !it.has_t1) n = 0;
+    it.n_t[t] = n;
+  }
+  it.seq.bits = a.tile_bits ? a.tile_bits + static_cast<size_t>(it.b) * a.n_kv_tiles * 4 : nullptr;
+  it.seq.end = max(it.n_t[0], it.n_t[1]);
+  return it;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -125,36 +164,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  // ---- work tile. Consecutive CTAs share one (batch, KV head): all query
-  // pairs of its g query heads, heaviest (last) pairs first, heads innermost,
-  // so the CTAs resident at any time read the same K/V tiles out of L2.
-  const int g = a.Hq / a.Hkv;
-  const int per_kv = a.n_qpairs * g;
-  const int bkv = static_cast<int>(blockIdx.x) / per_kv;
-  const int rem = static_cast<int>(blockIdx.x) % per_kv;
-  const int qp = a.n_qpairs - 1 - rem / g;
-  const int b = bkv / a.Hkv;
-  const int kvh = bkv % a.Hkv;
-  const int h = kvh * g + rem % g;
-  const int q_row0 = qp * 2 * kBM;
-  const bool has_t1 = q_row0 + kBM < a.S_q;
-  // KV tiles each Q tile needs (a prefix of the tile sequence)
-  int n_t[2];
-  for (int t = 0; t < 2; ++t) {
-    int n = a.n_kv_tiles;
-    if (a.causal) n = min(n, (q_row0 + t * kBM) / kBN + 1);
-    if (t == 1 && !has_t1) n = 0;
-    n_t[t] = n;
-  }
-  TileSeq seq;
-  seq.bits = a.tile_bits ? a.tile_bits + static_cast<size_t>(b) * a.n_kv_tiles * 4 : nullptr;
-  seq.end = max(n_t[0], n_t[1]);
+  // ---- persistent schedule: this CTA takes work items r*G + c (even rounds)
+  // and r*G + G-1-c (odd rounds). With items of one KV head ordered heaviest
+  // first, the snake pairs heavy with light items, which evens out the causal
+  // cost per CTA.
+  const int G = static_cast<int>(gridDim.x);
+  const int cta = static_cast<int>(blockIdx.x);
+  auto item_of = [&](int r) -> int { return r * G + ((r & 1) ? (G - 1 - cta) : cta); };
 
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t cnt = 1;
       if (i == kBarPReady || i == kBarPReady + 1) cnt = kBM;
+      if (i == kBarODrained || i == kBarODrained + 1) cnt = kBM;
       if (i >= kBarKvEmpty && i < kBarKvEmpty + kRing) cnt = 2;  // both issue streams
+      if (i == kBarQFree) cnt = 2;                                // both issue streams
       mbar_init(bar(i), cnt);
     }
     *abort_flag = 0;
@@ -180,18 +204,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&tm_q);
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
-      const int nq = has_t1 ? 2 : 1;
-      mbar_expect_tx(bar(kBarQ), nq * C::kTileBytes);
-      for (int t = 0; t < nq; ++t)
-        for (int s = 0; s < D / 64; ++s)
-          tma_load_4d(smem_u32(smem + C::kQOff + t * C::kTileBytes + s * C::kSubBytes), &tm_q,
-                      bar(kBarQ), s * 64, q_row0 + t * kBM, h, b);
     }
-    __syncwarp();
     int item = 0;  // ring items issued so far (K_j and V_j are one item each)
     int fixes = 0;
     bool ok = true;
-    for (int j = seq.next(0); ok && j < seq.end; j = seq.next(j + 1)) {
+    for (int r = 0; ok; ++r) {
+      const int w = item_of(r);
+      if (w >= a.n_items) break;
+      const WorkItem wi = work_item(a, w);
+      const int b = wi.b, kvh = wi.kvh;
+      const TileSeq& seq = wi.seq;
+      if (r > 0) {
+        // the Q region is free once both streams' S products of the last item are done
+        ok = mbar_wait(bar(kBarQFree), (r - 1) & 1, a.timeout_ns, a.status, kDevTimeoutQ,
+                       abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      if (lane == 0) {
+        const int nq = wi.has_t1 ? 2 : 1;
+        mbar_expect_tx(bar(kBarQ), nq * C::kTileBytes);
+        for (int t = 0; t < nq; ++t)
+          for (int s = 0; s < D / 64; ++s)
+            tma_load_4d(smem_u32(smem + C::kQOff + t * C::kTileBytes + s * C::kSubBytes), &tm_q,
+                        bar(kBarQ), s * 64, wi.q_row0 + t * kBM, wi.h, b);
+      }
+      __syncwarp();
+      for (int j = seq.next(0); ok && j < seq.end; j = seq.next(j + 1)) {
       const bool fix_v = !seq.full(j);
       for (int kv = 0; kv < 2; ++kv) {
         const int slot = item % kRing;
@@ -244,9 +283,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
     }
+    }
     if (ok) {
-      // tail: wait until the MMA warp has released the last ring slots, so no
-      // asynchronous arrival can reach this CTA's shared memory after exit
+      // tail: wait until the MMA warps have released the last ring slots, so
+      // no asynchronous arrival can reach this CTA's shared memory after exit
       for (int it = max(0, item - kRing); it < item && ok; ++it) {
         ok = mbar_wait(bar(kBarKvEmpty + it % kRing), (it / kRing) & 1, a.timeout_ns, a.status,
                        kDevTimeoutKvEmpty, abort_flag);
@@ -282,8 +322,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, 0, 1);
       const uint32_t q_base = smem_u32(smem + C::kQOff);
       const uint32_t ring_base = smem_u32(smem + C::kRingOff);
-      bool ok = mbar_wait(bar(kBarQ), 0, a.timeout_ns, a.status, kDevTimeoutQ, abort_flag);
-      tc_fence_after();
       // Descriptor bases built once; an MMA adds a constant to the 14-bit
       // address field (addresses stay below 256 KB, so the add never carries
       // out of the field). K-major tiles advance 32 B per 16-element k-step
@@ -310,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ts(o_tmem, s_tmem + kk * 8, bv + ((kk * 16 * 128) >> 4), idesc_pv,
                   (first && kk == 0) ? 0u : 1u);
       };
-      // bounded wait for this stream's turn (turn 2r + t in round r)
+      // bounded wait for this stream's turn (turn 2u + t in issue round u)
       auto take_turn = [&](int want) -> bool {
         if (*turn == want) return true;
         const uint64_t t0 = globaltimer_ns();
@@ -324,50 +362,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
-      const int n = n_t[t];
-      int item = 0;
-      int pv_count = 0;
-      int j = seq.next(0);
-      // round 0: S of the first tile
-      if (ok && j < seq.end) {
-        ok = mbar_wait(bar(kBarKvFull), 0, a.timeout_ns, a.status, kDevTimeoutKvFull, abort_flag);
-        if (ok) ok = take_turn(t);
-        if (ok) {
-          tc_fence_after();
-          if (j < n) issue_s(0);
-          *turn = t + 1;
-          if (j < n) umma_commit(bar(kBarSFull + t));
-          umma_commit(bar(kBarKvEmpty));
-        }
-      }
-      if ((t == 0 || has_t1) && !(j < n)) umma_commit(bar(kBarOFinal + t));  // sees no key
-      for (int r = 1; ok && j < seq.end; ++r) {
-        const int v_item = item + 1;
-        const int v_slot = v_item % kRing;
-        const int jn = seq.next(j + 1);
-        const int k_item = item + 2;
-        const int k_slot = k_item % kRing;
-        ok = mbar_wait(bar(kBarKvFull + v_slot), (v_item / kRing) & 1, a.timeout_ns, a.status,
-                       kDevTimeoutKvFull, abort_flag);
-        if (ok && j < n)
-          ok = mbar_wait(bar(kBarPReady + t), pv_count & 1, a.timeout_ns, a.status,
-                         kDevTimeoutPReady, abort_flag);
-        if (ok && jn < seq.end)
-          ok = mbar_wait(bar(kBarKvFull + k_slot), (k_item / kRing) & 1, a.timeout_ns, a.status,
-                         kDevTimeoutKvFull, abort_flag);
-        if (ok) ok = take_turn(2 * r + t);
+      int item = 0;      // ring items consumed so far
+      int pv_count = 0;  // P_t tiles consumed so far (all work items)
+      int u = 0;         // issue rounds so far (both streams run the same rounds)
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int w = item_of(r);
+        if (w >= a.n_items) break;
+        const WorkItem wi = work_item(a, w);
+        const TileSeq& seq = wi.seq;
+        const int n = t == 0 ? wi.n_t[0] : wi.n_t[1];
+        ok = mbar_wait(bar(kBarQ), r & 1, a.timeout_ns, a.status, kDevTimeoutQ, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        if (j < n) issue_pv(v_slot, pv_count == 0);
-        if (jn < n) issue_s(k_slot);
-        *turn = 2 * r + t + 1;
-        if (j < n) ++pv_count;
-        if (jn < n) umma_commit(bar(kBarSFull + t));
-        if (j < n && !(jn < n)) umma_commit(bar(kBarOFinal + t));
-        umma_commit(bar(kBarKvEmpty + v_slot));
-        if (jn < seq.end) umma_commit(bar(kBarKvEmpty + k_slot));
-        item += 2;
-        j = jn;
+        int j = seq.next(0);
+        bool q_freed = false;
+        bool first_pv = true;
+        // first round of the item: S of the first tile
+        if (j < seq.end) {
+          const int slot = item % kRing;
+          ok = mbar_wait(bar(kBarKvFull + slot), (item / kRing) & 1, a.timeout_ns, a.status,
+                         kDevTimeoutKvFull, abort_flag);
+          if (ok) ok = take_turn(2 * u + t);
+          if (!ok) break;
+          tc_fence_after();
+          if (j < n) issue_s(slot);
+          *turn = 2 * u + t + 1;
+          ++u;
+          if (j < n) umma_commit(bar(kBarSFull + t));
+          umma_commit(bar(kBarKvEmpty + slot));
+        }
+        // release Q once this stream's last S product of the item is issued
+        if (!(j < n) || !(seq.next(j + 1) < n)) {
+          umma_commit(bar(kBarQFree));
+          q_freed = true;
+        }
+        if (!(j < n)) umma_commit(bar(kBarOFinal + t));  // sees no key (or tile absent)
+        while (ok && j < seq.end) {
+          const int v_item = item + 1;
+          const int v_slot = v_item % kRing;
+          const int jn = seq.next(j + 1);
+          const int k_item = item + 2;
+          const int k_slot = k_item % kRing;
+          ok = mbar_wait(bar(kBarKvFull + v_slot), (v_item / kRing) & 1, a.timeout_ns, a.status,
+                         kDevTimeoutKvFull, abort_flag);
+          if (ok && j < n)
+            ok = mbar_wait(bar(kBarPReady + t), pv_count & 1, a.timeout_ns, a.status,
+                           kDevTimeoutPReady, abort_flag);
+          if (ok && j < n && first_pv && r > 0)
+            // O_t of the previous item must be read out before it is overwritten
+            ok = mbar_wait(bar(kBarODrained + t), (r - 1) & 1, a.timeout_ns, a.status,
+                           kDevTimeoutOFinal, abort_flag);
+          if (ok && jn < seq.end)
+            ok = mbar_wait(bar(kBarKvFull + k_slot), (k_item / kRing) & 1, a.timeout_ns,
+                           a.status, kDevTimeoutKvFull, abort_flag);
+          if (ok) ok = take_turn(2 * u + t);
+          if (!ok) break;
+          tc_fence_after();
+          if (j < n) issue_pv(v_slot, first_pv);
+          if (jn < n) issue_s(k_slot);
+          *turn = 2 * u + t + 1;
+          ++u;
+          if (j < n) {
+            ++pv_count;
+            first_pv = false;
+          }
+          if (jn < n) umma_commit(bar(kBarSFull + t));
+          if (jn < n && !q_freed && !(seq.next(jn + 1) < n)) {
+            umma_commit(bar(kBarQFree));
+            q_freed = true;
+          }
+          if (j < n && !(jn < n)) umma_commit(bar(kBarOFinal + t));
+          umma_commit(bar(kBarKvEmpty + v_slot));
+          if (jn < seq.end) umma_commit(bar(kBarKvEmpty + k_slot));
+          item += 2;
+          j = jn;
+        }
       }
     }
     __syncwarp();
@@ -378,16 +448,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp / 4;          // Q tile of this warpgroup
     const int wl = warp % 4;         // TMEM lane quarter
     const int row_in_tile = wl * 32 + lane;
-    const int row = q_row0 + t * kBM + row_in_tile;
     const uint32_t lane_bits = static_cast<uint32_t>(wl * 32) << 16;
     const uint32_t s_tmem = tmem + lane_bits + t * 128;
     const uint32_t o_tmem = tmem + lane_bits + 256 + t * 128;
     const float c = a.scale_log2;
-    float m_run = -INFINITY;  // reference max, log2 domain
-    float l_run = 0.f;
-    int k = 0;
+    int k = 0;  // S_t tiles consumed so far (all work items)
     bool ok = true;
-    for (int j = seq.next(0); j < n_t[t]; j = seq.next(j + 1), ++k) {
+    for (int r = 0; ok; ++r) {
+      const int w = item_of(r);
+      if (w >= a.n_items) break;
+      const WorkItem wi = work_item(a, w);
+      const TileSeq& seq = wi.seq;
+      const int q_row0 = wi.q_row0;
+      const int row = q_row0 + t * kBM + row_in_tile;
+      float m_run = -INFINITY;  // reference max, log2 domain
+      float l_run = 0.f;
+      const int n_mine = t == 0 ? wi.n_t[0] : wi.n_t[1];
+      for (int j = seq.next(0); j < n_mine; j = seq.next(j + 1), ++k) {
       ok = mbar_wait(bar(kBarSFull + t), k & 1, a.timeout_ns, a.status, kDevTimeoutSFull,
                      abort_flag);
       ok = __all_sync(0xffffffffu, ok);
@@ -496,46 +573,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(kBarPReady + t));
-    }
-    // ---- epilogue: out = O / l, lse = ln2 * (m + log2 l)
-    if (ok && (t == 0 || has_t1)) {
-      ok = mbar_wait(bar(kBarOFinal + t), 0, a.timeout_ns, a.status, kDevTimeoutOFinal,
+      }
+      if (!ok) break;
+      // ---- epilogue: out = O / l, lse = ln2 * (m + log2 l)
+      ok = mbar_wait(bar(kBarOFinal + t), r & 1, a.timeout_ns, a.status, kDevTimeoutOFinal,
                      abort_flag);
       ok = __all_sync(0xffffffffu, ok);
-      if (ok) {
-        tc_fence_after();
-        const bool row_ok = row < a.S_q;
-        const bool invalid = (l_run == 0.f);
-        const float inv_l = invalid ? 0.f : 1.f / l_run;
-        __nv_bfloat16* dst = a.out + static_cast<long long>(b) * a.out_batch_stride +
-                             static_cast<long long>(h) * a.out_head_stride +
-                             static_cast<long long>(row) * a.out_row_stride;
-        // the whole O row in one round of TMEM loads
-        uint32_t orr[D / 32][32];
+      if (!ok) break;
+      tc_fence_after();
+      // the whole O row in one round of TMEM loads, then O_t is free for the
+      // next item's products
+      uint32_t orr[D / 32][32];
 #pragma unroll
-        for (int q4 = 0; q4 < D / 32; ++q4) tmem_ld32(o_tmem + q4 * 32, orr[q4]);
-        tmem_ld_wait();
-        if (row_ok) {
+      for (int q4 = 0; q4 < D / 32; ++q4) tmem_ld32(o_tmem + q4 * 32, orr[q4]);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(bar(kBarODrained + t));
+      const bool row_ok = row < a.S_q;
+      const bool invalid = (l_run == 0.f);
+      const float inv_l = invalid ? 0.f : 1.f / l_run;
+      __nv_bfloat16* dst = a.out + static_cast<long long>(wi.b) * a.out_batch_stride +
+                           static_cast<long long>(wi.h) * a.out_head_stride +
+                           static_cast<long long>(row) * a.out_row_stride;
+      if (row_ok) {
 #pragma unroll
-          for (int q4 = 0; q4 < D / 32; ++q4) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + q4 * 32);
-            // an invalid row writes exact zeros: its O columns may never have
-            // been written by an MMA
+        for (int q4 = 0; q4 < D / 32; ++q4) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + q4 * 32);
+          // an invalid row writes exact zeros: its O columns may never have
+          // been written by an MMA
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              float f[8];
+          for (int i = 0; i < 32; i += 8) {
+            float f[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                f[e] = invalid ? 0.f : __uint_as_float(orr[q4][i + e]) * inv_l;
-              d4[i / 8] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                                     pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
-            }
+            for (int e = 0; e < 8; ++e)
+              f[e] = invalid ? 0.f : __uint_as_float(orr[q4][i + e]) * inv_l;
+            d4[i / 8] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                   pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
           }
         }
-        if (row_ok && a.lse != nullptr)
-          a.lse[(static_cast<long long>(b) * a.Hq + h) * a.S_q + row] =
-              invalid ? INFINITY : (m_run + log2f(l_run)) * 0.69314718055994530942f;
       }
+      if (row_ok && a.lse != nullptr)
+        a.lse[(static_cast<long long>(wi.b) * a.Hq + wi.h) * a.S_q + row] =
+            invalid ? INFINITY : (m_run + log2f(l_run)) * 0.69314718055994530942f;
     }
   }
 
@@ -615,6 +694,7 @@ cudaError_t launch_prefill_d(const PrefillLaunch& x, cudaStream_t stream) {
   pa.causal = x.causal;
   pa.n_qpairs = (x.S_q + 2 * kBM - 1) / (2 * kBM);
   pa.n_kv_tiles = (x.S_kv + kBN - 1) / kBN;
+  pa.n_items = pa.n_qpairs * x.B * x.Hq;
   if (x.layout == FA_LAYOUT_BNSD) {
     pa.out_row_stride = D;
     pa.out_head_stride = static_cast<long long>(x.S_q) * D;
@@ -625,9 +705,11 @@ cudaError_t launch_prefill_d(const PrefillLaunch& x, cudaStream_t stream) {
     pa.out_batch_stride = static_cast<long long>(x.S_q) * x.Hq * D;
   }
   pa.scale_log2 = x.scale * 1.4426950408889634f;
-  const long long grid = static_cast<long long>(pa.n_qpairs) * x.B * x.Hq;
-  prefill_kernel<D><<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, stream>>>(mq, mk, mv,
-                                                                                      pa);
+  // persistent: one CTA per SM (each CTA holds all 512 TMEM columns)
+  int sms = device_sm_count();
+  if (sms <= 0) sms = 1;
+  const int grid = std::min(pa.n_items, sms);
+  prefill_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, pa);
   return cudaGetLastError();
 }
 
