@@ -312,6 +312,18 @@ def roofline(kind, units_main, main_ms, peaks, peak_kind, workload):
             "traffic": traffic_from_profiles(kind, workload)}
 
 
+def max_over_ranks(vals, world, device=None):
+    """Each value's maximum over the ranks: the job takes as long as its
+    slowest rank. A no-op on one rank."""
+    if world == 1:
+        return [float(v) for v in vals]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
 def value_of(kind, units, ms):
     if kind == "decode":
         return units / (ms * 1e-3) / 1e9, "GB/s"
@@ -404,10 +416,7 @@ def run_gpu(args):
 
     ms = sum(step_ms) / len(step_ms)
     kms = sum(main_ms) / len(main_ms)
-    if world > 1:
-        t = torch.tensor([ms, kms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, kms = float(t[0]), float(t[1])
+    ms, kms = max_over_ranks([ms, kms], world, dev)
     value, unit = value_of(w.kind, main.units["step"] * world, ms)
 
     # end to end through the public call: pinned host inputs in, results out
@@ -417,10 +426,7 @@ def run_gpu(args):
     e_ms, _, _ = time_steps(main, e2e_steps, 2, flush,
                             fn=lambda: main.e2e_step(host_out, host_lse))
     e2e_ms = sum(e_ms) / len(e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    (e2e_ms,) = max_over_ranks([e2e_ms], world, dev)
     e2e_val, _ = value_of(w.kind, main.units["step"] * world, e2e_ms)
 
     others = {}
