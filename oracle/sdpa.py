@@ -19,6 +19,8 @@ definition itself, [FA] functional description; [IFA] §1.2):
 
     s_ij  = scale * sum_d q[b,h,i,d] * k[b,h//g,j,d]
     valid(i,j) = j < L_b  and  not key_mask[b,j]  and  not (causal and j > i)
+                 and  (win_left < 0 or j >= i - win_left)
+                 and  (win_right < 0 or j <= i + win_right)
     out_i = sum_{valid j} exp(s_ij - m_i) v_j / l_i,   m_i = max_{valid j} s_ij,
     l_i   = sum_{valid j} exp(s_ij - m_i),             lse_i = m_i + ln l_i
     a row with no valid key: out_i = 0, lse_i = +inf   ([FA] §1.7)
@@ -31,6 +33,11 @@ Readings taken where the pages are silent or ambiguous:
     and query row (the decode mask of [IFA] §四 has the (B,1,1,S) form);
   * "a very negative value" is read as exact exclusion (-inf);
   * causal means top-left aligned, j <= i ([FA] §1.5 "lower triangular");
+  * the window of [FA] §1.5 (mask_mode 4, a band of win_left tokens before
+    and win_right tokens after each query) is read as i - win_left <= j <=
+    i + win_right, top-left aligned like causal, with -1 meaning "no limit
+    on that side" (the value the page gives the two fields when no window
+    applies); causal is the window (-1, 0);
   * GQA: query head h reads KV head h // g, g = Hq / Hkv ([FA] §1.1: a group
     of g adjacent query heads shares one KV head);
   * keys at or past actualSeqLengths[b] do not exist ([IFA] §1.1: inputs are
@@ -88,11 +95,14 @@ def _from_bnsd(x: np.ndarray, layout: str) -> np.ndarray:
     return _to_bnsd(x, layout)  # the permutation is its own inverse
 
 
-def valid_key_matrix(rows, S_kv: int, L: int, key_mask_row, causal: bool) -> np.ndarray:
+def valid_key_matrix(rows, S_kv: int, L: int, key_mask_row, causal: bool,
+                     window=None) -> np.ndarray:
     """valid(i, j) for one batch: boolean [len(rows), S_kv] for query rows ``rows``.
 
     j < L ([IFA] §四 actualSeqLengths), key_mask_row[j] == 0 ([IFA] §8.1,
-    1 = masked), and j <= i when causal ([FA] §1.5, lower triangular).
+    1 = masked), j <= i when causal ([FA] §1.5, lower triangular), and
+    i - win_left <= j <= i + win_right for window = (win_left, win_right)
+    ([FA] §1.5 mask_mode 4; -1 = no limit on that side).
     """
     rows = np.asarray(rows)
     j = np.arange(S_kv)
@@ -101,18 +111,25 @@ def valid_key_matrix(rows, S_kv: int, L: int, key_mask_row, causal: bool) -> np.
         ok &= (np.asarray(key_mask_row) == 0)[None, :]
     if causal:
         ok &= j[None, :] <= rows[:, None]
+    if window is not None:
+        wl, wr = window
+        if wl >= 0:
+            ok &= j[None, :] >= rows[:, None] - wl
+        if wr >= 0:
+            ok &= j[None, :] <= rows[:, None] + wr
     return ok
 
 
 def attention(q, k, v, *, scale: float = 1.0, layout: str = "BNSD", causal: bool = False,
-              key_mask=None, actual_seq_lengths=None, rows=None):
+              key_mask=None, actual_seq_lengths=None, rows=None, window=None):
     """out (fp64, same layout as q) and lse (fp64, [B, Hq, S_q]).
 
     q: [B,Hq,S_q,D] (BNSD) or [B,S_q,Hq,D] (BSND); k, v likewise with Hkv heads.
     key_mask: optional [B, S_kv], nonzero = masked. actual_seq_lengths:
     optional per-batch valid KV length (default S_kv). rows: optional list of
     query indices; then only those rows are evaluated and the S_q axis of the
-    results has len(rows) entries, in that order.
+    results has len(rows) entries, in that order. window: optional
+    (win_left, win_right), see ``valid_key_matrix``.
     """
     qn = _to_bnsd(_as_f64(q), layout)
     kn = _to_bnsd(_as_f64(k), layout)
@@ -131,7 +148,7 @@ def attention(q, k, v, *, scale: float = 1.0, layout: str = "BNSD", causal: bool
     lse = np.full((B, Hq, R), np.inf)
     for b in range(B):
         L = max(0, min(lens[b], S_kv))
-        ok = valid_key_matrix(rows, S_kv, L, None if km is None else km[b], causal)
+        ok = valid_key_matrix(rows, S_kv, L, None if km is None else km[b], causal, window)
         # keys that no row can see (past L or masked) are dropped outright, so
         # whatever they hold (NaN included) never enters a product
         cols = np.nonzero(ok.any(axis=0))[0]
@@ -162,7 +179,8 @@ def decode(q, k, v, actual_seq_lengths, *, scale: float = 1.0, layout: str = "BN
 
 
 def attention_bruteforce(q, k, v, *, scale: float = 1.0, layout: str = "BNSD",
-                         causal: bool = False, key_mask=None, actual_seq_lengths=None):
+                         causal: bool = False, key_mask=None, actual_seq_lengths=None,
+                         window=None):
     """The same definition as scalar Python loops (tiny shapes only).
 
     Independent of ``attention``: every score, max, exponential and sum is a
@@ -188,6 +206,11 @@ def attention_bruteforce(q, k, v, *, scale: float = 1.0, layout: str = "BNSD",
                         continue
                     if causal and j > i:
                         continue
+                    if window is not None:
+                        if window[0] >= 0 and j < i - window[0]:
+                            continue
+                        if window[1] >= 0 and j > i + window[1]:
+                            continue
                     keys.append(j)
                 if not keys:
                     continue  # invalid row: out 0, lse +inf

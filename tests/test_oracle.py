@@ -293,3 +293,76 @@ def test_workload_generator_is_seeded_and_shaped():
     d = workloads.make_decode(4, 8, 2, 128, 16, "BNSD", seed=3, len_lo=10, len_hi=100)
     assert all(10 <= L <= 100 for L in d["lengths"])
     assert d["q"].shape == (4, 8, 1, 16)
+
+
+# ---------------------------------------------------------------- window mask
+# [FA] developer guide §1.5: mask_mode 4 is a band of win_left keys before and
+# win_right keys after each query (-1 = no limit on that side).
+
+WINDOWS = [(0, 0), (2, 0), (3, 1), (-1, 2), (1, -1), (5, 5)]
+
+
+@pytest.mark.parametrize("window", WINDOWS)
+def test_window_vectorised_matches_bruteforce(window):
+    q, k, v, km, _ = _case(2, 4, 2, 9, 9, 6, "BSND", 31, mask=True)
+    lens = [9, 6]
+    scale = 0.4
+    o1, l1 = oracle.attention(q, k, v, scale=scale, layout="BSND", key_mask=km,
+                              actual_seq_lengths=lens, window=window)
+    o2, l2 = oracle.attention_bruteforce(q, k, v, scale=scale, layout="BSND", key_mask=km,
+                                         actual_seq_lengths=lens, window=window)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    fin = np.isfinite(l2)
+    assert np.array_equal(fin, np.isfinite(l1))
+    np.testing.assert_allclose(l1[fin], l2[fin], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("window", WINDOWS)
+def test_window_matches_torch_sdpa_band(window):
+    """Library special case: torch's fp64 SDPA with the band built by
+    tril/triu (True = attend)."""
+    B, Hq, Hkv, S, D = 1, 4, 2, 12, 8
+    q, k, v, _, _ = _case(B, Hq, Hkv, S, S, D, "BNSD", 57)
+    scale = 1.0 / math.sqrt(D)
+    out, lse = oracle.attention(q, k, v, scale=scale, layout="BNSD", window=window)
+    qt, kt, vt = (t.double() for t in (q, k, v))
+    kt = kt.repeat_interleave(Hq // Hkv, dim=1)
+    vt = vt.repeat_interleave(Hq // Hkv, dim=1)
+    band = torch.ones(S, S, dtype=torch.bool)
+    wl, wr = window
+    if wr >= 0:
+        band = band.tril(wr)
+    if wl >= 0:
+        band = band.triu(-wl)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=band, scale=scale)
+    s = (scale * qt @ kt.transpose(-1, -2)).masked_fill(~band, float("-inf"))
+    np.testing.assert_allclose(out, ref.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_window_left_unbounded_right_zero_is_causal():
+    q, k, v, km, _ = _case(2, 2, 1, 10, 10, 4, "BNSD", 77, mask=True)
+    a = oracle.attention(q, k, v, scale=0.3, key_mask=km, causal=True)
+    b = oracle.attention(q, k, v, scale=0.3, key_mask=km, window=(-1, 0))
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_window_zero_width_returns_own_value_row():
+    """Closed form: with window (0, 0) query i sees only key i, so out_i =
+    v_i and lse_i = s_ii."""
+    q, k, v, _, _ = _case(1, 2, 2, 7, 7, 5, "BNSD", 91)
+    scale = 0.7
+    out, lse = oracle.attention(q, k, v, scale=scale, window=(0, 0))
+    qd, kd, vd = (t.double().numpy() for t in (q, k, v))
+    np.testing.assert_allclose(out, vd, rtol=0, atol=1e-15)
+    sii = scale * np.einsum("bhid,bhid->bhi", qd, kd)
+    np.testing.assert_allclose(lse, sii, rtol=0, atol=1e-12)
+
+
+def test_window_wider_than_sequence_is_no_mask():
+    q, k, v, _, _ = _case(1, 2, 1, 6, 6, 4, "BSND", 13)
+    a = oracle.attention(q, k, v, scale=0.5, layout="BSND")
+    b = oracle.attention(q, k, v, scale=0.5, layout="BSND", window=(6, 6))
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
