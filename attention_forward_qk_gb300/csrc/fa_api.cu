@@ -249,19 +249,27 @@ static fa_status check_common(int64_t B, int64_t S_q, int64_t S_kv, int64_t Hq, 
   return FA_OK;
 }
 
-fa_status fa_forward(const void* q, const void* k, const void* v, int mask_mode,
-                     const uint8_t* key_mask, const int64_t* lens, int64_t B, int64_t S_q,
-                     int64_t S_kv, int64_t num_heads, int64_t num_kv_heads, int64_t D,
-                     float scale, int layout, void* out, float* lse, void* workspace,
-                     size_t workspace_bytes, void* stream) {
+namespace {
+
+// Shared by fa_forward and fa_forward_window: the window (-1, -1) is no mask,
+// (-1, 0) is causal.
+fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok,
+                       int64_t win_left, int64_t win_right, const uint8_t* key_mask,
+                       const int64_t* lens,
+                       int64_t B, int64_t S_q, int64_t S_kv, int64_t num_heads,
+                       int64_t num_kv_heads, int64_t D, float scale, int layout, void* out,
+                       float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || workspace == nullptr)
     return FA_ERR_NULLPTR;
   int64_t Hkv = num_kv_heads;
   fa_status st = check_common(B, S_q, S_kv, num_heads, Hkv, D, scale, layout);
   if (st != FA_OK) return st;
-  if (mask_mode != FA_MASK_NONE && mask_mode != FA_MASK_CAUSAL) return FA_ERR_PARAM_INVALID;
-  const bool causal = mask_mode == FA_MASK_CAUSAL;
-  if (causal && S_q != S_kv) return FA_ERR_PARAM_INVALID;
+  if (!mask_ok || win_left < -1 || win_right < -1) return FA_ERR_PARAM_INVALID;
+  const bool windowed = win_left >= 0 || win_right >= 0;
+  if (windowed && S_q != S_kv) return FA_ERR_PARAM_INVALID;
+  // wider than the sequence is no limit (and keeps the tile arithmetic in int)
+  if (win_left >= S_kv) win_left = -1;
+  if (win_right >= S_kv) win_right = -1;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
     return FA_ERR_PARAM_INVALID;
@@ -301,7 +309,8 @@ fa_status fa_forward(const void* q, const void* k, const void* v, int mask_mode,
   x.S_kv = static_cast<int>(S_kv);
   x.D = static_cast<int>(D);
   x.layout = layout;
-  x.causal = causal ? 1 : 0;
+  x.win_left = static_cast<int>(win_left);
+  x.win_right = static_cast<int>(win_right);
   x.scale = scale;
   x.tile_bits = bits;
   x.out = out;
@@ -314,6 +323,30 @@ fa_status fa_forward(const void* q, const void* k, const void* v, int mask_mode,
   if (e != cudaSuccess) return FA_ERR_RUNTIME;
   count_launches(1);
   return FA_OK;
+}
+
+}  // namespace
+
+fa_status fa_forward(const void* q, const void* k, const void* v, int mask_mode,
+                     const uint8_t* key_mask, const int64_t* lens, int64_t B, int64_t S_q,
+                     int64_t S_kv, int64_t num_heads, int64_t num_kv_heads, int64_t D,
+                     float scale, int layout, void* out, float* lse, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  const bool mask_ok = mask_mode == FA_MASK_NONE || mask_mode == FA_MASK_CAUSAL;
+  const bool causal = mask_mode == FA_MASK_CAUSAL;
+  return forward_impl(q, k, v, mask_ok, -1, causal ? 0 : -1, key_mask, lens, B, S_q, S_kv, num_heads,
+                      num_kv_heads, D, scale, layout, out, lse, workspace, workspace_bytes,
+                      stream);
+}
+
+fa_status fa_forward_window(const void* q, const void* k, const void* v, int64_t win_left,
+                            int64_t win_right, const uint8_t* key_mask, const int64_t* lens,
+                            int64_t B, int64_t S_q, int64_t S_kv, int64_t num_heads,
+                            int64_t num_kv_heads, int64_t D, float scale, int layout, void* out,
+                            float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return forward_impl(q, k, v, true, win_left, win_right, key_mask, lens, B, S_q, S_kv, num_heads,
+                      num_kv_heads, D, scale, layout, out, lse, workspace, workspace_bytes,
+                      stream);
 }
 
 fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* key_mask,

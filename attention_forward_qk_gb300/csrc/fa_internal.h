@@ -57,7 +57,8 @@ struct PrefillLaunch {
   const void* q;
   const void* k;
   const void* v;
-  int B, Hq, Hkv, S_q, S_kv, D, layout, causal;
+  int B, Hq, Hkv, S_q, S_kv, D, layout;
+  int win_left, win_right;    // key j seen by query i iff i - wl <= j <= i + wr; -1 = no limit
   float scale;
   const uint32_t* tile_bits;  // [B][ceil(S_kv/128)][4] or null
   void* out;

@@ -72,7 +72,8 @@ struct PrefillArgs {
   const uint32_t* tile_bits;  // [B][n_kv_tiles][4], bit set = key valid; or null
   uint32_t* status;
   uint64_t timeout_ns;
-  int B, Hq, Hkv, S_q, S_kv, causal;
+  int B, Hq, Hkv, S_q, S_kv;
+  int win_left, win_right;    // key j is seen by query i iff i - wl <= j <= i + wr; -1 = no limit
   int n_qpairs, n_kv_tiles, n_items;
   long long out_row_stride, out_head_stride, out_batch_stride;  // elements
   float scale_log2;
@@ -95,9 +96,10 @@ enum : int {
 
 struct TileSeq {
   const uint32_t* bits;  // this batch's rows of the tile table, or null
-  int end;               // one past the last KV tile any Q tile of the CTA needs
+  int begin;             // first KV tile any Q tile of the item needs
+  int end;               // one past the last KV tile any Q tile of the item needs
   __device__ __forceinline__ int next(int j) const {
-    for (; j < end; ++j) {
+    for (j = max(j, begin); j < end; ++j) {
       if (bits == nullptr) return j;
       const uint4 w = __ldg(reinterpret_cast<const uint4*>(bits) + j);
       if ((w.x | w.y | w.z | w.w) != 0u) return j;
@@ -119,7 +121,7 @@ struct TileSeq {
 struct WorkItem {
   int b, kvh, h, q_row0;
   bool has_t1;
-  int n_t[2];  // KV tiles each Q tile needs (a prefix of the tile sequence)
+  int lo_t[2], n_t[2];  // KV tiles [lo_t, n_t) each Q tile needs
   TileSeq seq;
 };
 
@@ -136,12 +138,19 @@ __device__ __forceinline__ WorkItem work_item(const PrefillArgs& a, int w) {
   it.q_row0 = qp * 2 * kBM;
   it.has_t1 = it.q_row0 + kBM < a.S_q;
   for (int t = 0; t < 2; ++t) {
-    int n = a.n_kv_tiles;
-    if (a.causal) n = min(n, (it.q_row0 + t * kBM) / kBN + 1);
+    // rows r0 .. r0+127 see keys r0 - wl .. r0 + 127 + wr (window, causal = (-1, 0))
+    const int r0 = it.q_row0 + t * kBM;
+    int lo = 0, n = a.n_kv_tiles;
+    if (a.win_left >= 0) lo = max(0, r0 - a.win_left) / kBN;
+    if (a.win_right >= 0) n = min(n, (r0 + kBM - 1 + a.win_right) / kBN + 1);
     if (t == 1 && !it.has_t1) n = 0;
+    it.lo_t[t] = min(lo, n);
     it.n_t[t] = n;
   }
   it.seq.bits = a.tile_bits ? a.tile_bits + static_cast<size_t>(it.b) * a.n_kv_tiles * 4 : nullptr;
+  // the union of the two ranges (contiguous: the second tile's range is the
+  // first one shifted by one tile)
+  it.seq.begin = it.n_t[1] > it.lo_t[1] ? min(it.lo_t[0], it.lo_t[1]) : it.lo_t[0];
   it.seq.end = max(it.n_t[0], it.n_t[1]);
   return it;
 }
@@ -371,7 +380,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w >= a.n_items) break;
         const WorkItem wi = work_item(a, w);
         const TileSeq& seq = wi.seq;
+        // this stream's KV tiles: those of the item's sequence in [lo, n)
+        const int lo = t == 0 ? wi.lo_t[0] : wi.lo_t[1];
         const int n = t == 0 ? wi.n_t[0] : wi.n_t[1];
+        auto mine = [&](int jj) { return jj >= lo && jj < n; };
+        const bool has_any = seq.next(lo) < n;
         ok = mbar_wait(bar(kBarQ), r & 1, a.timeout_ns, a.status, kDevTimeoutQ, abort_flag);
         if (!ok) break;
         tc_fence_after();
@@ -386,18 +399,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) ok = take_turn(2 * u + t);
           if (!ok) break;
           tc_fence_after();
-          if (j < n) issue_s(slot);
+          if (mine(j)) issue_s(slot);
           *turn = 2 * u + t + 1;
           ++u;
-          if (j < n) umma_commit(bar(kBarSFull + t));
+          if (mine(j)) umma_commit(bar(kBarSFull + t));
           umma_commit(bar(kBarKvEmpty + slot));
         }
         // release Q once this stream's last S product of the item is issued
-        if (!(j < n) || !(seq.next(j + 1) < n)) {
+        if (!has_any || (mine(j) && !(seq.next(j + 1) < n))) {
           umma_commit(bar(kBarQFree));
           q_freed = true;
         }
-        if (!(j < n)) umma_commit(bar(kBarOFinal + t));  // sees no key (or tile absent)
+        if (!has_any) umma_commit(bar(kBarOFinal + t));  // sees no key (or tile absent)
         while (ok && j < seq.end) {
           const int v_item = item + 1;
           const int v_slot = v_item % kRing;
@@ -406,10 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int k_slot = k_item % kRing;
           ok = mbar_wait(bar(kBarKvFull + v_slot), (v_item / kRing) & 1, a.timeout_ns, a.status,
                          kDevTimeoutKvFull, abort_flag);
-          if (ok && j < n)
+          if (ok && mine(j))
             ok = mbar_wait(bar(kBarPReady + t), pv_count & 1, a.timeout_ns, a.status,
                            kDevTimeoutPReady, abort_flag);
-          if (ok && j < n && first_pv && r > 0)
+          if (ok && mine(j) && first_pv && r > 0)
             // O_t of the previous item must be read out before it is overwritten
             ok = mbar_wait(bar(kBarODrained + t), (r - 1) & 1, a.timeout_ns, a.status,
                            kDevTimeoutOFinal, abort_flag);
@@ -419,20 +432,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) ok = take_turn(2 * u + t);
           if (!ok) break;
           tc_fence_after();
-          if (j < n) issue_pv(v_slot, first_pv);
-          if (jn < n) issue_s(k_slot);
+          if (mine(j)) issue_pv(v_slot, first_pv);
+          if (mine(jn)) issue_s(k_slot);
           *turn = 2 * u + t + 1;
           ++u;
-          if (j < n) {
+          if (mine(j)) {
             ++pv_count;
             first_pv = false;
           }
-          if (jn < n) umma_commit(bar(kBarSFull + t));
-          if (jn < n && !q_freed && !(seq.next(jn + 1) < n)) {
+          if (mine(jn)) umma_commit(bar(kBarSFull + t));
+          if (mine(jn) && !q_freed && !(seq.next(jn + 1) < n)) {
             umma_commit(bar(kBarQFree));
             q_freed = true;
           }
-          if (j < n && !(jn < n)) umma_commit(bar(kBarOFinal + t));
+          if (mine(j) && !(jn < n)) umma_commit(bar(kBarOFinal + t));
           umma_commit(bar(kBarKvEmpty + v_slot));
           if (jn < seq.end) umma_commit(bar(kBarKvEmpty + k_slot));
           item += 2;
@@ -463,8 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = q_row0 + t * kBM + row_in_tile;
       float m_run = -INFINITY;  // reference max, log2 domain
       float l_run = 0.f;
+      const int lo_mine = t == 0 ? wi.lo_t[0] : wi.lo_t[1];
       const int n_mine = t == 0 ? wi.n_t[0] : wi.n_t[1];
-      for (int j = seq.next(0); j < n_mine; j = seq.next(j + 1), ++k) {
+      for (int j = seq.next(lo_mine); j < n_mine; j = seq.next(j + 1), ++k) {
       ok = mbar_wait(bar(kBarSFull + t), k & 1, a.timeout_ns, a.status, kDevTimeoutSFull,
                      abort_flag);
       ok = __all_sync(0xffffffffu, ok);
@@ -473,7 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sr[4][32];
       // per-element path: masked tiles, and a negative scale (whose row max is
       // the scale times the row min)
-      const bool masked = (a.causal && j * kBN + kBN - 1 > q_row0 + t * kBM) ||
+      const int r0 = q_row0 + t * kBM;
+      const bool masked = (a.win_right >= 0 && j * kBN + kBN - 1 > r0 + a.win_right) ||
+                          (a.win_left >= 0 && j * kBN < r0 + kBM - 1 - a.win_left) ||
                           ((j + 1) * kBN > a.S_kv) || !seq.full(j) || c < 0.f;
       float tmax = -INFINITY;
       if (masked) {
@@ -485,13 +501,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint4 w = __ldg(reinterpret_cast<const uint4*>(seq.bits) + j);
           words[0] = w.x; words[1] = w.y; words[2] = w.z; words[3] = w.w;
         }
+        // this row's keys of the tile, [lo_k, hi_k) relative to its first key:
+        // past S_kv, or outside the window (causal is the window (-1, 0)),
+        // folded into the validity words
+        {
+          const int base = j * kBN;
+          int hi_k = a.S_kv - base;
+          if (a.win_right >= 0) hi_k = min(hi_k, row + a.win_right + 1 - base);
+          const int lo_k = a.win_left >= 0 ? row - a.win_left - base : 0;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int lo_i = min(max(lo_k - q4 * 32, 0), 32);
+            const int hi_i = min(max(hi_k - q4 * 32, 0), 32);
+            const uint32_t below_hi = hi_i >= 32 ? 0xFFFFFFFFu : ((1u << hi_i) - 1u);
+            const uint32_t below_lo = lo_i >= 32 ? 0xFFFFFFFFu : ((1u << lo_i) - 1u);
+            words[q4] &= below_hi & ~below_lo;
+          }
+        }
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const int key = j * kBN + q4 * 32 + i;
-            const bool valid = ((words[q4] >> i) & 1u) && key < a.S_kv && (!a.causal || key <= row);
+            const bool valid = (words[q4] >> i) & 1u;
             const float tv = valid ? __uint_as_float(sr[q4][i]) * c : -INFINITY;
             sr[q4][i] = __float_as_uint(tv);
             mx[q4] = fmaxf(mx[q4], tv);
@@ -691,7 +723,8 @@ cudaError_t launch_prefill_d(const PrefillLaunch& x, cudaStream_t stream) {
   pa.Hkv = x.Hkv;
   pa.S_q = x.S_q;
   pa.S_kv = x.S_kv;
-  pa.causal = x.causal;
+  pa.win_left = x.win_left;
+  pa.win_right = x.win_right;
   pa.n_qpairs = (x.S_q + 2 * kBM - 1) / (2 * kBM);
   pa.n_kv_tiles = (x.S_kv + kBN - 1) / kBN;
   pa.n_items = pa.n_qpairs * x.B * x.Hq;

@@ -91,10 +91,8 @@ def fa_decode_plan(actual_seq_lengths, S_kv_max, num_heads, num_kv_heads, D, num
     return c.value, n.value, m.value
 
 
-def fa_forward(q, k, v, *, mask_mode=None, key_mask=None, actual_seq_lengths=None, scale=1.0,
-               layout="BNSD", num_heads=None, num_kv_heads=None, out=None, lse=None,
-               return_lse=True, workspace=None, stream=None):
-    """Prefill attention. Returns (out, lse); lse is None unless requested."""
+def _forward_prep(q, k, v, layout, num_heads, num_kv_heads, out, lse, return_lse, key_mask,
+                  workspace, actual_seq_lengths):
     lid = _layout_id(layout)
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check_tensor(t, n)
@@ -119,12 +117,39 @@ def fa_forward(q, k, v, *, mask_mode=None, key_mask=None, actual_seq_lengths=Non
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     lens_arr, _ = _lens_array(actual_seq_lengths, B)
+    return lid, (B, S_q, S_kv, Hq, Hkv, D), out, lse, workspace, lens_arr
+
+
+def fa_forward(q, k, v, *, mask_mode=None, key_mask=None, actual_seq_lengths=None, scale=1.0,
+               layout="BNSD", num_heads=None, num_kv_heads=None, out=None, lse=None,
+               return_lse=True, workspace=None, stream=None):
+    """Prefill attention. Returns (out, lse); lse is None unless requested."""
+    lid, (B, S_q, S_kv, Hq, Hkv, D), out, lse, workspace, lens_arr = _forward_prep(
+        q, k, v, layout, num_heads, num_kv_heads, out, lse, return_lse, key_mask, workspace,
+        actual_seq_lengths)
     st = _lib.load().fa_forward(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), MASK_MODES.get(mask_mode, mask_mode),
         key_mask.data_ptr() if key_mask is not None else None, lens_arr, B, S_q, S_kv, Hq, Hkv,
         D, float(scale), lid, out.data_ptr(), lse.data_ptr() if lse is not None else None,
         workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
     check(st, "fa_forward")
+    return out, lse
+
+
+def fa_forward_window(q, k, v, win_left, win_right, *, key_mask=None, actual_seq_lengths=None,
+                      scale=1.0, layout="BNSD", num_heads=None, num_kv_heads=None, out=None,
+                      lse=None, return_lse=True, workspace=None, stream=None):
+    """Prefill attention with a sliding window: query i sees keys i - win_left
+    .. i + win_right (-1 = no limit on that side). Returns (out, lse)."""
+    lid, (B, S_q, S_kv, Hq, Hkv, D), out, lse, workspace, lens_arr = _forward_prep(
+        q, k, v, layout, num_heads, num_kv_heads, out, lse, return_lse, key_mask, workspace,
+        actual_seq_lengths)
+    st = _lib.load().fa_forward_window(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), int(win_left), int(win_right),
+        key_mask.data_ptr() if key_mask is not None else None, lens_arr, B, S_q, S_kv, Hq, Hkv,
+        D, float(scale), lid, out.data_ptr(), lse.data_ptr() if lse is not None else None,
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    check(st, "fa_forward_window")
     return out, lse
 
 

@@ -73,8 +73,9 @@ typedef enum {
 
 typedef enum { FA_LAYOUT_BNSD = 0, FA_LAYOUT_BSND = 1 } fa_layout;
 
-/* Mask modes, numbered as in FlashAttn guide §1.5 (0 = none, 3 = causal). */
-typedef enum { FA_MASK_NONE = 0, FA_MASK_CAUSAL = 3 } fa_mask_mode;
+/* Mask modes, numbered as in FlashAttn guide §1.5 (0 = none, 3 = causal,
+ * 4 = window; the window takes its widths through fa_forward_window). */
+typedef enum { FA_MASK_NONE = 0, FA_MASK_CAUSAL = 3, FA_MASK_WINDOW = 4 } fa_mask_mode;
 
 /* Version of this ABI (FA_ABI_VERSION). */
 int fa_abi_version(void);
@@ -108,6 +109,22 @@ fa_status fa_forward(const void* q, const void* k, const void* v, int mask_mode,
                      int64_t S_q, int64_t S_kv, int64_t num_heads, int64_t num_kv_heads,
                      int64_t D, float scale, int layout, void* out, float* lse,
                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Fused attention forward with a sliding window (FlashAttn guide §1.5,
+ * mask_mode 4: a band of win_left tokens before and win_right tokens after
+ * each query). Query row i keeps key j iff
+ *     (win_left  < 0 or j >= i - win_left) and (win_right < 0 or j <= i + win_right),
+ * top-left aligned as causal is; -1 means no limit on that side, so (-1, 0)
+ * is causal and (-1, -1) no mask. A window requires S_q == S_kv; widths below
+ * -1 are FA_ERR_PARAM_INVALID. KV tiles wholly outside every row's window
+ * are never loaded or multiplied. All other arguments, the workspace
+ * (fa_forward_workspace_size) and the errors are those of fa_forward. */
+fa_status fa_forward_window(const void* q, const void* k, const void* v, int64_t win_left,
+                            int64_t win_right, const uint8_t* key_mask,
+                            const int64_t* actual_seq_lengths, int64_t B, int64_t S_q,
+                            int64_t S_kv, int64_t num_heads, int64_t num_kv_heads, int64_t D,
+                            float scale, int layout, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, void* stream);
 
 /* ----------------------------------------------------------------- decode
  * Workspace bytes fa_decode needs. num_splits as for fa_decode (0 = the

@@ -111,6 +111,36 @@ def test_forward_rejects_before_any_cuda_call(lib, kw, expect):
     assert _fwd(lib, **kw) == expect
 
 
+def _fwd_window(lib, wl, wr, **kw):
+    args = dict(q=P, k=P, v=P, key_mask=None, lens=None, B=1, S_q=128, S_kv=128, Hq=2, Hkv=2,
+                D=64, scale=0.125, layout=0, out=P, lse=None, ws=WS, ws_bytes=1 << 20,
+                stream=None)
+    args.update(kw)
+    return lib.fa_forward_window(args["q"], args["k"], args["v"], wl, wr, args["key_mask"],
+                                 None, args["B"], args["S_q"], args["S_kv"], args["Hq"],
+                                 args["Hkv"], args["D"], args["scale"], args["layout"],
+                                 args["out"], args["lse"], args["ws"], args["ws_bytes"],
+                                 args["stream"])
+
+
+@pytest.mark.parametrize("wl,wr,kw,expect", [
+    (-2, 0, {}, _lib.FA_ERR_PARAM_INVALID),
+    (0, -5, {}, _lib.FA_ERR_PARAM_INVALID),
+    (4, 4, dict(S_q=64, S_kv=128), _lib.FA_ERR_PARAM_INVALID),  # a window needs S_q == S_kv
+    (4, 4, dict(q=None), _lib.FA_ERR_NULLPTR),
+    (4, 4, dict(D=96), _lib.FA_ERR_UNSUPPORTED),
+    (4, 4, dict(ws_bytes=16), _lib.FA_ERR_WORKSPACE_TOO_SMALL),
+])
+def test_forward_window_rejects_before_any_cuda_call(lib, wl, wr, kw, expect):
+    assert _fwd_window(lib, wl, wr, **kw) == expect
+
+
+def test_forward_window_noop_shapes_return_ok(lib):
+    assert _fwd_window(lib, 3, 2, B=0) == _lib.FA_OK
+    # no window at all: S_q may differ from S_kv (as for fa_forward without a mask)
+    assert _fwd_window(lib, -1, -1, B=0, S_q=5, S_kv=9) == _lib.FA_OK
+
+
 def test_forward_noop_shapes_return_ok(lib):
     assert _fwd(lib, B=0) == _lib.FA_OK
     assert _fwd(lib, S_q=0, S_kv=5) == _lib.FA_OK
