@@ -90,7 +90,12 @@ def work_units(w, lens=None, pads=None):
         qo = 2 * 2 * w.B * w.Hq * w.D + 4 * w.B * w.Hq
         return {"step": kv + qo, "main": kv + 2 * w.B * w.Hq * w.D}
     S = w.S_q
-    if w.causal and pads:
+    if w.window is not None:
+        wl, wr = w.window
+        per_row = [min(S, i + wr + 1 if wr >= 0 else S) - max(0, i - wl if wl >= 0 else 0)
+                   for i in range(S)]
+        pairs = w.B * w.Hq * sum(per_row)
+    elif w.causal and pads:
         pairs = w.Hq * sum(sum(min(i + 1, S - p) for i in range(S)) for p in pads)
     elif w.causal:
         pairs = w.B * w.Hq * S * (S + 1) // 2
@@ -227,6 +232,10 @@ class Runner:
         if self.kind == "decode":
             F.fa_decode(self.q, self.k, self.v, self.lens, scale=w.scale, layout=w.layout,
                         out=self.out, lse=self.lse, workspace=self.ws)
+        elif w.window is not None:
+            F.fa_forward_window(self.q, self.k, self.v, w.window[0], w.window[1],
+                                key_mask=self.km, scale=w.scale, layout=w.layout, out=self.out,
+                                lse=self.lse, workspace=self.ws)
         else:
             F.fa_forward(self.q, self.k, self.v, mask_mode="causal" if w.causal else None,
                          key_mask=self.km, scale=w.scale, layout=w.layout, out=self.out,
@@ -362,10 +371,14 @@ def cpu_baseline(w, budget_s=12.0):
         bsl = slice(passes % w.B, passes % w.B + 1)
         km = x["key_mask"][bsl] if x["key_mask"] is not None else None
         oracle.attention(x["q"][bsl], x["k"][bsl], x["v"][bsl], scale=w.scale, layout=w.layout,
-                         causal=w.causal, key_mask=km, rows=rows)
+                         causal=w.causal, key_mask=km, rows=rows, window=w.window)
         p = pads[passes % w.B] if pads else 0
         for i in rows:
-            n = min(i + 1, w.S_kv - p) if w.causal else w.S_kv - p
+            if w.window is not None:
+                wl, wr = w.window
+                n = min(w.S_kv, i + wr + 1 if wr >= 0 else w.S_kv) - max(0, i - wl if wl >= 0 else 0)
+            else:
+                n = min(i + 1, w.S_kv - p) if w.causal else w.S_kv - p
             done_units += 4 * w.D * n * w.Hq
         rows_done += len(rows)
         passes += 1
@@ -432,7 +445,7 @@ def run_gpu(args):
     others = {}
     if not args.only:
         for name in ("long_decode", "causal_prefill", "gqa_masked_prefill", "tiny_prefill",
-                     "gqa_decode"):
+                     "window_prefill", "gqa_decode"):
             if name == args.workload:
                 continue
             wo = workloads.WORKLOADS[name]

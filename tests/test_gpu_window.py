@@ -69,3 +69,17 @@ def test_window_long_sequence_sampled_rows(cuda_device):
                       g.choice(S, 56, replace=False).tolist()))
     ro, rl = oracle.attention(x["q"], x["k"], x["v"], scale=scale, window=window, rows=rows)
     compare(out, lse, ro, rl, "BNSD", rows=rows)
+
+
+def test_window_workload_sampled_rows(cuda_device):
+    """The bench's window workload at full size (B=2, Hq=32, Hkv=8, S=8192,
+    window (1023, 0)), on sampled rows of every head."""
+    w = workloads.WORKLOADS["window_prefill"]
+    x = workloads.make(w)
+    out, lse = _run(x, w.window, w.scale)
+    g = np.random.default_rng(5)
+    rows = sorted(set([0, 1022, 1023, 1024, 1025, 4096, w.S_q - 1] +
+                      g.choice(w.S_q, 41, replace=False).tolist()))
+    ro, rl = oracle.attention(x["q"], x["k"], x["v"], scale=w.scale, layout=w.layout,
+                              window=w.window, rows=rows)
+    compare(out, lse, ro, rl, w.layout, rows=rows)

@@ -55,6 +55,8 @@ class Workload:
     garbage: bool = False
     # prefill: per-batch count of masked trailing keys, uniform in [0, max_pad]
     max_pad: int | None = None
+    # prefill: sliding window (win_left, win_right), -1 = no limit on that side
+    window: tuple | None = None
     note: str = field(default="", compare=False)
 
     @property
@@ -84,6 +86,12 @@ WORKLOADS: dict[str, Workload] = {
         "gqa_masked_prefill", "prefill", B=2, Hq=64, Hkv=8, S_q=8192, S_kv=8192, D=128,
         layout="BNSD", causal=True, seed=105, max_pad=1024,
         note="B=2 Hq=64 Hkv=8 S=8192 D=128 BNSD causal AND key padding p_b~U[0,1024]"),
+    # Beyond the five: the sliding-window mask (FlashAttn guide §1.5, mode 4)
+    # on a long GQA prefill, each query seeing itself and the 1023 keys before.
+    "window_prefill": Workload(
+        "window_prefill", "prefill", B=2, Hq=32, Hkv=8, S_q=8192, S_kv=8192, D=128,
+        layout="BNSD", seed=106, window=(1023, 0),
+        note="B=2 Hq=32 Hkv=8 S=8192 D=128 BNSD, window of 1024 keys (1023 before, 0 after)"),
 }
 
 
