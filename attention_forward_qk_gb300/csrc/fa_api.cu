@@ -64,12 +64,21 @@ int64_t max_slots_bound(int64_t S_kv_max, int num_splits) {
 }
 
 struct PrefillWs {
-  size_t lens, bits, total;
+  size_t sched, lens, bits, total;
 };
 
-PrefillWs prefill_ws(int64_t B, int64_t S_kv) {
+// Work items of a prefill launch: 256 query rows of one (batch, query head).
+int64_t prefill_items(int64_t B, int64_t S_q, int64_t num_heads) {
+  return B * num_heads * ceil_div(S_q, 256);
+}
+
+// [status, item counter | pad][schedule: offsets of kMaxPrefillCtas + 1 CTAs,
+// then the item lists][lengths][per-tile key validity]
+PrefillWs prefill_ws(int64_t B, int64_t S_q, int64_t S_kv, int64_t num_heads) {
   PrefillWs w;
   size_t off = kAlign;  // status word
+  w.sched = off;
+  off += align_up(sizeof(int32_t) * (kMaxPrefillCtas + 1 + prefill_items(B, S_q, num_heads)));
   w.lens = off;
   off += align_up(sizeof(int32_t) * B);
   w.bits = off;
@@ -78,6 +87,74 @@ PrefillWs prefill_ws(int64_t B, int64_t S_kv) {
   return w;
 }
 
+
+// Static schedule of the persistent prefill CTAs. Items are numbered as the
+// kernel decodes them: (batch, KV head) units one after another, inside a
+// unit its query pairs heaviest (last) first, query heads innermost. Units
+// are taken in groups of 8; inside a group the items go, longest first, to
+// the CTA with the least work so far (a greedy longest-processing-time
+// schedule), and the groups follow one another, so the items in flight at any
+// time read the K/V of a few units out of L2. The cost of an item is its KV
+// tiles under the causal or window limits plus a constant for its start-up.
+// Layout: offsets[grid + 1] into the lists, then the item lists (int32).
+void build_prefill_schedule(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t S_kv,
+                            int64_t win_left, int64_t win_right, int grid,
+                            std::vector<int32_t>& sched) {
+  const int64_t g = Hq / Hkv;
+  const int64_t nq = ceil_div(S_q, 256);
+  const int64_t n_tiles = ceil_div(std::max<int64_t>(S_kv, 1), 128);
+  const int64_t per_unit = nq * g;
+  const int64_t units = B * Hkv;
+  const int64_t n_items = units * per_unit;
+  auto cost = [&](int64_t w) -> int64_t {
+    const int64_t qp = nq - 1 - (w % per_unit) / g;
+    int64_t lo_u = n_tiles, hi_u = 0;
+    for (int t = 0; t < 2; ++t) {
+      const int64_t r0 = qp * 256 + t * 128;
+      if (t == 1 && r0 >= S_q) break;
+      int64_t lo = 0, hi = n_tiles;
+      if (win_left >= 0) lo = std::max<int64_t>(0, r0 - win_left) / 128;
+      if (win_right >= 0) hi = std::min(hi, (r0 + 127 + win_right) / 128 + 1);
+      lo_u = std::min(lo_u, lo);
+      hi_u = std::max(hi_u, hi);
+    }
+    return std::max<int64_t>(0, hi_u - lo_u) + 3;
+  };
+  std::vector<std::vector<int32_t>> lists(grid);
+  // min-heap of (load, cta)
+  std::vector<std::pair<int64_t, int>> heap;
+  heap.reserve(grid);
+  for (int c = 0; c < grid; ++c) heap.emplace_back(0, c);
+  auto cmp = [](const std::pair<int64_t, int>& x, const std::pair<int64_t, int>& y) {
+    return x > y;
+  };
+  std::vector<std::pair<int64_t, int64_t>> grp;
+  for (int64_t u0 = 0; u0 < units; u0 += 8) {
+    const int64_t w0 = u0 * per_unit;
+    const int64_t w1 = std::min(units, u0 + 8) * per_unit;
+    grp.clear();
+    for (int64_t w = w0; w < w1; ++w) grp.emplace_back(-cost(w), w);
+    std::stable_sort(grp.begin(), grp.end(),
+                     [](const std::pair<int64_t, int64_t>& x, const std::pair<int64_t, int64_t>& y) {
+                       return x.first < y.first;
+                     });
+    for (const auto& it : grp) {
+      std::pop_heap(heap.begin(), heap.end(), cmp);
+      auto& top = heap.back();
+      lists[top.second].push_back(static_cast<int32_t>(it.second));
+      top.first += -it.first;
+      std::push_heap(heap.begin(), heap.end(), cmp);
+    }
+  }
+  sched.assign(grid + 1 + n_items, 0);
+  int32_t off = 0;
+  for (int c = 0; c < grid; ++c) {
+    sched[c] = off;
+    std::copy(lists[c].begin(), lists[c].end(), sched.begin() + grid + 1 + off);
+    off += static_cast<int32_t>(lists[c].size());
+  }
+  sched[grid] = off;
+}
 
 // ------------------------------------------------------------ driver entry
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -179,11 +256,9 @@ const char* fa_status_string(int s) {
 size_t fa_forward_workspace_size(int64_t B, int64_t S_q, int64_t S_kv, int64_t num_heads,
                                  int64_t num_kv_heads, int64_t D) {
   if (B < 0 || S_q < 0 || S_kv < 0 || num_heads < 0 || num_kv_heads < 0 || D < 0) return 0;
-  (void)S_q;
-  (void)num_heads;
   (void)num_kv_heads;
   (void)D;
-  return prefill_ws(B, S_kv).total;
+  return prefill_ws(B, S_q, S_kv, num_heads).total;
 }
 
 fa_status fa_decode_plan(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t num_kv_heads,
@@ -276,16 +351,38 @@ fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok
   if (lens != nullptr)
     for (int64_t b = 0; b < B; ++b)
       if (lens[b] < 0 || lens[b] > S_kv) return FA_ERR_PARAM_INVALID;
-  const PrefillWs ws = prefill_ws(B, S_kv);
+  const PrefillWs ws = prefill_ws(B, S_q, S_kv, num_heads);
   if (workspace_bytes < ws.total) return FA_ERR_WORKSPACE_TOO_SMALL;
   if (B == 0 || S_q == 0) return FA_OK;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned char* wsb = static_cast<unsigned char*>(workspace);
-  // header: zeroed status word, then the lengths as int32 when given
-  std::vector<int32_t> blob(kAlign / 4 + (lens ? B : 0), 0);
+  const int sms = device_sm_count();
+  if (sms <= 0) return FA_ERR_RUNTIME;
+  const int64_t n_items = prefill_items(B, S_q, num_heads);
+  const int grid = static_cast<int>(
+      std::min<int64_t>(std::min<int64_t>(n_items, sms), kMaxPrefillCtas));
+  // the schedule depends on the shapes only; the last one is kept per thread
+  struct SchedKey {
+    int64_t B, Hq, Hkv, S_q, S_kv, wl, wr;
+    int grid;
+    bool operator==(const SchedKey& o) const {
+      return B == o.B && Hq == o.Hq && Hkv == o.Hkv && S_q == o.S_q && S_kv == o.S_kv &&
+             wl == o.wl && wr == o.wr && grid == o.grid;
+    }
+  };
+  thread_local SchedKey sched_key{-1, 0, 0, 0, 0, 0, 0, 0};
+  thread_local std::vector<int32_t> sched;
+  const SchedKey key{B, num_heads, Hkv, S_q, S_kv, win_left, win_right, grid};
+  if (!(key == sched_key)) {
+    build_prefill_schedule(B, num_heads, Hkv, S_q, S_kv, win_left, win_right, grid, sched);
+    sched_key = key;
+  }
+  // header: zeroed status word, the schedule, then the lengths as int32 when given
+  std::vector<int32_t> blob(ws.lens / 4 + (lens ? B : 0), 0);
+  std::copy(sched.begin(), sched.end(), blob.begin() + ws.sched / 4);
   if (lens)
-    for (int64_t b = 0; b < B; ++b) blob[kAlign / 4 + b] = static_cast<int32_t>(lens[b]);
+    for (int64_t b = 0; b < B; ++b) blob[ws.lens / 4 + b] = static_cast<int32_t>(lens[b]);
   if (cudaMemcpyAsync(wsb, blob.data(), blob.size() * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return FA_ERR_RUNTIME;
   const uint32_t* bits = nullptr;
@@ -313,6 +410,8 @@ fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok
   x.win_right = static_cast<int>(win_right);
   x.scale = scale;
   x.tile_bits = bits;
+  x.sched = reinterpret_cast<const int32_t*>(wsb + ws.sched);
+  x.grid = grid;
   x.out = out;
   x.lse = lse;
   x.status = reinterpret_cast<uint32_t*>(wsb);

@@ -30,6 +30,8 @@ constexpr int kDecodeStageRows = 112;
 constexpr int kDecodeParamBatches = 1024;
 // Smallest share of the work space one decode CTA is given.
 constexpr int kDecodeMinRowsPerCta = 224;
+// Largest persistent prefill grid the workspace's schedule has room for.
+constexpr int kMaxPrefillCtas = 1024;
 
 struct DecodeLaunch {
   const void* q;
@@ -61,6 +63,8 @@ struct PrefillLaunch {
   int win_left, win_right;    // key j seen by query i iff i - wl <= j <= i + wr; -1 = no limit
   float scale;
   const uint32_t* tile_bits;  // [B][ceil(S_kv/128)][4] or null
+  const int32_t* sched;       // per-CTA work-item lists (offsets[grid + 1], then the lists)
+  int grid;                   // persistent CTAs
   void* out;
   float* lse;
   uint32_t* status;

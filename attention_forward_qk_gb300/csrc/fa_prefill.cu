@@ -70,6 +70,7 @@ struct PrefillArgs {
   __nv_bfloat16* out;
   float* lse;
   const uint32_t* tile_bits;  // [B][n_kv_tiles][4], bit set = key valid; or null
+  const int32_t* sched;       // offsets[grid + 1], then each CTA's work items in order
   uint32_t* status;
   uint64_t timeout_ns;
   int B, Hq, Hkv, S_q, S_kv;
@@ -173,13 +174,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  // ---- persistent schedule: this CTA takes work items r*G + c (even rounds)
-  // and r*G + G-1-c (odd rounds). With items of one KV head ordered heaviest
-  // first, the snake pairs heavy with light items, which evens out the causal
-  // cost per CTA.
+  // ---- persistent schedule: this CTA's list of work items, built on the
+  // host (longest first, per group of 8 (batch, KV head) units, to the least
+  // loaded CTA); n_items past the end of the list
   const int G = static_cast<int>(gridDim.x);
   const int cta = static_cast<int>(blockIdx.x);
-  auto item_of = [&](int r) -> int { return r * G + ((r & 1) ? (G - 1 - cta) : cta); };
+  const int list0 = __ldg(a.sched + cta);
+  const int list_n = __ldg(a.sched + cta + 1) - list0;
+  auto item_of = [&](int r) -> int {
+    return r < list_n ? __ldg(a.sched + G + 1 + list0 + r) : a.n_items;
+  };
 
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) {
@@ -716,6 +720,7 @@ cudaError_t launch_prefill_d(const PrefillLaunch& x, cudaStream_t stream) {
   pa.out = static_cast<__nv_bfloat16*>(x.out);
   pa.lse = x.lse;
   pa.tile_bits = x.tile_bits;
+  pa.sched = x.sched;
   pa.status = x.status;
   pa.timeout_ns = x.timeout_ns;
   pa.B = x.B;
@@ -739,9 +744,7 @@ cudaError_t launch_prefill_d(const PrefillLaunch& x, cudaStream_t stream) {
   }
   pa.scale_log2 = x.scale * 1.4426950408889634f;
   // persistent: one CTA per SM (each CTA holds all 512 TMEM columns)
-  int sms = device_sm_count();
-  if (sms <= 0) sms = 1;
-  const int grid = std::min(pa.n_items, sms);
+  const int grid = x.grid;  // the schedule in the workspace was built for this grid
   prefill_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, pa);
   return cudaGetLastError();
 }
