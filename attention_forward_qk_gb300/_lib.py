@@ -24,6 +24,8 @@ FA_LAYOUT_BSND = 1
 FA_MASK_NONE = 0
 FA_MASK_CAUSAL = 3
 FA_MASK_WINDOW = 4
+FA_LAYOUT_PA_BBND = 2
+FA_LAYOUT_PA_BNBD = 3
 
 _i64 = ctypes.c_int64
 _vp = ctypes.c_void_p
@@ -40,6 +42,9 @@ SIGNATURES = {
     "fa_forward_window": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _i64, _i64,
                                          _i64, _i64, _i64, ctypes.c_float, ctypes.c_int, _vp,
                                          _vp, _vp, _sz, _vp]),
+    "fa_decode_paged": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int, _vp, _i64, _i64, _i64, _vp,
+                                       _vp, _i64, _i64, _i64, _i64, ctypes.c_float, ctypes.c_int,
+                                       _vp, _vp, _vp, _sz, _vp]),
     "fa_decode_workspace_size": (_sz, [_i64] * 5 + [ctypes.c_int]),
     "fa_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                                  ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _sz,

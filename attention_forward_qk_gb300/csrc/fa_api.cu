@@ -38,7 +38,7 @@ int64_t chunk_for_splits(int64_t S_kv_max, int num_splits) {
 }
 
 struct DecodeWs {
-  size_t prefix, part_lse, part_o, total;
+  size_t prefix, real_lens, part_lse, part_o, total;
 };
 
 // [status | pad][length prefix sums, large batches only][partial lse][partial o]
@@ -47,6 +47,8 @@ DecodeWs decode_ws(int64_t B, int64_t Hq, int64_t D, int64_t max_slots) {
   size_t off = kAlign;  // status word
   w.prefix = off;
   off += align_up(sizeof(int64_t) * (B + 1));
+  w.real_lens = off;  // paged cache only
+  off += align_up(sizeof(int32_t) * B);
   w.part_lse = off;
   off += align_up(sizeof(float) * B * Hq * max_slots);
   w.part_o = off;
@@ -261,9 +263,27 @@ size_t fa_forward_workspace_size(int64_t B, int64_t S_q, int64_t S_kv, int64_t n
   return prefill_ws(B, S_q, S_kv, num_heads).total;
 }
 
+namespace {
+fa_status decode_plan_impl(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t num_kv_heads,
+                           int64_t D, const int64_t* lens, int num_sms, int num_splits,
+                           int64_t rc_align, int64_t* chunk_rows, int64_t* num_chunks,
+                           int64_t* max_chunks);
+}  // namespace
+
 fa_status fa_decode_plan(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t num_kv_heads,
                          int64_t D, const int64_t* lens, int num_sms, int num_splits,
                          int64_t* chunk_rows, int64_t* num_chunks, int64_t* max_chunks) {
+  return decode_plan_impl(B, S_kv_max, num_heads, num_kv_heads, D, lens, num_sms, num_splits, 1,
+                          chunk_rows, num_chunks, max_chunks);
+}
+
+namespace {
+// rc_align: the per-CTA share is rounded up to a multiple of it (16 rows for
+// a paged cache, whose work space is laid out in 16-row boxes)
+fa_status decode_plan_impl(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t num_kv_heads,
+                           int64_t D, const int64_t* lens, int num_sms, int num_splits,
+                           int64_t rc_align, int64_t* chunk_rows, int64_t* num_chunks,
+                           int64_t* max_chunks) {
   if (lens == nullptr || chunk_rows == nullptr || num_chunks == nullptr || max_chunks == nullptr)
     return FA_ERR_NULLPTR;
   if (num_kv_heads == 0) num_kv_heads = num_heads;
@@ -287,6 +307,7 @@ fa_status fa_decode_plan(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t
     // one equal share per SM (at least a couple of stages each)
     rc = std::max<int64_t>(ceil_div(std::max<int64_t>(total, 1), num_sms), kDecodeMinRowsPerCta);
   }
+  rc = ceil_div(rc, rc_align) * rc_align;
   int64_t mx = 0, prefix = 0;
   for (int64_t b = 0; b < B; ++b) {
     const int64_t L = lens[b];
@@ -303,6 +324,7 @@ fa_status fa_decode_plan(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t
   *max_chunks = mx;
   return FA_OK;
 }
+}  // namespace
 
 size_t fa_decode_workspace_size(int64_t B, int64_t S_kv_max, int64_t num_heads,
                                 int64_t num_kv_heads, int64_t D, int num_splits) {
@@ -448,11 +470,19 @@ fa_status fa_forward_window(const void* q, const void* k, const void* v, int64_t
                       stream);
 }
 
-fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* key_mask,
-                    const int64_t* lens, int64_t B, int64_t S_kv_max, int64_t num_heads,
-                    int64_t num_kv_heads, int64_t D, float scale, int layout, int num_splits,
-                    void* out, float* lse, void* workspace, size_t workspace_bytes,
-                    void* stream) {
+namespace {
+
+// A paged K/V cache (fa_decode_paged); null for a contiguous one.
+struct PagedKv {
+  const int32_t* block_table;
+  int64_t max_blocks, num_blocks, block_size;
+};
+
+fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv* pg,
+                      const uint8_t* key_mask, const int64_t* lens, int64_t B, int64_t S_kv_max,
+                      int64_t num_heads, int64_t num_kv_heads, int64_t D, float scale, int layout,
+                      int num_splits, void* out, float* lse, void* workspace,
+                      size_t workspace_bytes, void* stream) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || workspace == nullptr ||
       lens == nullptr)
     return FA_ERR_NULLPTR;
@@ -469,11 +499,20 @@ fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* 
     return FA_ERR_WORKSPACE_TOO_SMALL;
   if (B == 0) return FA_OK;
 
+  // a paged cache is streamed in 16-row boxes: its work space holds every
+  // length rounded up to 16 rows (the kernel masks the extra rows)
+  std::vector<int64_t> lens16;
+  const int64_t* wlens = lens;
+  if (pg != nullptr) {
+    lens16.resize(B);
+    for (int64_t b = 0; b < B; ++b) lens16[b] = ceil_div(lens[b], 16) * 16;
+    wlens = lens16.data();
+  }
   const int sms = device_sm_count();
   if (sms <= 0) return FA_ERR_RUNTIME;
   int64_t rc = 0, n_ctas = 0, max_slots = 0;
-  st = fa_decode_plan(B, S_kv_max, num_heads, Hkv, D, lens, sms, num_splits, &rc, &n_ctas,
-                      &max_slots);
+  st = decode_plan_impl(B, S_kv_max, num_heads, Hkv, D, wlens, sms, num_splits,
+                        pg != nullptr ? 16 : 1, &rc, &n_ctas, &max_slots);
   if (st != FA_OK) return st;
   const int64_t slots = std::max<int64_t>(max_slots, 1);
   if (slots > max_slots_bound(S_kv_max, num_splits)) return FA_ERR_RUNTIME;  // cannot happen
@@ -492,7 +531,7 @@ fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* 
   prefix[0] = 0;
   bool has_empty = false;
   for (int64_t b = 0; b < B; ++b) {
-    prefix[b + 1] = prefix[b] + lens[b];
+    prefix[b + 1] = prefix[b] + wlens[b];
     has_empty = has_empty || lens[b] == 0;
   }
   const int64_t g = num_heads / Hkv;
@@ -504,6 +543,14 @@ fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* 
                                     cudaMemcpyHostToDevice, s) != cudaSuccess)
     return FA_ERR_RUNTIME;
   const int64_t total = KH * prefix[B];
+  // the real lengths of a paged cache go to the workspace
+  if (pg != nullptr) {
+    std::vector<int> real(B);
+    for (int64_t b = 0; b < B; ++b) real[b] = static_cast<int>(lens[b]);
+    if (cudaMemcpyAsync(wsb + ws.real_lens, real.data(), B * sizeof(int), cudaMemcpyHostToDevice,
+                        s) != cudaSuccess)
+      return FA_ERR_RUNTIME;
+  }
   // the main kernel clears the status word when it starts; without one, clear it here
   if (total == 0 && cudaMemsetAsync(wsb, 0, sizeof(uint32_t), s) != cudaSuccess)
     return FA_ERR_RUNTIME;
@@ -528,11 +575,47 @@ fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* 
   x.prefix_dev = in_params ? nullptr : reinterpret_cast<const long long*>(wsb + ws.prefix);
   x.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
   x.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
+  x.block_table = pg != nullptr ? pg->block_table : nullptr;
+  x.max_blocks = pg != nullptr ? static_cast<int>(pg->max_blocks) : 0;
+  x.num_blocks = pg != nullptr ? static_cast<int>(pg->num_blocks) : 0;
+  x.block_size = pg != nullptr ? static_cast<int>(pg->block_size) : 0;
+  x.lens_dev = pg != nullptr ? reinterpret_cast<const int*>(wsb + ws.real_lens) : nullptr;
   x.out = out;
   x.lse = lse;
   x.status = reinterpret_cast<uint32_t*>(wsb);
   x.timeout_ns = kDefaultTimeoutNs;
   return launch_decode(x, s) == cudaSuccess ? FA_OK : FA_ERR_RUNTIME;
+}
+
+}  // namespace
+
+fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                    const int64_t* lens, int64_t B, int64_t S_kv_max, int64_t num_heads,
+                    int64_t num_kv_heads, int64_t D, float scale, int layout, int num_splits,
+                    void* out, float* lse, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  return decode_impl(q, k, v, nullptr, key_mask, lens, B, S_kv_max, num_heads, num_kv_heads, D,
+                     scale, layout, num_splits, out, lse, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                          int kv_layout, const int32_t* block_table, int64_t max_blocks_per_seq,
+                          int64_t num_blocks, int64_t block_size, const uint8_t* key_mask,
+                          const int64_t* lens, int64_t B, int64_t num_heads,
+                          int64_t num_kv_heads, int64_t D, float scale, int num_splits, void* out,
+                          float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (block_table == nullptr && B > 0) return FA_ERR_NULLPTR;
+  if (kv_layout != FA_LAYOUT_PA_BBND && kv_layout != FA_LAYOUT_PA_BNBD) return FA_ERR_PARAM_INVALID;
+  if (block_size < 16 || block_size > 1024 || block_size % 16 != 0 || max_blocks_per_seq < 0 ||
+      num_blocks < 0 || max_blocks_per_seq > kMaxDim / 1024 || num_blocks > kMaxDim)
+    return FA_ERR_PARAM_INVALID;
+  const PagedKv pg{block_table, max_blocks_per_seq, std::max<int64_t>(num_blocks, 1), block_size};
+  // blocks of PA_BBND hold rows as BSND does (a block is a batch of
+  // block_size rows), those of PA_BNBD as BNSD
+  const int layout = kv_layout == FA_LAYOUT_PA_BBND ? FA_LAYOUT_BSND : FA_LAYOUT_BNSD;
+  return decode_impl(q, k_cache, v_cache, &pg, key_mask, lens, B, max_blocks_per_seq * block_size,
+                     num_heads, num_kv_heads, D, scale, layout, num_splits, out, lse, workspace,
+                     workspace_bytes, stream);
 }
 
 fa_status fa_workspace_status(void* workspace, void* stream) {

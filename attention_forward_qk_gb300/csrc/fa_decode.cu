@@ -104,7 +104,12 @@ struct DecodeArgs {
   long long rows_per_cta;  // Rc
   int B, Hq, Hkv, S_kv, max_slots, head_groups, G;
   float scale_log2;
-  Prefix prefix;           // prefix[b] = sum of lengths of batches < b
+  // paged K/V: block table [B][max_blocks] (null: contiguous cache), the
+  // real lengths (the work space holds them rounded up to 16 rows)
+  const int32_t* block_table;
+  int max_blocks, block_size;
+  const int* real_len;     // [B] in the workspace (paged only)
+  Prefix prefix;           // prefix[b] = sum of lengths of batches < b (work space)
 };
 
 // Largest b with KH * prefix[b] <= r (the batch whose rows hold r; batches
@@ -124,7 +129,8 @@ struct SlotHeader {
   int piece;   // piece counter of this CTA, -1 = no more work
   int stage;   // stage index within the piece
   int nstage;  // stages of the piece
-  int b, kh, row0, rows, slot, nsp, pad;
+  int b, kh, row0, rows, slot, nsp;
+  int vend;    // rows of the piece that hold keys (< rows only past a paged length)
 };
 
 template <int D, int G>
@@ -210,6 +216,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           h.slot = static_cast<int>(blockIdx.x - u0 / Rc);
           h.nsp = static_cast<int>((u1 - 1) / Rc - u0 / Rc + 1);
           h.nstage = static_cast<int>((rows + C::R - 1) / C::R);
+          h.vend = h.rows;
+          if (a.block_table != nullptr)
+            h.vend = max(0, min(h.rows, __ldg(a.real_len + b) - h.row0));
           kvh = h.kh / a.head_groups;
           hg = h.kh % a.head_groups;
           r += rows;
@@ -234,7 +243,22 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           const int row = h.row0 + s * C::R;
           const int rows_here = min(C::R, h.rows - s * C::R);
           const uint32_t q_bytes = s == 0 ? G * D * 2 : 0;
-          if (rows_here == C::R) {
+          if (a.block_table != nullptr) {
+            // paged: 16-row boxes (pieces and lengths are multiples of 16 rows in
+            // the work space, blocks are multiples of 16 rows), each from its block
+            const int nb = (rows_here + kTailBox - 1) / kTailBox;
+            mbar_expect_tx(full0 + 8 * slot, 2 * nb * kTailBox * D * 2 + q_bytes);
+            const int32_t* bt = a.block_table + static_cast<size_t>(h.b) * a.max_blocks;
+            for (int t = 0; t < nb; ++t) {
+              const int lr = row + t * kTailBox;
+              const int blk = __ldg(bt + lr / a.block_size);
+              const int in_blk = lr % a.block_size;
+              tma_load_4d(dst + t * kTailBox * D * 2, &tm_k16, full0 + 8 * slot, 0, in_blk, kvh,
+                          blk);
+              tma_load_4d(dst + C::TILE_BYTES + t * kTailBox * D * 2, &tm_v16, full0 + 8 * slot,
+                          0, in_blk, kvh, blk);
+            }
+          } else if (rows_here == C::R) {
             mbar_expect_tx(full0 + 8 * slot, C::STAGE_BYTES + q_bytes);
             tma_load_4d(dst, &tm_k, full0 + 8 * slot, 0, row, kvh, h.b);
             tma_load_4d(dst + C::TILE_BYTES, &tm_v, full0 + 8 * slot, 0, row, kvh, h.b);
@@ -286,7 +310,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         // ---- a new piece: q landed with this stage; fresh softmax state
         ++piece_seq;
         row_begin = hd.row0;
-        row_end = hd.row0 + hd.rows;
+        row_end = hd.row0 + hd.vend;  // rows past a paged length hold no key
         mask_row = a.key_mask ? a.key_mask + static_cast<size_t>(hd.b) * a.S_kv : nullptr;
         const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(qbuf + slot * kQBytes);
 #pragma unroll
@@ -661,17 +685,25 @@ cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
   da.prefix.global = x.prefix_dev;
   if (x.prefix_dev == nullptr)
     for (int b = 0; b <= x.B; ++b) da.prefix.local[b] = x.prefix_host[b];
+  da.block_table = x.block_table;
+  da.max_blocks = x.max_blocks;
+  da.block_size = x.block_size;
+  da.real_len = x.lens_dev;
 
   if (x.total > 0) {
     CUtensorMap maps[4];  // K, V with 112-row boxes; K, V with 16-row boxes
-    const int S_map = std::max(x.S_kv, 1);
-    if (!encode_bf16_map(&maps[0], x.k, x.layout, x.B, x.Hkv, S_map, x.D, x.D, kDecodeStageRows,
+    // a paged cache is a batch of num_blocks sequences of block_size rows
+    const int nbat = x.block_table != nullptr ? x.num_blocks : x.B;
+    const int S_map = x.block_table != nullptr ? x.block_size : std::max(x.S_kv, 1);
+    // (the 112-row maps are not used for a paged cache, whose blocks may be shorter)
+    const int box_rows = x.block_table != nullptr ? kTailBox : kDecodeStageRows;
+    if (!encode_bf16_map(&maps[0], x.k, x.layout, nbat, x.Hkv, S_map, x.D, x.D, box_rows,
                          CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_bf16_map(&maps[1], x.v, x.layout, x.B, x.Hkv, S_map, x.D, x.D, kDecodeStageRows,
+        !encode_bf16_map(&maps[1], x.v, x.layout, nbat, x.Hkv, S_map, x.D, x.D, box_rows,
                          CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_bf16_map(&maps[2], x.k, x.layout, x.B, x.Hkv, S_map, x.D, x.D, kTailBox,
+        !encode_bf16_map(&maps[2], x.k, x.layout, nbat, x.Hkv, S_map, x.D, x.D, kTailBox,
                          CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_bf16_map(&maps[3], x.v, x.layout, x.B, x.Hkv, S_map, x.D, x.D, kTailBox,
+        !encode_bf16_map(&maps[3], x.v, x.layout, nbat, x.Hkv, S_map, x.D, x.D, kTailBox,
                          CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
     const int grid = static_cast<int>((x.total + x.rows_per_cta - 1) / x.rows_per_cta);

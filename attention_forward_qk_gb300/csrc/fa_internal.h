@@ -48,6 +48,14 @@ struct DecodeLaunch {
   const long long* prefix_dev;   // the same in the workspace, or null (then in params)
   float* part_o;            // [B, Hq, max_slots, D]
   float* part_lse;          // [B, Hq, max_slots] (log2 domain)
+  // paged K/V (block_table != null): k, v are block pools of num_blocks blocks
+  // of block_size rows in `layout` (BSND: PA_BBND, BNSD: PA_BNBD), logical
+  // row r of batch b lives in block block_table[b * max_blocks + r / block_size];
+  // the work space then holds every length rounded up to 16 rows and
+  // lens_host / lens_dev give the real ones
+  const int32_t* block_table;
+  int max_blocks, num_blocks, block_size;
+  const int* lens_dev;      // [B] real lengths in the workspace (paged only)
   void* out;
   float* lse;
   uint32_t* status;

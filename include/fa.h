@@ -71,7 +71,13 @@ typedef enum {
   FA_ERR_DEVICE_TIMEOUT = 6       /* a kernel's bounded wait expired; outputs are undefined */
 } fa_status;
 
-typedef enum { FA_LAYOUT_BNSD = 0, FA_LAYOUT_BSND = 1 } fa_layout;
+typedef enum {
+  FA_LAYOUT_BNSD = 0,
+  FA_LAYOUT_BSND = 1,
+  /* paged K/V caches (FlashAttn guide §1.2, layout_kv), fa_decode_paged only */
+  FA_LAYOUT_PA_BBND = 2, /* [num_blocks, block_size, KV_N, D]: rows of a block as BSND */
+  FA_LAYOUT_PA_BNBD = 3  /* [num_blocks, KV_N, block_size, D]: rows of a block as BNSD */
+} fa_layout;
 
 /* Mask modes, numbered as in FlashAttn guide §1.5 (0 = none, 3 = causal,
  * 4 = window; the window takes its widths through fa_forward_window). */
@@ -154,6 +160,34 @@ fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* 
                     int64_t num_heads, int64_t num_kv_heads, int64_t D, float scale, int layout,
                     int num_splits, void* out, float* lse, void* workspace,
                     size_t workspace_bytes, void* stream);
+
+/* Split-KV decode against a paged K/V cache (FlashAttn guide §1.2,
+ * PagedAttention: the cache is stored in blocks of block_size tokens and a
+ * block table maps each sequence's logical blocks to physical ones).
+ *   q                   [B, num_heads, 1, D] or [B, 1, num_heads, D], device bf16
+ *   k_cache, v_cache    device bf16 block pools in kv_layout:
+ *                       FA_LAYOUT_PA_BBND [num_blocks, block_size, KV_N, D] or
+ *                       FA_LAYOUT_PA_BNBD [num_blocks, KV_N, block_size, D]
+ *   block_table         device int32 [B, max_blocks_per_seq]; token r of
+ *                       sequence b is row r % block_size of block
+ *                       block_table[b * max_blocks_per_seq + r / block_size].
+ *                       Entries past a sequence's last block are never read;
+ *                       an entry outside [0, num_blocks) reads zeros.
+ *   block_size          in [16, 1024], a multiple of 16
+ *   key_mask            NULL or device uint8 [B, max_blocks_per_seq * block_size]
+ *   actual_seq_lengths  HOST int64 [B], required, each in
+ *                       [0, max_blocks_per_seq * block_size]
+ *   the rest as for fa_decode; the workspace is
+ *   fa_decode_workspace_size(B, max_blocks_per_seq * block_size, ...).
+ * Errors: a bad kv_layout or block_size, or negative counts ->
+ * FA_ERR_PARAM_INVALID; block_table NULL with B > 0 -> FA_ERR_NULLPTR;
+ * otherwise those of fa_decode. */
+fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cache, int kv_layout,
+                          const int32_t* block_table, int64_t max_blocks_per_seq,
+                          int64_t num_blocks, int64_t block_size, const uint8_t* key_mask,
+                          const int64_t* actual_seq_lengths, int64_t B, int64_t num_heads,
+                          int64_t num_kv_heads, int64_t D, float scale, int num_splits, void* out,
+                          float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /* The decode split plan for these arguments (pure host computation, no
  * CUDA call). Every (batch, KV head, group of query heads handled together)

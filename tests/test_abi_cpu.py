@@ -240,3 +240,39 @@ def test_plan_rejects_bad_args(lib):
         _plan([5], 8, 8, 8, sms=0)
     with pytest.raises(_lib.FaError):
         _plan([5], 8, 8, 8, D=96)
+
+
+def _dec_paged(lib, **kw):
+    args = dict(q=P, k=P, v=P, kvl=2, bt=P, maxb=4, nblk=16, bs=64, key_mask=None, lens=[100, 7],
+                B=2, Hq=8, Hkv=2, D=128, scale=0.1, splits=0, out=P, lse=None, ws=WS,
+                ws_bytes=1 << 22, stream=None)
+    args.update(kw)
+    lens = args["lens"]
+    if lens is not None:
+        lens = (ctypes.c_int64 * max(len(lens), 1))(*lens)
+    return lib.fa_decode_paged(args["q"], args["k"], args["v"], args["kvl"], args["bt"],
+                               args["maxb"], args["nblk"], args["bs"], args["key_mask"], lens,
+                               args["B"], args["Hq"], args["Hkv"], args["D"], args["scale"],
+                               args["splits"], args["out"], args["lse"], args["ws"],
+                               args["ws_bytes"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(bt=None), _lib.FA_ERR_NULLPTR),
+    (dict(lens=None), _lib.FA_ERR_NULLPTR),
+    (dict(kvl=0), _lib.FA_ERR_PARAM_INVALID),    # a contiguous layout is not a paged one
+    (dict(kvl=7), _lib.FA_ERR_PARAM_INVALID),
+    (dict(bs=8), _lib.FA_ERR_PARAM_INVALID),     # below 16
+    (dict(bs=40), _lib.FA_ERR_PARAM_INVALID),    # not a multiple of 16
+    (dict(bs=2048), _lib.FA_ERR_PARAM_INVALID),  # above 1024
+    (dict(maxb=-1), _lib.FA_ERR_PARAM_INVALID),
+    (dict(lens=[257, 1]), _lib.FA_ERR_PARAM_INVALID),  # past max_blocks * block_size
+    (dict(D=96), _lib.FA_ERR_UNSUPPORTED),
+    (dict(ws_bytes=16), _lib.FA_ERR_WORKSPACE_TOO_SMALL),
+])
+def test_decode_paged_rejects_before_any_cuda_call(lib, kw, expect):
+    assert _dec_paged(lib, **kw) == expect
+
+
+def test_decode_paged_zero_batch_is_noop(lib):
+    assert _dec_paged(lib, B=0, lens=[], bt=None) == _lib.FA_OK
