@@ -219,6 +219,26 @@ class Runner:
                     if p:
                         km[b, w.S_kv - p:] = 1
                 self.km = km.to(dev)
+        self.table = None
+        if w.block_size is not None:
+            # scatter the cache into a pool of blocks in a seeded random order
+            bs = w.block_size
+            nb_seq = (w.S_kv + bs - 1) // bs
+            perm = torch.randperm(w.B * nb_seq, generator=torch.Generator().manual_seed(w.seed))
+            self.table = perm.view(w.B, nb_seq).to(torch.int32).to(dev)
+            pool = lambda t: torch.empty(w.B * nb_seq, bs, w.Hkv, w.D, dtype=t.dtype, device=dev)
+            kp, vp = pool(self.k), pool(self.v)
+            kb = workloads.to_bnsd(self.k, w.layout)
+            vb = workloads.to_bnsd(self.v, w.layout)
+            idx = self.table.view(-1).long()
+            kp[idx] = kb.reshape(w.B, w.Hkv, nb_seq, bs, w.D).permute(0, 2, 3, 1, 4) \
+                .reshape(w.B * nb_seq, bs, w.Hkv, w.D)
+            vp[idx] = vb.reshape(w.B, w.Hkv, nb_seq, bs, w.D).permute(0, 2, 3, 1, 4) \
+                .reshape(w.B * nb_seq, bs, w.Hkv, w.D)
+            self.k, self.v = kp, vp
+            if host_copy:  # the end-to-end copies then move the pools
+                self.host["k"] = kp.cpu().pin_memory()
+                self.host["v"] = vp.cpu().pin_memory()
         self.out = torch.empty_like(self.q)
         self.lse = torch.empty((w.B, w.Hq, w.S_q), dtype=torch.float32, device=dev)
         if w.kind == "decode":
@@ -229,7 +249,10 @@ class Runner:
 
     def step(self):
         w, F = self.w, self.F
-        if self.kind == "decode":
+        if self.kind == "decode" and self.table is not None:
+            F.fa_decode_paged(self.q, self.k, self.v, self.table, w.block_size, self.lens,
+                              scale=w.scale, out=self.out, lse=self.lse, workspace=self.ws)
+        elif self.kind == "decode":
             F.fa_decode(self.q, self.k, self.v, self.lens, scale=w.scale, layout=w.layout,
                         out=self.out, lse=self.lse, workspace=self.ws)
         elif w.window is not None:
@@ -445,7 +468,7 @@ def run_gpu(args):
     others = {}
     if not args.only:
         for name in ("long_decode", "causal_prefill", "gqa_masked_prefill", "tiny_prefill",
-                     "window_prefill", "gqa_decode"):
+                     "window_prefill", "paged_decode", "gqa_decode"):
             if name == args.workload:
                 continue
             wo = workloads.WORKLOADS[name]

@@ -107,3 +107,28 @@ def test_paged_equals_contiguous_decode(cuda_device):
     torch.cuda.synchronize()
     assert (a[0].float() - b[0].float()).abs().max().item() <= 2e-2
     assert (a[1] - b[1]).abs().max().item() <= 1e-3
+
+
+def test_paged_workload_matches_contiguous_run(cuda_device):
+    """The bench's paged decode workload: the paged call on the shuffled pool
+    against the oracle on the logical cache (full size, every head)."""
+    w = workloads.WORKLOADS["paged_decode"]
+    x = workloads.make(w)
+    lens = x["lengths"]
+    bs = w.block_size
+    nb = (w.S_kv + bs - 1) // bs
+    perm = torch.randperm(w.B * nb, generator=torch.Generator().manual_seed(w.seed))
+    table = perm.view(w.B, nb).to(torch.int32)
+    kb = workloads.to_bnsd(x["k"], w.layout)
+    vb = workloads.to_bnsd(x["v"], w.layout)
+    kp = torch.empty(w.B * nb, bs, w.Hkv, w.D, dtype=torch.bfloat16)
+    vp = torch.empty_like(kp)
+    kp[table.view(-1).long()] = kb.reshape(w.B, w.Hkv, nb, bs, w.D).permute(0, 2, 3, 1, 4) \
+        .reshape(-1, bs, w.Hkv, w.D)
+    vp[table.view(-1).long()] = vb.reshape(w.B, w.Hkv, nb, bs, w.D).permute(0, 2, 3, 1, 4) \
+        .reshape(-1, bs, w.Hkv, w.D)
+    out, lse = F.fa_decode_paged(x["q"].cuda(), kp.cuda(), vp.cuda(), table.cuda(), bs, lens,
+                                 scale=w.scale)
+    torch.cuda.synchronize()
+    ro, rl = oracle.decode(x["q"], x["k"], x["v"], lens, scale=w.scale, layout=w.layout)
+    compare(out, lse, ro, rl, w.layout)

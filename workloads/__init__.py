@@ -57,6 +57,8 @@ class Workload:
     max_pad: int | None = None
     # prefill: sliding window (win_left, win_right), -1 = no limit on that side
     window: tuple | None = None
+    # decode: paged cache of blocks of this many rows (PA_BBND), or None
+    block_size: int | None = None
     note: str = field(default="", compare=False)
 
     @property
@@ -92,6 +94,13 @@ WORKLOADS: dict[str, Workload] = {
         "window_prefill", "prefill", B=2, Hq=32, Hkv=8, S_q=8192, S_kv=8192, D=128,
         layout="BNSD", seed=106, window=(1023, 0),
         note="B=2 Hq=32 Hkv=8 S=8192 D=128 BNSD, window of 1024 keys (1023 before, 0 after)"),
+    # Beyond the five: the GQA decode workload with its cache paged (FlashAttn
+    # guide §1.2, PA_BBND, 128-row blocks in shuffled order).
+    "paged_decode": Workload(
+        "paged_decode", "decode", B=8, Hq=32, Hkv=8, S_q=1, S_kv=8192, D=128,
+        layout="BNSD", seed=107, len_lo=1024, len_hi=8192, garbage=True, block_size=128,
+        note="B=8 Hq=32 Hkv=8 D=128, paged cache (PA_BBND, 128-row blocks, shuffled), "
+             "L_b~U[1024,8192]"),
 }
 
 
