@@ -8,6 +8,7 @@ package imports nothing from the product path.
 from .sdpa import (  # noqa: F401
     attention,
     attention_bruteforce,
+    attention_varlen,
     decode,
     split_partials,
     merge_max_sum,

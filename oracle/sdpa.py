@@ -283,3 +283,28 @@ def merge_lse(lses, onorms):
     W = sum(w)
     res = sum(oi * (wi / W) for oi, wi in zip(onorms, w))
     return res, M + math.log(W)
+
+
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, *, scale: float = 1.0,
+                     causal: bool = False):
+    """Packed variable-length sequences ([FA] §1.3 TND layout, §1.4
+    cu_seqlens): q [T_q, Hq, D], k/v [T_kv, Hkv, D]; sequence b is q rows
+    cu_q[b]..cu_q[b+1]-1 against k/v rows cu_kv[b]..cu_kv[b+1]-1, each an
+    independent attention (causal top-left aligned within the sequence).
+    Returns out [T_q, Hq, D] and lse [T_q, Hq] (the TND lse shape of [FA] §1.6).
+    """
+    qn, kn, vn = _as_f64(q), _as_f64(k), _as_f64(v)
+    T_q, Hq, D = qn.shape
+    out = np.zeros((T_q, Hq, D))
+    lse = np.full((T_q, Hq), np.inf)
+    B = len(cu_seqlens_q) - 1
+    for b in range(B):
+        q0, q1 = int(cu_seqlens_q[b]), int(cu_seqlens_q[b + 1])
+        k0, k1 = int(cu_seqlens_kv[b]), int(cu_seqlens_kv[b + 1])
+        if q1 == q0:
+            continue
+        o, l = attention(qn[None, q0:q1], kn[None, k0:k1], vn[None, k0:k1], scale=scale,
+                         layout="BSND", causal=causal)
+        out[q0:q1] = o[0]
+        lse[q0:q1] = l[0].T
+    return out, lse

@@ -366,3 +366,43 @@ def test_window_wider_than_sequence_is_no_mask():
     b = oracle.attention(q, k, v, scale=0.5, layout="BSND", window=(6, 6))
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_array_equal(a[1], b[1])
+
+
+# ------------------------------------------------------- packed sequences
+# [FA] developer guide §1.3 (TND) and §1.4 (cu_seqlens).
+
+def test_varlen_equals_per_sequence_bruteforce():
+    g = torch.Generator().manual_seed(12)
+    lq, lkv = [3, 0, 5, 1], [4, 2, 5, 0]
+    cq = np.concatenate([[0], np.cumsum(lq)])
+    ckv = np.concatenate([[0], np.cumsum(lkv)])
+    Hq, Hkv, D = 4, 2, 6
+    q = torch.randn(int(cq[-1]), Hq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(int(ckv[-1]), Hkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(int(ckv[-1]), Hkv, D, generator=g).to(torch.bfloat16)
+    out, lse = oracle.attention_varlen(q, k, v, cq, ckv, scale=0.3)
+    for b in range(4):
+        if lq[b] == 0:
+            continue
+        qs = q[cq[b]:cq[b + 1]][None]
+        ks, vs = k[ckv[b]:ckv[b + 1]][None], v[ckv[b]:ckv[b + 1]][None]
+        ro, rl = oracle.attention_bruteforce(qs, ks, vs, scale=0.3, layout="BSND")
+        np.testing.assert_allclose(out[cq[b]:cq[b + 1]], ro[0], rtol=0, atol=1e-12)
+        np.testing.assert_array_equal(np.isfinite(lse[cq[b]:cq[b + 1]]), np.isfinite(rl[0].T))
+        fin = np.isfinite(rl[0].T)
+        np.testing.assert_allclose(lse[cq[b]:cq[b + 1]][fin], rl[0].T[fin], rtol=0, atol=1e-12)
+    # the sequence with no keys: invalid rows (out 0, lse +inf), [FA] §1.7
+    assert np.all(out[cq[3]:cq[4]] == 0) and np.all(lse[cq[3]:cq[4]] == np.inf)
+
+
+def test_varlen_equal_lengths_match_padded_batch():
+    """With equal lengths the packed layout is the BSND batch reshaped."""
+    B, S, Hq, Hkv, D = 3, 7, 4, 2, 8
+    x = workloads.make_prefill(B, Hq, Hkv, S, S, D, "BSND", 21)
+    cu = np.arange(B + 1) * S
+    o1, l1 = oracle.attention_varlen(x["q"].reshape(B * S, Hq, D), x["k"].reshape(B * S, Hkv, D),
+                                     x["v"].reshape(B * S, Hkv, D), cu, cu, scale=0.2,
+                                     causal=True)
+    o2, l2 = oracle.attention(x["q"], x["k"], x["v"], scale=0.2, layout="BSND", causal=True)
+    np.testing.assert_array_equal(o1, o2.reshape(B * S, Hq, D))
+    np.testing.assert_array_equal(l1, l2.transpose(0, 2, 1).reshape(B * S, Hq))
