@@ -66,7 +66,7 @@ int64_t max_slots_bound(int64_t S_kv_max, int num_splits) {
 }
 
 struct PrefillWs {
-  size_t sched, lens, bits, total;
+  size_t sched, varlen, lens, bits, total;
 };
 
 // Work items of a prefill launch: 256 query rows of one (batch, query head).
@@ -75,12 +75,14 @@ int64_t prefill_items(int64_t B, int64_t S_q, int64_t num_heads) {
 }
 
 // [status, item counter | pad][schedule: offsets of kMaxPrefillCtas + 1 CTAs,
-// then the item lists][lengths][per-tile key validity]
+// then the item lists][packed-sequence table][lengths][per-tile key validity]
 PrefillWs prefill_ws(int64_t B, int64_t S_q, int64_t S_kv, int64_t num_heads) {
   PrefillWs w;
   size_t off = kAlign;  // status word
   w.sched = off;
   off += align_up(sizeof(int32_t) * (kMaxPrefillCtas + 1 + prefill_items(B, S_q, num_heads)));
+  w.varlen = off;  // packed sequences only: [4][B] offsets and lengths
+  off += align_up(sizeof(int32_t) * 4 * B);
   w.lens = off;
   off += align_up(sizeof(int32_t) * B);
   w.bits = off;
@@ -99,22 +101,30 @@ PrefillWs prefill_ws(int64_t B, int64_t S_q, int64_t S_kv, int64_t num_heads) {
 // time read the K/V of a few units out of L2. The cost of an item is its KV
 // tiles under the causal or window limits plus a constant for its start-up.
 // Layout: offsets[grid + 1] into the lists, then the item lists (int32).
+// lq, lkv: per-sequence lengths of packed sequences (else null); items past a
+// sequence's query rows do not exist and are not scheduled.
 void build_prefill_schedule(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t S_kv,
                             int64_t win_left, int64_t win_right, int grid,
-                            std::vector<int32_t>& sched) {
+                            std::vector<int32_t>& sched, const int32_t* lq = nullptr,
+                            const int32_t* lkv = nullptr) {
   const int64_t g = Hq / Hkv;
   const int64_t nq = ceil_div(S_q, 256);
   const int64_t n_tiles = ceil_div(std::max<int64_t>(S_kv, 1), 128);
   const int64_t per_unit = nq * g;
   const int64_t units = B * Hkv;
   const int64_t n_items = units * per_unit;
+  // -1: the item does not exist
   auto cost = [&](int64_t w) -> int64_t {
     const int64_t qp = nq - 1 - (w % per_unit) / g;
-    int64_t lo_u = n_tiles, hi_u = 0;
+    const int64_t b = (w / per_unit) / Hkv;
+    const int64_t sq = lq ? lq[b] : S_q;
+    const int64_t nt = lkv ? ceil_div(static_cast<int64_t>(lkv[b]), 128) : n_tiles;
+    if (qp * 256 >= sq) return -1;
+    int64_t lo_u = nt, hi_u = 0;
     for (int t = 0; t < 2; ++t) {
       const int64_t r0 = qp * 256 + t * 128;
-      if (t == 1 && r0 >= S_q) break;
-      int64_t lo = 0, hi = n_tiles;
+      if (t == 1 && r0 >= sq) break;
+      int64_t lo = 0, hi = nt;
       if (win_left >= 0) lo = std::max<int64_t>(0, r0 - win_left) / 128;
       if (win_right >= 0) hi = std::min(hi, (r0 + 127 + win_right) / 128 + 1);
       lo_u = std::min(lo_u, lo);
@@ -135,7 +145,10 @@ void build_prefill_schedule(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int
     const int64_t w0 = u0 * per_unit;
     const int64_t w1 = std::min(units, u0 + 8) * per_unit;
     grp.clear();
-    for (int64_t w = w0; w < w1; ++w) grp.emplace_back(-cost(w), w);
+    for (int64_t w = w0; w < w1; ++w) {
+      const int64_t c = cost(w);
+      if (c >= 0) grp.emplace_back(-c, w);
+    }
     std::stable_sort(grp.begin(), grp.end(),
                      [](const std::pair<int64_t, int64_t>& x, const std::pair<int64_t, int64_t>& y) {
                        return x.first < y.first;
@@ -148,7 +161,10 @@ void build_prefill_schedule(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int
       std::push_heap(heap.begin(), heap.end(), cmp);
     }
   }
-  sched.assign(grid + 1 + n_items, 0);
+  (void)n_items;
+  size_t listed = 0;
+  for (const auto& l : lists) listed += l.size();
+  sched.assign(grid + 1 + listed, 0);
   int32_t off = 0;
   for (int c = 0; c < grid; ++c) {
     sched[c] = off;
@@ -350,12 +366,15 @@ namespace {
 
 // Shared by fa_forward and fa_forward_window: the window (-1, -1) is no mask,
 // (-1, 0) is causal.
+// cu_q, cu_kv: HOST prefix offsets of packed sequences (else null); then
+// S_q / S_kv are the longest sequences and the tensors are [T, H, D].
 fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok,
                        int64_t win_left, int64_t win_right, const uint8_t* key_mask,
                        const int64_t* lens,
                        int64_t B, int64_t S_q, int64_t S_kv, int64_t num_heads,
                        int64_t num_kv_heads, int64_t D, float scale, int layout, void* out,
-                       float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+                       float* lse, void* workspace, size_t workspace_bytes, void* stream,
+                       const int64_t* cu_q = nullptr, const int64_t* cu_kv = nullptr) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || workspace == nullptr)
     return FA_ERR_NULLPTR;
   int64_t Hkv = num_kv_heads;
@@ -363,7 +382,10 @@ fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok
   if (st != FA_OK) return st;
   if (!mask_ok || win_left < -1 || win_right < -1) return FA_ERR_PARAM_INVALID;
   const bool windowed = win_left >= 0 || win_right >= 0;
-  if (windowed && S_q != S_kv) return FA_ERR_PARAM_INVALID;
+  if (windowed && S_q != S_kv && cu_q == nullptr) return FA_ERR_PARAM_INVALID;
+  if (windowed && cu_q != nullptr)
+    for (int64_t b = 0; b < B; ++b)
+      if (cu_q[b + 1] - cu_q[b] != cu_kv[b + 1] - cu_kv[b]) return FA_ERR_PARAM_INVALID;
   // wider than the sequence is no limit (and keeps the tile arithmetic in int)
   if (win_left >= S_kv) win_left = -1;
   if (win_right >= S_kv) win_right = -1;
@@ -396,13 +418,28 @@ fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok
   thread_local SchedKey sched_key{-1, 0, 0, 0, 0, 0, 0, 0};
   thread_local std::vector<int32_t> sched;
   const SchedKey key{B, num_heads, Hkv, S_q, S_kv, win_left, win_right, grid};
-  if (!(key == sched_key)) {
+  std::vector<int32_t> vtab;  // packed sequences: [4][B] q off, q len, kv off, kv len
+  if (cu_q != nullptr) {
+    vtab.resize(4 * B);
+    for (int64_t b = 0; b < B; ++b) {
+      vtab[b] = static_cast<int32_t>(cu_q[b]);
+      vtab[B + b] = static_cast<int32_t>(cu_q[b + 1] - cu_q[b]);
+      vtab[2 * B + b] = static_cast<int32_t>(cu_kv[b]);
+      vtab[3 * B + b] = static_cast<int32_t>(cu_kv[b + 1] - cu_kv[b]);
+    }
+    // depends on the lengths: built for every call
+    build_prefill_schedule(B, num_heads, Hkv, S_q, S_kv, win_left, win_right, grid, sched,
+                           vtab.data() + B, vtab.data() + 3 * B);
+    sched_key = SchedKey{-1, 0, 0, 0, 0, 0, 0, 0};
+  } else if (!(key == sched_key)) {
     build_prefill_schedule(B, num_heads, Hkv, S_q, S_kv, win_left, win_right, grid, sched);
     sched_key = key;
   }
-  // header: zeroed status word, the schedule, then the lengths as int32 when given
+  // header: zeroed status word, the schedule, the packed-sequence table, then
+  // the lengths as int32 when given
   std::vector<int32_t> blob(ws.lens / 4 + (lens ? B : 0), 0);
   std::copy(sched.begin(), sched.end(), blob.begin() + ws.sched / 4);
+  std::copy(vtab.begin(), vtab.end(), blob.begin() + ws.varlen / 4);
   if (lens)
     for (int64_t b = 0; b < B; ++b) blob[ws.lens / 4 + b] = static_cast<int32_t>(lens[b]);
   if (cudaMemcpyAsync(wsb, blob.data(), blob.size() * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
@@ -434,6 +471,9 @@ fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok
   x.tile_bits = bits;
   x.sched = reinterpret_cast<const int32_t*>(wsb + ws.sched);
   x.grid = grid;
+  x.varlen = cu_q != nullptr ? reinterpret_cast<const int32_t*>(wsb + ws.varlen) : nullptr;
+  x.T_q = cu_q != nullptr ? cu_q[B] : 0;
+  x.T_kv = cu_kv != nullptr ? cu_kv[B] : 0;
   x.out = out;
   x.lse = lse;
   x.status = reinterpret_cast<uint32_t*>(wsb);
@@ -458,6 +498,36 @@ fa_status fa_forward(const void* q, const void* k, const void* v, int mask_mode,
   return forward_impl(q, k, v, mask_ok, -1, causal ? 0 : -1, key_mask, lens, B, S_q, S_kv, num_heads,
                       num_kv_heads, D, scale, layout, out, lse, workspace, workspace_bytes,
                       stream);
+}
+
+size_t fa_forward_varlen_workspace_size(int64_t B, int64_t max_seqlen_q, int64_t max_seqlen_kv,
+                                        int64_t num_heads, int64_t num_kv_heads, int64_t D) {
+  return fa_forward_workspace_size(B, max_seqlen_q, max_seqlen_kv, num_heads, num_kv_heads, D);
+}
+
+fa_status fa_forward_varlen(const void* q, const void* k, const void* v,
+                            const int64_t* cu_seqlens_q, const int64_t* cu_seqlens_kv,
+                            int mask_mode, int64_t B, int64_t num_heads, int64_t num_kv_heads,
+                            int64_t D, float scale, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (cu_seqlens_q == nullptr || cu_seqlens_kv == nullptr) return FA_ERR_NULLPTR;
+  if (B < 0) return FA_ERR_PARAM_INVALID;
+  if (cu_seqlens_q[0] != 0 || cu_seqlens_kv[0] != 0) return FA_ERR_PARAM_INVALID;
+  int64_t max_q = 0, max_kv = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t lq = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+    const int64_t lkv = cu_seqlens_kv[b + 1] - cu_seqlens_kv[b];
+    if (lq < 0 || lkv < 0) return FA_ERR_PARAM_INVALID;
+    max_q = std::max(max_q, lq);
+    max_kv = std::max(max_kv, lkv);
+  }
+  if (cu_seqlens_q[B] > kMaxDim || cu_seqlens_kv[B] > kMaxDim) return FA_ERR_PARAM_INVALID;
+  const bool mask_ok = mask_mode == FA_MASK_NONE || mask_mode == FA_MASK_CAUSAL;
+  const bool causal = mask_mode == FA_MASK_CAUSAL;
+  // packed tensors [T, H, D] are BSND with one batch
+  return forward_impl(q, k, v, mask_ok, -1, causal ? 0 : -1, nullptr, nullptr, B, max_q, max_kv,
+                      num_heads, num_kv_heads, D, scale, FA_LAYOUT_BSND, out, lse, workspace,
+                      workspace_bytes, stream, cu_seqlens_q, cu_seqlens_kv);
 }
 
 fa_status fa_forward_window(const void* q, const void* k, const void* v, int64_t win_left,

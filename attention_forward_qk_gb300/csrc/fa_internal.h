@@ -72,6 +72,11 @@ struct PrefillLaunch {
   float scale;
   const uint32_t* tile_bits;  // [B][ceil(S_kv/128)][4] or null
   const int32_t* sched;       // per-CTA work-item lists (offsets[grid + 1], then the lists)
+  // packed sequences: [4][B] q offset, q length, kv offset, kv length (device),
+  // or null; then q/k/v/out are [T, H, D] (BSND with B = 1 in the tile maps),
+  // S_q / S_kv the longest sequence and lse [T_q, Hq]
+  const int32_t* varlen;
+  long long T_q, T_kv;        // packed rows of q and k/v (packed sequences only)
   int grid;                   // persistent CTAs
   void* out;
   float* lse;

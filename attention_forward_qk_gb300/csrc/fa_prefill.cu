@@ -71,6 +71,9 @@ struct PrefillArgs {
   float* lse;
   const uint32_t* tile_bits;  // [B][n_kv_tiles][4], bit set = key valid; or null
   const int32_t* sched;       // offsets[grid + 1], then each CTA's work items in order
+  // packed variable-length sequences (TND): q offset, q length, kv offset, kv
+  // length per sequence ([4][B]); null for the padded layouts
+  const int32_t* varlen;
   uint32_t* status;
   uint64_t timeout_ns;
   int B, Hq, Hkv, S_q, S_kv;
@@ -121,6 +124,9 @@ struct TileSeq {
 // the same K/V tiles out of L2.
 struct WorkItem {
   int b, kvh, h, q_row0;
+  int S_q, S_kv, n_kv;   // this sequence's query rows, keys and KV tiles
+  int q_base, kv_base;   // its first row in the q and k/v tensors (packed layout)
+  int tma_b;             // batch coordinate of its tiles (0 when packed)
   bool has_t1;
   int lo_t[2], n_t[2];  // KV tiles [lo_t, n_t) each Q tile needs
   TileSeq seq;
@@ -137,11 +143,26 @@ __device__ __forceinline__ WorkItem work_item(const PrefillArgs& a, int w) {
   it.kvh = bkv % a.Hkv;
   it.h = it.kvh * g + rem % g;
   it.q_row0 = qp * 2 * kBM;
-  it.has_t1 = it.q_row0 + kBM < a.S_q;
+  if (a.varlen != nullptr) {
+    it.q_base = __ldg(a.varlen + it.b);
+    it.S_q = __ldg(a.varlen + a.B + it.b);
+    it.kv_base = __ldg(a.varlen + 2 * a.B + it.b);
+    it.S_kv = __ldg(a.varlen + 3 * a.B + it.b);
+    it.n_kv = (it.S_kv + kBN - 1) / kBN;
+    it.tma_b = 0;
+  } else {
+    it.q_base = 0;
+    it.S_q = a.S_q;
+    it.kv_base = 0;
+    it.S_kv = a.S_kv;
+    it.n_kv = a.n_kv_tiles;
+    it.tma_b = it.b;
+  }
+  it.has_t1 = it.q_row0 + kBM < it.S_q;
   for (int t = 0; t < 2; ++t) {
     // rows r0 .. r0+127 see keys r0 - wl .. r0 + 127 + wr (window, causal = (-1, 0))
     const int r0 = it.q_row0 + t * kBM;
-    int lo = 0, n = a.n_kv_tiles;
+    int lo = 0, n = it.n_kv;
     if (a.win_left >= 0) lo = max(0, r0 - a.win_left) / kBN;
     if (a.win_right >= 0) n = min(n, (r0 + kBM - 1 + a.win_right) / kBN + 1);
     if (t == 1 && !it.has_t1) n = 0;
@@ -225,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int w = item_of(r);
       if (w >= a.n_items) break;
       const WorkItem wi = work_item(a, w);
-      const int b = wi.b, kvh = wi.kvh;
+      const int kvh = wi.kvh;
       const TileSeq& seq = wi.seq;
       if (r > 0) {
         // the Q region is free once both streams' S products of the last item are done
@@ -240,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < nq; ++t)
           for (int s = 0; s < D / 64; ++s)
             tma_load_4d(smem_u32(smem + C::kQOff + t * C::kTileBytes + s * C::kSubBytes), &tm_q,
-                        bar(kBarQ), s * 64, wi.q_row0 + t * kBM, wi.h, b);
+                        bar(kBarQ), s * 64, wi.q_base + wi.q_row0 + t * kBM, wi.h, wi.tma_b);
       }
       __syncwarp();
       for (int j = seq.next(0); ok && j < seq.end; j = seq.next(j + 1)) {
@@ -261,7 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             mbar_expect_tx(bar(kBarFix), C::kTileBytes);
             for (int s = 0; s < D / 64; ++s)
-              tma_load_4d(dst + s * C::kSubBytes, map, bar(kBarFix), s * 64, j * kBN, kvh, b);
+              tma_load_4d(dst + s * C::kSubBytes, map, bar(kBarFix), s * 64,
+                          wi.kv_base + j * kBN, kvh, wi.tma_b);
           }
           ++item;
           ok = mbar_wait(bar(kBarFix), fixes & 1, a.timeout_ns, a.status, kDevTimeoutKvFull,
@@ -288,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             mbar_expect_tx(bar(kBarKvFull + slot), C::kTileBytes);
             for (int s = 0; s < D / 64; ++s)
-              tma_load_4d(dst + s * C::kSubBytes, map, bar(kBarKvFull + slot), s * 64, j * kBN,
-                          kvh, b);
+              tma_load_4d(dst + s * C::kSubBytes, map, bar(kBarKvFull + slot), s * 64,
+                          wi.kv_base + j * kBN, kvh, wi.tma_b);
           }
           ++item;
         }
@@ -494,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r0 = q_row0 + t * kBM;
       const bool masked = (a.win_right >= 0 && j * kBN + kBN - 1 > r0 + a.win_right) ||
                           (a.win_left >= 0 && j * kBN < r0 + kBM - 1 - a.win_left) ||
-                          ((j + 1) * kBN > a.S_kv) || !seq.full(j) || c < 0.f;
+                          ((j + 1) * kBN > wi.S_kv) || !seq.full(j) || c < 0.f;
       float tmax = -INFINITY;
       if (masked) {
 #pragma unroll
@@ -510,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // folded into the validity words
         {
           const int base = j * kBN;
-          int hi_k = a.S_kv - base;
+          int hi_k = wi.S_kv - base;
           if (a.win_right >= 0) hi_k = min(hi_k, row + a.win_right + 1 - base);
           const int lo_k = a.win_left >= 0 ? row - a.win_left - base : 0;
 #pragma unroll
@@ -625,12 +647,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(bar(kBarODrained + t));
-      const bool row_ok = row < a.S_q;
+      const bool row_ok = row < wi.S_q;
       const bool invalid = (l_run == 0.f);
       const float inv_l = invalid ? 0.f : 1.f / l_run;
-      __nv_bfloat16* dst = a.out + static_cast<long long>(wi.b) * a.out_batch_stride +
+      __nv_bfloat16* dst = a.out + static_cast<long long>(wi.tma_b) * a.out_batch_stride +
                            static_cast<long long>(wi.h) * a.out_head_stride +
-                           static_cast<long long>(row) * a.out_row_stride;
+                           static_cast<long long>(wi.q_base + row) * a.out_row_stride;
       if (row_ok) {
 #pragma unroll
         for (int q4 = 0; q4 < D / 32; ++q4) {
@@ -649,7 +671,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (row_ok && a.lse != nullptr)
-        a.lse[(static_cast<long long>(wi.b) * a.Hq + wi.h) * a.S_q + row] =
+        // [B, Hq, S_q], or [T_q, Hq] for packed sequences
+        a.lse[a.varlen != nullptr ? static_cast<long long>(wi.q_base + row) * a.Hq + wi.h
+                                  : (static_cast<long long>(wi.b) * a.Hq + wi.h) * a.S_q + row] =
             invalid ? INFINITY : (m_run + log2f(l_run)) * 0.69314718055994530942f;
     }
   }
@@ -708,12 +732,16 @@ cudaError_t launch_prefill_d(const PrefillLaunch& x, cudaStream_t stream) {
     configured = true;
   }
   CUtensorMap mq, mk, mv;
-  const int64_t S_kv_map = x.S_kv > 0 ? x.S_kv : 1;
-  if (!encode_bf16_map(&mq, x.q, x.layout, x.B, x.Hq, x.S_q, D, 64, kBM,
+  // packed sequences: [T, H, D] tensors, one batch of T rows
+  const bool packed = x.varlen != nullptr;
+  const int64_t map_B = packed ? 1 : x.B;
+  const int64_t S_q_map = packed ? std::max<int64_t>(x.T_q, 1) : x.S_q;
+  const int64_t S_kv_map = packed ? std::max<int64_t>(x.T_kv, 1) : (x.S_kv > 0 ? x.S_kv : 1);
+  if (!encode_bf16_map(&mq, x.q, x.layout, map_B, x.Hq, S_q_map, D, 64, kBM,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_bf16_map(&mk, x.k, x.layout, x.B, x.Hkv, S_kv_map, D, 64, kBN,
+      !encode_bf16_map(&mk, x.k, x.layout, map_B, x.Hkv, S_kv_map, D, 64, kBN,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_bf16_map(&mv, x.v, x.layout, x.B, x.Hkv, S_kv_map, D, 64, kBN,
+      !encode_bf16_map(&mv, x.v, x.layout, map_B, x.Hkv, S_kv_map, D, 64, kBN,
                        CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   PrefillArgs pa;
@@ -721,6 +749,7 @@ cudaError_t launch_prefill_d(const PrefillLaunch& x, cudaStream_t stream) {
   pa.lse = x.lse;
   pa.tile_bits = x.tile_bits;
   pa.sched = x.sched;
+  pa.varlen = x.varlen;
   pa.status = x.status;
   pa.timeout_ns = x.timeout_ns;
   pa.B = x.B;

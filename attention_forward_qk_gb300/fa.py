@@ -136,6 +136,49 @@ def fa_forward(q, k, v, *, mask_mode=None, key_mask=None, actual_seq_lengths=Non
     return out, lse
 
 
+def fa_forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, *, mask_mode=None, scale=1.0,
+                      num_heads=None, num_kv_heads=None, out=None, lse=None, return_lse=True,
+                      workspace=None, stream=None):
+    """Prefill attention over packed variable-length sequences (TND): q, out
+    [T_q, Hq, D]; k, v [T_kv, Hkv, D]; cu_seqlens_* host sequences of B + 1
+    offsets. Returns (out, lse) with lse [T_q, Hq]."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n)
+    if q.dim() != 3 or k.dim() != 3 or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("q, k, v must be [T, H, D] with k and v alike")
+    cq = [int(x) for x in cu_seqlens_q]
+    ckv = [int(x) for x in cu_seqlens_kv]
+    if len(cq) != len(ckv) or len(cq) < 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_kv need B + 1 entries each")
+    B = len(cq) - 1
+    T_q, Hq, D = q.shape
+    T_kv, Hkv, Dk = k.shape
+    if Dk != D or cq[-1] != T_q or ckv[-1] != T_kv:
+        raise ValueError("tensor rows disagree with the offsets")
+    if num_heads is not None and num_heads != Hq:
+        raise ValueError("num_heads does not match q")
+    if out is None:
+        out = torch.empty_like(q)
+    _check_tensor(out, "out")
+    if lse is None and return_lse:
+        lse = torch.empty((T_q, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_tensor(lse, "lse", torch.float32)
+    max_q = max([b - a for a, b in zip(cq[:-1], cq[1:])] + [0])
+    max_kv = max([b - a for a, b in zip(ckv[:-1], ckv[1:])] + [0])
+    need = int(_lib.load().fa_forward_varlen_workspace_size(B, max_q, max_kv, Hq, Hkv, D))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    aq = (ctypes.c_int64 * (B + 1))(*cq)
+    akv = (ctypes.c_int64 * (B + 1))(*ckv)
+    st = _lib.load().fa_forward_varlen(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), aq, akv, MASK_MODES.get(mask_mode, mask_mode),
+        B, Hq, Hkv, D, float(scale), out.data_ptr(), lse.data_ptr() if lse is not None else None,
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    check(st, "fa_forward_varlen")
+    return out, lse
+
+
 def fa_forward_window(q, k, v, win_left, win_right, *, key_mask=None, actual_seq_lengths=None,
                       scale=1.0, layout="BNSD", num_heads=None, num_kv_heads=None, out=None,
                       lse=None, return_lse=True, workspace=None, stream=None):

@@ -116,6 +116,30 @@ fa_status fa_forward(const void* q, const void* k, const void* v, int mask_mode,
                      int64_t D, float scale, int layout, void* out, float* lse,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* Fused attention forward over packed variable-length sequences (the TND
+ * layout of FlashAttn guide §1.3 and §1.4: the tokens of all sequences laid
+ * end to end, cu_seqlens giving each sequence's start).
+ *   q, out   [T_q, num_heads, D], device bf16, T_q = cu_seqlens_q[B]
+ *   k, v     [T_kv, num_kv_heads, D], device bf16, T_kv = cu_seqlens_kv[B]
+ *   cu_seqlens_q, cu_seqlens_kv  HOST int64 [B + 1], 0 first, non-decreasing;
+ *            sequence b is q rows [cu_q[b], cu_q[b+1]) against k/v rows
+ *            [cu_kv[b], cu_kv[b+1]); a sequence with no keys gives out 0,
+ *            lse +inf; one with no queries writes nothing
+ *   mask_mode  FA_MASK_NONE or FA_MASK_CAUSAL (causal needs equal q and kv
+ *            lengths per sequence, top-left aligned within it)
+ *   lse      NULL or device fp32 [T_q, num_heads]
+ *   workspace  >= fa_forward_varlen_workspace_size(B, longest q sequence,
+ *            longest kv sequence, ...) bytes, 256-byte aligned
+ * Errors: bad offsets or lengths -> FA_ERR_PARAM_INVALID; NULL offsets ->
+ * FA_ERR_NULLPTR; otherwise those of fa_forward. */
+size_t fa_forward_varlen_workspace_size(int64_t B, int64_t max_seqlen_q, int64_t max_seqlen_kv,
+                                        int64_t num_heads, int64_t num_kv_heads, int64_t D);
+fa_status fa_forward_varlen(const void* q, const void* k, const void* v,
+                            const int64_t* cu_seqlens_q, const int64_t* cu_seqlens_kv,
+                            int mask_mode, int64_t B, int64_t num_heads, int64_t num_kv_heads,
+                            int64_t D, float scale, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
 /* Fused attention forward with a sliding window (FlashAttn guide §1.5,
  * mask_mode 4: a band of win_left tokens before and win_right tokens after
  * each query). Query row i keeps key j iff

@@ -276,3 +276,34 @@ def test_decode_paged_rejects_before_any_cuda_call(lib, kw, expect):
 
 def test_decode_paged_zero_batch_is_noop(lib):
     assert _dec_paged(lib, B=0, lens=[], bt=None) == _lib.FA_OK
+
+
+def _fwd_varlen(lib, cq, ckv, **kw):
+    args = dict(q=P, k=P, v=P, mask=0, Hq=4, Hkv=2, D=128, scale=0.1, out=P, lse=None, ws=WS,
+                ws_bytes=1 << 22, stream=None)
+    args.update(kw)
+    B = len(cq) - 1
+    aq = (ctypes.c_int64 * len(cq))(*cq) if cq is not None else None
+    akv = (ctypes.c_int64 * len(ckv))(*ckv) if ckv is not None else None
+    return lib.fa_forward_varlen(args["q"], args["k"], args["v"], aq, akv, args["mask"],
+                                 args.get("B", B), args["Hq"], args["Hkv"], args["D"],
+                                 args["scale"], args["out"], args["lse"], args["ws"],
+                                 args["ws_bytes"], args["stream"])
+
+
+@pytest.mark.parametrize("cq,ckv,kw,expect", [
+    ([1, 5], [0, 5], {}, _lib.FA_ERR_PARAM_INVALID),          # must start at 0
+    ([0, 5, 3], [0, 5, 9], {}, _lib.FA_ERR_PARAM_INVALID),    # decreasing
+    ([0, 5, 9], [0, 5, 8], dict(mask=3), _lib.FA_ERR_PARAM_INVALID),  # causal, unequal lengths
+    ([0, 5], [0, 5], dict(mask=4), _lib.FA_ERR_PARAM_INVALID),
+    ([0, 5], [0, 5], dict(q=None), _lib.FA_ERR_NULLPTR),
+    ([0, 5], [0, 5], dict(D=96), _lib.FA_ERR_UNSUPPORTED),
+    ([0, 5], [0, 5], dict(ws_bytes=16), _lib.FA_ERR_WORKSPACE_TOO_SMALL),
+])
+def test_forward_varlen_rejects_before_any_cuda_call(lib, cq, ckv, kw, expect):
+    assert _fwd_varlen(lib, cq, ckv, **kw) == expect
+
+
+def test_forward_varlen_null_offsets(lib):
+    assert lib.fa_forward_varlen(P, P, P, None, None, 0, 1, 4, 2, 128, 0.1, P, None, WS,
+                                 1 << 22, None) == _lib.FA_ERR_NULLPTR
