@@ -90,6 +90,11 @@ def work_units(w, lens=None, pads=None):
         qo = 2 * 2 * w.B * w.Hq * w.D + 4 * w.B * w.Hq
         return {"step": kv + qo, "main": kv + 2 * w.B * w.Hq * w.D}
     S = w.S_q
+    if w.packed:
+        # lens: the packed sequences' lengths (q = kv)
+        pairs = w.Hq * sum(L * (L + 1) // 2 if w.causal else L * L for L in lens)
+        f = 4 * w.D * pairs
+        return {"step": f, "main": f}
     if w.window is not None:
         wl, wr = w.window
         per_row = [min(S, i + wr + 1 if wr >= 0 else S) - max(0, i - wl if wl >= 0 else 0)
@@ -188,16 +193,22 @@ class Runner:
         from attention_forward_qk_gb300 import fa as F
         self.w, self.dev, self.F = w, dev, F
         self.kind = w.kind
-        x = workloads.make(w) if host_copy else None  # same seeded inputs as the parity tests
-        if w.kind == "decode":
+        # same seeded inputs as the parity tests
+        x = workloads.make(w) if (host_copy or w.packed) else None
+        self.cu = None
+        if w.packed:
+            self.lens = x["lengths"]
+            self.cu = x["cu_seqlens"]
+            self.pads = None
+        elif w.kind == "decode":
             self.lens = x["lengths"] if x else decode_lengths(w)
             self.pads = None
         else:
             self.lens = None
             self.pads = x["pads"] if x else prefill_pads(w)
         self.units = work_units(w, self.lens, self.pads)
-        if host_copy:
-            self.host = {k: x[k].pin_memory() for k in ("q", "k", "v")}
+        if host_copy or w.packed:
+            self.host = {k: (x[k].pin_memory() if host_copy else x[k]) for k in ("q", "k", "v")}
             if x.get("key_mask") is not None:
                 self.host["key_mask"] = x["key_mask"].pin_memory()
             self.q = self.host["q"].to(dev)
@@ -240,8 +251,12 @@ class Runner:
                 self.host["k"] = kp.cpu().pin_memory()
                 self.host["v"] = vp.cpu().pin_memory()
         self.out = torch.empty_like(self.q)
-        self.lse = torch.empty((w.B, w.Hq, w.S_q), dtype=torch.float32, device=dev)
-        if w.kind == "decode":
+        lse_shape = (self.q.shape[0], w.Hq) if w.packed else (w.B, w.Hq, w.S_q)
+        self.lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+        if w.packed:
+            n = F._lib.load().fa_forward_varlen_workspace_size(w.B, max(self.lens), max(self.lens),
+                                                               w.Hq, w.Hkv, w.D)
+        elif w.kind == "decode":
             n = F.fa_decode_workspace_size(w.B, w.S_kv, w.Hq, w.Hkv, w.D, 0)
         else:
             n = F.fa_forward_workspace_size(w.B, w.S_q, w.S_kv, w.Hq, w.Hkv, w.D)
@@ -249,7 +264,11 @@ class Runner:
 
     def step(self):
         w, F = self.w, self.F
-        if self.kind == "decode" and self.table is not None:
+        if w.packed:
+            F.fa_forward_varlen(self.q, self.k, self.v, self.cu, self.cu,
+                                mask_mode="causal" if w.causal else None, scale=w.scale,
+                                out=self.out, lse=self.lse, workspace=self.ws)
+        elif self.kind == "decode" and self.table is not None:
             F.fa_decode_paged(self.q, self.k, self.v, self.table, w.block_size, self.lens,
                               scale=w.scale, out=self.out, lse=self.lse, workspace=self.ws)
         elif self.kind == "decode":
@@ -389,6 +408,23 @@ def cpu_baseline(w, budget_s=12.0):
     rng = np.random.default_rng(0)
     pads = x.get("pads")
     rows_done = 0
+    if w.packed:
+        cu, lens = x["cu_seqlens"], x["lengths"]
+        while time.perf_counter() - t0 < budget_s:
+            b = passes % w.B
+            L = lens[b]
+            rows = sorted(rng.choice(L, size=min(16, L), replace=False).tolist())
+            sl = slice(cu[b], cu[b + 1])
+            oracle.attention(x["q"][sl][None], x["k"][sl][None], x["v"][sl][None], scale=w.scale,
+                             layout="BSND", causal=w.causal, rows=rows)
+            done_units += sum(4 * w.D * (i + 1 if w.causal else L) * w.Hq for i in rows)
+            rows_done += len(rows)
+            passes += 1
+        el = time.perf_counter() - t0
+        return {"value": done_units / el / 1e12, "unit": "TFLOP/s", "cores": cores,
+                "kind": "oracle",
+                "sample": f"{rows_done} query rows x {w.Hq} heads in {passes} passes, numpy fp64, "
+                          f"{el:.1f} s"}
     while time.perf_counter() - t0 < budget_s:
         rows = sorted(rng.choice(w.S_q, size=min(16, w.S_q), replace=False).tolist())
         bsl = slice(passes % w.B, passes % w.B + 1)
@@ -468,7 +504,7 @@ def run_gpu(args):
     others = {}
     if not args.only:
         for name in ("long_decode", "causal_prefill", "gqa_masked_prefill", "tiny_prefill",
-                     "window_prefill", "paged_decode", "gqa_decode"):
+                     "window_prefill", "varlen_prefill", "paged_decode", "gqa_decode"):
             if name == args.workload:
                 continue
             wo = workloads.WORKLOADS[name]

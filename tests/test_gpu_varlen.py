@@ -77,3 +77,29 @@ def test_varlen_equal_lengths_match_padded_call_bitwise(cuda_device):
     torch.cuda.synchronize()
     assert torch.equal(a[0], b[0].view(B * S, Hq, D))
     assert torch.equal(a[1], b[1].permute(0, 2, 1).reshape(B * S, Hq))
+
+
+def test_varlen_workload_sampled_rows(cuda_device):
+    """The bench's packed workload at full size (16 sequences of 512..8192
+    tokens): every sequence checked on sampled rows against the oracle."""
+    import workloads
+    w = workloads.WORKLOADS["varlen_prefill"]
+    x = workloads.make(w)
+    cu = x["cu_seqlens"]
+    out, lse = F.fa_forward_varlen(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), cu, cu,
+                                   mask_mode="causal", scale=w.scale)
+    torch.cuda.synchronize()
+    o = out.cpu()
+    l = lse.cpu()
+    g = np.random.default_rng(2)
+    for b in range(w.B):
+        L = cu[b + 1] - cu[b]
+        rows = sorted(set([0, L - 1] + g.choice(L, 6, replace=False).tolist()))
+        sl = slice(cu[b], cu[b + 1])
+        ro, rl = oracle.attention(x["q"][sl][None], x["k"][sl][None], x["v"][sl][None],
+                                  scale=w.scale, layout="BSND", causal=True, rows=rows)
+        got_o = o[sl][rows].double().numpy()
+        got_l = l[sl][rows].double().numpy()
+        err = np.abs(got_o - ro[0])
+        assert err.max() <= OUT_MAX and err.mean() <= OUT_MEAN
+        assert np.abs(got_l - rl[0].T).max() <= LSE_MAX

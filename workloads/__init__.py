@@ -59,6 +59,9 @@ class Workload:
     window: tuple | None = None
     # decode: paged cache of blocks of this many rows (PA_BBND), or None
     block_size: int | None = None
+    # prefill: B packed sequences (TND) of lengths drawn uniform in
+    # [len_lo, len_hi] (equal q and kv lengths), S_q = S_kv = len_hi
+    packed: bool = False
     note: str = field(default="", compare=False)
 
     @property
@@ -94,6 +97,12 @@ WORKLOADS: dict[str, Workload] = {
         "window_prefill", "prefill", B=2, Hq=32, Hkv=8, S_q=8192, S_kv=8192, D=128,
         layout="BNSD", seed=106, window=(1023, 0),
         note="B=2 Hq=32 Hkv=8 S=8192 D=128 BNSD, window of 1024 keys (1023 before, 0 after)"),
+    # Beyond the five: packed variable-length causal prefill (FlashAttn guide
+    # §1.3 TND with cu_seqlens), 16 sequences of 512..8192 tokens.
+    "varlen_prefill": Workload(
+        "varlen_prefill", "prefill", B=16, Hq=32, Hkv=8, S_q=8192, S_kv=8192, D=128,
+        layout="TND", causal=True, seed=108, len_lo=512, len_hi=8192, packed=True,
+        note="16 packed sequences (TND), lengths ~U[512,8192], Hq=32 Hkv=8 D=128, causal"),
     # Beyond the five: the GQA decode workload with its cache paged (FlashAttn
     # guide §1.2, PA_BBND, 128-row blocks in shuffled order).
     "paged_decode": Workload(
@@ -185,10 +194,28 @@ def make_decode(B, Hq, Hkv, S_kv, D, layout="BNSD", seed=0, *,
             "layout": layout}
 
 
+def make_packed(B, Hq, Hkv, D, seed, *, len_lo, len_hi):
+    """Packed (TND) prefill inputs: sequence lengths drawn first, then q, k,
+    v [T, H, D] from randn cast to bf16; cu_seqlens (equal for q and kv)."""
+    g = torch.Generator().manual_seed(seed)
+    lens = [int(x) for x in torch.randint(len_lo, len_hi + 1, (B,), generator=g)]
+    cu = [0]
+    for L in lens:
+        cu.append(cu[-1] + L)
+    T = cu[-1]
+    q = torch.randn(T, Hq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(T, Hkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(T, Hkv, D, generator=g).to(torch.bfloat16)
+    return {"q": q, "k": k, "v": v, "cu_seqlens": cu, "lengths": lens, "layout": "TND",
+            "key_mask": None}
+
+
 def make(w: Workload | str):
     """Inputs of a named workload (see ``WORKLOADS``)."""
     if isinstance(w, str):
         w = WORKLOADS[w]
+    if w.packed:
+        return make_packed(w.B, w.Hq, w.Hkv, w.D, w.seed, len_lo=w.len_lo, len_hi=w.len_hi)
     if w.kind == "prefill":
         return make_prefill(w.B, w.Hq, w.Hkv, w.S_q, w.S_kv, w.D, w.layout, w.seed,
                             max_pad=w.max_pad)
