@@ -38,7 +38,7 @@ int64_t chunk_for_splits(int64_t S_kv_max, int num_splits) {
 }
 
 struct DecodeWs {
-  size_t prefix, real_lens, part_lse, part_o, total;
+  size_t prefix, real_lens, counters, part_lse, part_o, total;
 };
 
 // [status | pad][length prefix sums, large batches only][partial lse][partial o]
@@ -49,6 +49,8 @@ DecodeWs decode_ws(int64_t B, int64_t Hq, int64_t D, int64_t max_slots) {
   off += align_up(sizeof(int64_t) * (B + 1));
   w.real_lens = off;  // paged cache only
   off += align_up(sizeof(int32_t) * B);
+  w.counters = off;  // per (batch, KV head, head group): pieces finished
+  off += align_up(sizeof(uint32_t) * B * Hq);
   w.part_lse = off;
   off += align_up(sizeof(float) * B * Hq * max_slots);
   w.part_o = off;
@@ -613,8 +615,9 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
                                     cudaMemcpyHostToDevice, s) != cudaSuccess)
     return FA_ERR_RUNTIME;
   const int64_t total = KH * prefix[B];
-  // the real lengths of a paged cache go to the workspace
-  if (pg != nullptr) {
+  // the real lengths of a paged cache: in the launch parameters with the
+  // prefix sums, else in the workspace
+  if (pg != nullptr && !in_params) {
     std::vector<int> real(B);
     for (int64_t b = 0; b < B; ++b) real[b] = static_cast<int>(lens[b]);
     if (cudaMemcpyAsync(wsb + ws.real_lens, real.data(), B * sizeof(int), cudaMemcpyHostToDevice,
@@ -623,6 +626,10 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
   }
   // the main kernel clears the status word when it starts; without one, clear it here
   if (total == 0 && cudaMemsetAsync(wsb, 0, sizeof(uint32_t), s) != cudaSuccess)
+    return FA_ERR_RUNTIME;
+  // the piece counters of the units cut into several pieces start at zero
+  if (total > 0 && max_slots > 1 &&
+      cudaMemsetAsync(wsb + ws.counters, 0, sizeof(uint32_t) * B * KH, s) != cudaSuccess)
     return FA_ERR_RUNTIME;
 
   DecodeLaunch x;
@@ -640,16 +647,19 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
   x.total = total;
   x.rows_per_cta = rc;
   x.max_slots = static_cast<int>(slots);
-  x.needs_merge = has_empty || max_slots > 1;
   x.prefix_host = prefix;
   x.prefix_dev = in_params ? nullptr : reinterpret_cast<const long long*>(wsb + ws.prefix);
   x.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
   x.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
+  x.counters = reinterpret_cast<unsigned int*>(wsb + ws.counters);
+  x.has_empty = has_empty;
   x.block_table = pg != nullptr ? pg->block_table : nullptr;
   x.max_blocks = pg != nullptr ? static_cast<int>(pg->max_blocks) : 0;
   x.num_blocks = pg != nullptr ? static_cast<int>(pg->num_blocks) : 0;
   x.block_size = pg != nullptr ? static_cast<int>(pg->block_size) : 0;
-  x.lens_dev = pg != nullptr ? reinterpret_cast<const int*>(wsb + ws.real_lens) : nullptr;
+  x.lens_dev = pg != nullptr && !in_params ? reinterpret_cast<const int*>(wsb + ws.real_lens)
+                                           : nullptr;
+  x.lens_host = pg != nullptr ? lens : nullptr;
   x.out = out;
   x.lse = lse;
   x.status = reinterpret_cast<uint32_t*>(wsb);

@@ -13,26 +13,27 @@
 // rows (112-row stages; a piece's last, partial stage with 16-row boxes)
 // through one 168 KB shared-memory ring with TMA tensor loads, without a
 // break between pieces; q arrives with a piece's first stage. Seven consumer
-// warps compute q.k with 128-bit shared loads, packed f32x2 FMAs and
-// butterfly shuffles over the 8 lanes that share a row (the G query heads of
-// a GQA group reuse each K/V row), keep an online softmax per head (running
-// max m and sum l, exp2 domain) and accumulate p*v. This is the FlashDecoding
+// warps compute q.k with 128-bit shared loads, packed f32x2 FMAs and a
+// butterfly over the 8 lanes that share a row (the G query heads of a GQA
+// group reuse each K/V row), keep an online softmax per head (running max m
+// and sum l, exp2 domain) and accumulate p*v. This is the FlashDecoding
 // tutorial's stage 1 (§3.2) with the scale and the length mask applied.
 // At the end of a piece every warp parks its (m, l, o) in a double-buffered
-// scratch slot and goes on; the last warp to arrive combines the seven
-// states into the piece's normalised partial o/l and log-sum-exp (or, when
-// the piece is the whole unit, into the final output).
+// scratch slot; once all seven have, each combines a slice of the piece's
+// normalised partial o/l and log-sum-exp (or, when the piece is the whole
+// unit, of the final output).
 //
-// Stage 2 (decode_merge_kernel), launched with programmatic dependent launch
-// so that it is resident as soon as stage 1 drains, merges the pieces of
-// every (batch, query head) by their log-sum-exp with the largest value
-// factored out, in piece order:
+// Stage 2 (in the same kernel): a unit cut into several pieces is counted in
+// a per-unit counter (cleared before the launch) when a CTA finishes; the
+// CTA that completes the count merges the unit's pieces for every query head
+// by their log-sum-exp with the largest value factored out, in piece order:
 //   M = max_c lse_c, w_c = 2^(lse_c - M), out = sum_c w_c o_c / sum_c w_c,
 //   lse = M + log2(sum_c w_c)  (reported as natural log)
 // which is aclnnIncreFlashAttention guide §8.3's combine() and the FlashAttn
 // guide §10 formula written for normalised partials (FlashDecoding tutorial
-// §3.3). A sequence of length 0 gets out = 0, lse = +inf (FlashAttn guide
-// §1.7).
+// §3.3). No CTA waits for another: the merge is a stream-K fixup by whichever
+// finishes last. A sequence of length 0 gets out = 0, lse = +inf (FlashAttn
+// guide §1.7).
 //
 // Rows at or past a batch's length are never used by any arithmetic (they
 // may land in shared memory with the rest of a box and are skipped), so
@@ -70,6 +71,8 @@ struct DecCfg {
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
   static constexpr int NST = kRingBytes / STAGE_BYTES;  // 3 (D = 128) or 6 (D = 64)
   static constexpr int NP = 4 * NCH;                // fp32 pairs per lane per head
+  static constexpr int LG = G >= 8 ? 3 : G >= 4 ? 2 : G >= 2 ? 1 : 0;  // log2(G)
+  static constexpr int SHIFT = 3 - LG;              // head of lane `sub`: sub >> SHIFT
   // one scratch buffer: m[warps][G] and l[warps][G], each padded to a
   // multiple of 4 floats so that o[warps][G][D] and the next buffer stay
   // 16-byte aligned for the float4 accesses
@@ -96,6 +99,8 @@ struct DecodeArgs {
   const uint8_t* key_mask;
   float* part_o;     // [B][Hq][max_slots][D]
   float* part_lse;   // [B][Hq][max_slots], log2 domain
+  unsigned int* counters;  // [B * KH] pieces finished per unit (zero at launch)
+  int has_empty;           // some sequence has length 0
   __nv_bfloat16* out;
   float* lse;
   uint32_t* status;
@@ -108,19 +113,36 @@ struct DecodeArgs {
   // real lengths (the work space holds them rounded up to 16 rows)
   const int32_t* block_table;
   int max_blocks, block_size;
-  const int* real_len;     // [B] in the workspace (paged only)
+  const int* real_len;     // [B] in the workspace (paged, large batches only)
+  // paged, batches that travel in the parameters: how far each length was
+  // rounded up (the real length is the work-space length minus this)
+  unsigned char pad16[kDecodeParamBatches];
   Prefix prefix;           // prefix[b] = sum of lengths of batches < b (work space)
 };
 
 // Largest b with KH * prefix[b] <= r (the batch whose rows hold r; batches
-// of length 0 own no row and are passed over).
+// of length 0 own no row and are passed over). Small batches count the
+// prefix entries at or below r with independent loads, larger ones bisect.
 __device__ __forceinline__ int find_batch(const Prefix& p, int B, long long KH, long long r) {
+  if (B <= 64) {
+    int b = 0;
+#pragma unroll 8
+    for (int i = 1; i < B; ++i) b += (KH * p[i] <= r) ? 1 : 0;
+    return b;
+  }
   int lo = 0, hi = B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (KH * p[mid] <= r) lo = mid; else hi = mid - 1;
   }
   return lo;
+}
+
+// n / d for non-negative n and positive d, in 32 bits when both fit.
+__device__ __forceinline__ long long div_nn(long long n, long long d) {
+  if (((n | d) >> 32) == 0)
+    return static_cast<long long>(static_cast<uint32_t>(n) / static_cast<uint32_t>(d));
+  return n / d;
 }
 
 // Per-slot header the producer writes before the slot's loads, so consumers
@@ -131,6 +153,66 @@ struct SlotHeader {
   int nstage;  // stages of the piece
   int b, kh, row0, rows, slot, nsp;
   int vend;    // rows of the piece that hold keys (< rows only past a paged length)
+};
+
+// Merge the nsp normalised partials of one (batch, query head) row into the
+// output (one warp): all lse and o loads of up to 8 pieces are in flight
+// before any is used, the largest lse is factored out.
+template <int D>
+__device__ __forceinline__ void merge_row(const DecodeArgs& a, size_t row, int nsp, int lane) {
+  constexpr int EPL = D / 32;  // output elements per lane
+  const float* pl = a.part_lse + row * a.max_slots;
+  const float* po = a.part_o + row * a.max_slots * D + lane * EPL;
+  float M = -INFINITY, W = 0.f, acc[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+  for (int k0 = 0; k0 < nsp; k0 += 8) {
+    float lk[8], v[8][EPL];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const bool in = k0 + u < nsp;
+      lk[u] = in ? __ldcg(pl + k0 + u) : -INFINITY;
+      if constexpr (EPL == 4) {
+        const float4 t = in ? __ldcg(reinterpret_cast<const float4*>(po + static_cast<size_t>(k0 + u) * D))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+      } else {
+        const float2 t = in ? __ldcg(reinterpret_cast<const float2*>(po + static_cast<size_t>(k0 + u) * D))
+                            : make_float2(0.f, 0.f);
+        v[u][0] = t.x; v[u][1] = t.y;
+      }
+    }
+    float mb = M;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) mb = fmaxf(mb, lk[u]);
+    if (mb == -INFINITY) continue;  // only empty pieces so far
+    const float sc = ex2(M - mb);   // rescale what was summed under the old maximum (0 at first)
+    W *= sc;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] *= sc;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float wk = ex2(lk[u] - mb);  // empty or absent piece: 0
+      W += wk;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wk, v[u][e], acc[e]);
+    }
+    M = mb;
+  }
+  const bool invalid = (M == -INFINITY);
+  const float inv = invalid ? 0.f : 1.f / W;
+  __nv_bfloat16* dst = a.out + row * D + lane * EPL;
+  if constexpr (EPL == 4) {
+    *reinterpret_cast<uint2*>(dst) =
+        make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  }
+  if (lane == 0 && a.lse != nullptr) a.lse[row] = invalid ? INFINITY : (M + log2f(W)) * kLn2;
+}
+
+struct Pending {
+  int unit, nsp, b, kh;
 };
 
 template <int D, int G>
@@ -148,10 +230,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   float* scratch = reinterpret_cast<float*>(smem + kRingBytes);  // 2 buffers
   unsigned char* qbuf = smem + kRingBytes + 2 * C::SCRATCH_FLOATS * 4;
   uint64_t* bars = reinterpret_cast<uint64_t*>(qbuf + kMaxStages * kQBytes);
-  // bars: full[kMaxStages], empty[kMaxStages], scratch_free[2]
-  SlotHeader* hdr = reinterpret_cast<SlotHeader*>(bars + 2 * kMaxStages + 2);
-  int* arrivals = reinterpret_cast<int*>(hdr + kMaxStages);  // [2] warps done per buffer
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(arrivals + 2);
+  // bars: full[kMaxStages], empty[kMaxStages], scratch free[2], scratch parked[2]
+  SlotHeader* hdr = reinterpret_cast<SlotHeader*>(bars + 2 * kMaxStages + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(hdr + kMaxStages);
+  // split pieces of this CTA (at most its first and its last): counted at the end
+  int* n_pending = const_cast<int*>(abort_flag) + 1;
+  Pending* pending = reinterpret_cast<Pending*>(n_pending + 3);  // [2]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -162,67 +246,79 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = smem_u32(bars + kMaxStages);
   const uint32_t sfree0 = smem_u32(bars + 2 * kMaxStages);
+  const uint32_t parked0 = smem_u32(bars + 2 * kMaxStages + 2);
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, kDecWarps);
     }
-    mbar_init(sfree0, 1);
-    mbar_init(sfree0 + 8, 1);
-    arrivals[0] = 0;
-    arrivals[1] = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(sfree0 + 8 * i, kDecWarps);
+      mbar_init(parked0 + 8 * i, kDecWarps);
+    }
     *abort_flag = 0;
+    *n_pending = 0;
     fence_mbar_init();
   }
   __syncthreads();
-  // launched with programmatic dependent launch: wait until the work that
-  // precedes this kernel on the stream (which may produce q, K, V) is done
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // a timeout needs timeout_ns to fire, long after this clear
-  if (tid == 0 && blockIdx.x == 0) *a.status = 0;
-  // the merge kernel may be scheduled as soon as SMs free up; it waits for
-  // this grid's completion before it reads any partial
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == kDecWarps) {
     // ================================================================ producer
+    const long long Rc = a.rows_per_cta;
+    long long r = static_cast<long long>(blockIdx.x) * Rc;
+    const long long r1 = min(r + Rc, a.total);
+    // the next piece of this CTA's range [r, r1): its unit, rows and stages
+    auto plan = [&](int piece, SlotHeader& h, int& kvh, int& hg) {
+      h = SlotHeader{-1, 0, 1, 0, 0, 0, 0, 0, 0, 0};
+      if (r >= r1) return;
+      const int b = find_batch(a.prefix, a.B, KH, r);
+      const long long base = KH * a.prefix[b];
+      const long long L = a.prefix[b + 1] - a.prefix[b];
+      const long long kh = div_nn(r - base, L);
+      const long long u0 = base + kh * L;  // the unit's first row in the work space
+      const long long u1 = u0 + L;
+      const long long rows = min(u1, r1) - r;
+      h.piece = piece;
+      h.b = b;
+      h.kh = static_cast<int>(kh);
+      h.row0 = static_cast<int>(r - u0);
+      h.rows = static_cast<int>(rows);
+      const long long c0 = div_nn(u0, Rc);  // the CTA holding the unit's first row
+      h.slot = static_cast<int>(blockIdx.x - c0);
+      h.nsp = static_cast<int>(div_nn(u1 - 1, Rc) - c0 + 1);
+      h.nstage = static_cast<int>((rows + C::R - 1) / C::R);
+      h.vend = h.rows;
+      if (a.block_table != nullptr) {
+        const long long real = a.real_len != nullptr ? __ldg(a.real_len + b) : L - a.pad16[b];
+        h.vend = static_cast<int>(max(0ll, min(static_cast<long long>(h.rows), real - h.row0)));
+      }
+      kvh = h.kh / a.head_groups;
+      hg = h.kh % a.head_groups;
+      r += rows;
+    };
+    SlotHeader h{};
+    int kvh = 0, hg = 0;
+    // the first piece needs only the launch parameters (unless the prefix
+    // sums or the paged lengths sit in the workspace): plan it while the
+    // work before this kernel may still be running
+    const bool early = a.prefix.global == nullptr && a.real_len == nullptr;
     if (lane == 0) {
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
       tma_prefetch_map(&tm_k16);
       tma_prefetch_map(&tm_v16);
-      const long long Rc = a.rows_per_cta;
-      long long r = static_cast<long long>(blockIdx.x) * Rc;
-      const long long r1 = min(r + Rc, a.total);
+      if (early) plan(0, h, kvh, hg);
+    }
+    // launched with programmatic dependent launch: wait until the work that
+    // precedes this kernel on the stream (which may produce q, K, V) is done
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (lane == 0) {
       int st = 0;  // stages issued by this CTA
       bool ok = true;
       for (int piece = 0; ok; ++piece) {
-        const bool done = r >= r1;
-        SlotHeader h{-1, 0, 1, 0, 0, 0, 0, 0, 0, 0};
-        int kvh = 0, hg = 0;
-        if (!done) {
-          const int b = find_batch(a.prefix, a.B, KH, r);
-          const long long base = KH * a.prefix[b];
-          const long long L = a.prefix[b + 1] - a.prefix[b];
-          const long long kh = (r - base) / L;
-          const long long u0 = base + kh * L;  // the unit's first row in the work space
-          const long long u1 = u0 + L;
-          const long long rows = min(u1, r1) - r;
-          h.piece = piece;
-          h.b = b;
-          h.kh = static_cast<int>(kh);
-          h.row0 = static_cast<int>(r - u0);
-          h.rows = static_cast<int>(rows);
-          h.slot = static_cast<int>(blockIdx.x - u0 / Rc);
-          h.nsp = static_cast<int>((u1 - 1) / Rc - u0 / Rc + 1);
-          h.nstage = static_cast<int>((rows + C::R - 1) / C::R);
-          h.vend = h.rows;
-          if (a.block_table != nullptr)
-            h.vend = max(0, min(h.rows, __ldg(a.real_len + b) - h.row0));
-          kvh = h.kh / a.head_groups;
-          hg = h.kh % a.head_groups;
-          r += rows;
-        }
+        if (piece > 0 || !early) plan(piece, h, kvh, hg);
+        const bool done = h.piece < 0;
         for (int s = 0; s < h.nstage; ++s, ++st) {
           const int slot = st % NST;
           const int use = st / NST;
@@ -288,12 +384,39 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
     }
   } else {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // a timeout needs timeout_ns to fire, long after this clear
+    if (tid == 0 && blockIdx.x == 0) *a.status = 0;
+    // work queued after this kernel may be scheduled as soon as SMs free up
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (a.has_empty) {
+      // sequences of length 0: out = 0, lse = +inf; one thread per row
+      for (int row = static_cast<int>(blockIdx.x) * kDecWarps * 32 + tid; row < a.B * a.Hq;
+           row += static_cast<int>(gridDim.x) * kDecWarps * 32) {
+        const int b = row / a.Hq;
+        if (a.prefix[b + 1] != a.prefix[b]) continue;
+        uint4* dst = reinterpret_cast<uint4*>(a.out + static_cast<size_t>(row) * D);
+#pragma unroll
+        for (int i = 0; i < D * 2 / 16; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (a.lse != nullptr) a.lse[row] = INFINITY;
+      }
+    }
     // ================================================================ consumers
-    const int sub = lane % C::LPR;  // this lane owns 16-byte chunks sub, sub+8 of a row
-    const int rg = lane / C::LPR;   // row group within a warp step
-    float m[G], l[G];
+    // Lane layout: the LPR = 8 lanes of a row group share one K/V row (lane
+    // `sub` owns its 16-byte chunks sub, sub+8). Every lane holds the q and o
+    // of all G heads in the order j -> head j ^ x, x = sub >> SHIFT: with that
+    // order the butterfly over the 8 lanes halves the heads still carried at
+    // each of its first log2(G) levels, so that a lane ends with the full dot
+    // product of one head, head x (the lanes sub with equal x hold the same
+    // one), in log2(8) levels of G - 1 + (3 - log2 G) shuffles instead of 3G.
+    // The softmax of a row group runs per lane for head x; p and the
+    // rescale factor of the other heads come back by G - 1 shuffles.
+    const int sub = lane % C::LPR;
+    const int rg = lane / C::LPR;  // row group within a warp step
+    const int x = sub >> C::SHIFT;
+    float m = -INFINITY, l = 0.f;  // head x of this row group
     uint64_t o[G][NP];
-    uint64_t qp[G][NP];  // q * scale * log2(e), as fp32 pairs
+    uint64_t qp[G][NP];  // q * scale * log2(e) of head j ^ x, as fp32 pairs
     int row_begin = 0, row_end = 0, piece_seq = -1;
     const uint8_t* mask_row = nullptr;
 
@@ -313,19 +436,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         row_end = hd.row0 + hd.vend;  // rows past a paged length hold no key
         mask_row = a.key_mask ? a.key_mask + static_cast<size_t>(hd.b) * a.S_kv : nullptr;
         const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(qbuf + slot * kQBytes);
+        m = -INFINITY;
+        l = 0.f;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          m[h] = -INFINITY;
-          l[h] = 0.f;
+        for (int j = 0; j < G; ++j) {
 #pragma unroll
-          for (int k = 0; k < NP; ++k) o[h][k] = 0ull;
+          for (int k = 0; k < NP; ++k) o[j][k] = 0ull;
 #pragma unroll
           for (int ch = 0; ch < C::NCH; ++ch) {
-            const uint4 u = *reinterpret_cast<const uint4*>(qs + h * D + (sub + 8 * ch) * 8);
+            const uint4 u = *reinterpret_cast<const uint4*>(qs + (j ^ x) * D + (sub + 8 * ch) * 8);
             const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              qp[h][ch * 4 + k] = pair_f32(bf16lo_to_f32(w4[k]) * a.scale_log2,
+              qp[j][ch * 4 + k] = pair_f32(bf16lo_to_f32(w4[k]) * a.scale_log2,
                                            bf16hi_to_f32(w4[k]) * a.scale_log2);
           }
         }
@@ -335,14 +458,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const __nv_bfloat16* Ks = reinterpret_cast<const __nv_bfloat16*>(smem + slot * C::STAGE_BYTES);
       const __nv_bfloat16* Vs = Ks + C::R * D;
       const int stage_row0 = row_begin + hd.stage * C::R;
-      float s[C::STEPS][G];
+      // every row of the stage holds a key: no per-row checks
+      const bool dense = mask_row == nullptr && stage_row0 + C::R <= row_end;
+      float s[C::STEPS];
       bool valid[C::STEPS];
 #pragma unroll
       for (int i = 0; i < C::STEPS; ++i) {
         const int r = warp * C::RPWS + i * C::RPW + rg;
         const int gr = stage_row0 + r;
-        bool ok = gr < row_end;
-        if (ok && mask_row != nullptr) ok = mask_row[gr] == 0;
+        bool ok = true;
+        if (!dense) {
+          ok = gr < row_end;
+          if (ok && mask_row != nullptr) ok = mask_row[gr] == 0;
+        }
         valid[i] = ok;
         uint64_t kp[NP];
 #pragma unroll
@@ -353,41 +481,67 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           kp[ch * 4 + 2] = bf16x2_pair(u.z);
           kp[ch * 4 + 3] = bf16x2_pair(u.w);
         }
+        float part[G];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          // two accumulator pairs: half the dependent-FMA chain length
-          uint64_t acc_a = 0ull, acc_b = 0ull;
+        for (int j = 0; j < G; ++j) {
+          // with few heads, two chains of FMAs keep the pipe busy
+          uint64_t acc = ffma2(qp[j][0], kp[0], 0ull);
+          if constexpr (G <= 2) {
+            uint64_t acc2 = ffma2(qp[j][1], kp[1], 0ull);
 #pragma unroll
-          for (int k = 0; k < NP; k += 2) {
-            acc_a = ffma2(qp[h][k], kp[k], acc_a);
-            acc_b = ffma2(qp[h][k + 1], kp[k + 1], acc_b);
+            for (int k = 2; k < NP; k += 2) {
+              acc = ffma2(qp[j][k], kp[k], acc);
+              acc2 = ffma2(qp[j][k + 1], kp[k + 1], acc2);
+            }
+            acc = fadd2(acc, acc2);
+          } else {
+#pragma unroll
+            for (int k = 1; k < NP; ++k) acc = ffma2(qp[j][k], kp[k], acc);
           }
-          const float2 a2 = unpair(acc_a);
-          const float2 b2 = unpair(acc_b);
-          float acc = (a2.x + a2.y) + (b2.x + b2.y);
-#pragma unroll
-          for (int off = C::LPR / 2; off > 0; off >>= 1)
-            acc += __shfl_xor_sync(0xffffffffu, acc, off);
-          s[i][h] = ok ? acc : -INFINITY;
+          const float2 a2 = unpair(acc);
+          part[j] = a2.x + a2.y;
         }
+        // butterfly: the first log2(G) levels keep the lower half of the
+        // heads still carried and receive the partner's sums of the same heads
+#pragma unroll
+        for (int lv = 0; lv < C::LG; ++lv) {
+          const int half = G >> (lv + 1);
+#pragma unroll
+          for (int j = 0; j < half; ++j)
+            part[j] += __shfl_xor_sync(0xffffffffu, part[j + half], (C::LPR / 2) >> lv);
+        }
+#pragma unroll
+        for (int lv = C::LG; lv < 3; ++lv)
+          part[0] += __shfl_xor_sync(0xffffffffu, part[0], (C::LPR / 2) >> lv);
+        s[i] = ok ? part[0] : -INFINITY;
       }
+      // online softmax of head x over this warp's rows of the stage: the
+      // running max is shared by the 4 row groups (so that their sums and
+      // accumulators add up without rescaling at the end of the piece)
+      float mx = s[0];
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float mx = s[0][h];
+      for (int i = 1; i < C::STEPS; ++i) mx = fmaxf(mx, s[i]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, C::LPR));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2 * C::LPR));
+      const float mn = fmaxf(m, mx);
+      const float m_use = (mn == -INFINITY) ? 0.f : mn;
+      const float alpha = ex2(m - m_use);  // 0 when m was -inf
+      m = mn;
+      float ps = 0.f;
 #pragma unroll
-        for (int i = 1; i < C::STEPS; ++i) mx = fmaxf(mx, s[i][h]);
-        const float mn = fmaxf(m[h], mx);
-        const float m_use = (mn == -INFINITY) ? 0.f : mn;
-        const float alpha = ex2(m[h] - m_use);  // 0 when m was -inf
-        m[h] = mn;
-        l[h] *= alpha;
-        const uint64_t a2 = pair_f32(alpha, alpha);
+      for (int i = 0; i < C::STEPS; ++i) {
+        s[i] = ex2(s[i] - m_use);  // -inf -> 0
+        ps += s[i];
+      }
+      l = fmaf(l, alpha, ps);
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        // some running maximum moved: rescale the accumulators of every head
 #pragma unroll
-        for (int k = 0; k < NP; ++k) o[h][k] = fmul2(o[h][k], a2);
+        for (int j = 0; j < G; ++j) {
+          const float aj = j == 0 ? alpha : __shfl_xor_sync(0xffffffffu, alpha, j << C::SHIFT);
+          const uint64_t a2 = pair_f32(aj, aj);
 #pragma unroll
-        for (int i = 0; i < C::STEPS; ++i) {
-          s[i][h] = ex2(s[i][h] - m_use);  // -inf -> 0
-          l[h] += s[i][h];
+          for (int k = 0; k < NP; ++k) o[j][k] = fmul2(o[j][k], a2);
         }
       }
 #pragma unroll
@@ -397,17 +551,18 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
         for (int ch = 0; ch < C::NCH; ++ch) {
           uint4 u = *reinterpret_cast<const uint4*>(Vs + r * D + (sub + 8 * ch) * 8);
-          if (!valid[i]) u = make_uint4(0u, 0u, 0u, 0u);  // stale rows never enter a product
+          if (!dense && !valid[i]) u = make_uint4(0u, 0u, 0u, 0u);  // stale rows never enter a product
           vp[ch * 4 + 0] = bf16x2_pair(u.x);
           vp[ch * 4 + 1] = bf16x2_pair(u.y);
           vp[ch * 4 + 2] = bf16x2_pair(u.z);
           vp[ch * 4 + 3] = bf16x2_pair(u.w);
         }
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const uint64_t p2 = pair_f32(s[i][h], s[i][h]);
+        for (int j = 0; j < G; ++j) {
+          const float pj = j == 0 ? s[i] : __shfl_xor_sync(0xffffffffu, s[i], j << C::SHIFT);
+          const uint64_t p2 = pair_f32(pj, pj);
 #pragma unroll
-          for (int k = 0; k < NP; ++k) o[h][k] = ffma2(p2, vp[k], o[h][k]);
+          for (int k = 0; k < NP; ++k) o[j][k] = ffma2(p2, vp[k], o[j][k]);
         }
       }
       __syncwarp();
@@ -415,33 +570,39 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       if (hd.stage != hd.nstage - 1) continue;
 
       // ================================================= end of the piece
-      // 1) merge the row groups of this warp (lanes with equal `sub`)
+      // 1) this warp's state: m is shared by the row groups, l and o add up.
+      //    The accumulators are halved twice across the row groups (lanes
+      //    xor 8, xor 16): a lane keeps one half and adds the partner's copy
+      //    of it, so that it ends with a quarter of them, summed over the warp.
+      l += __shfl_xor_sync(0xffffffffu, l, C::LPR);
+      l += __shfl_xor_sync(0xffffffffu, l, 2 * C::LPR);
+      constexpr int F = G * NP;  // accumulator pairs of a lane, slot-major
+      const bool b0 = (rg & 1) != 0, b1 = (rg & 2) != 0;
+      uint64_t h1[F / 2];
 #pragma unroll
-      for (int off = C::LPR; off < 32; off <<= 1) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float m2 = __shfl_xor_sync(0xffffffffu, m[h], off);
-          const float l2 = __shfl_xor_sync(0xffffffffu, l[h], off);
-          const float mn = fmaxf(m[h], m2);
-          const float m_use = (mn == -INFINITY) ? 0.f : mn;
-          const float a1 = ex2(m[h] - m_use);
-          const float a2 = ex2(m2 - m_use);
-          l[h] = l[h] * a1 + l2 * a2;
-#pragma unroll
-          for (int k = 0; k < NP; ++k) {
-            const float2 mine = unpair(o[h][k]);
-            const float ox = __shfl_xor_sync(0xffffffffu, mine.x, off);
-            const float oy = __shfl_xor_sync(0xffffffffu, mine.y, off);
-            o[h][k] = pair_f32(mine.x * a1 + ox * a2, mine.y * a1 + oy * a2);
-          }
-          m[h] = mn;
-        }
+      for (int f = 0; f < F / 2; ++f) {
+        const uint64_t lo = o[f / NP][f % NP], hi = o[(f + F / 2) / NP][(f + F / 2) % NP];
+        const uint64_t keep = b0 ? hi : lo, send = b0 ? lo : hi;
+        const float2 sp = unpair(send);
+        const float rx = __shfl_xor_sync(0xffffffffu, sp.x, C::LPR);
+        const float ry = __shfl_xor_sync(0xffffffffu, sp.y, C::LPR);
+        h1[f] = fadd2(keep, pair_f32(rx, ry));
       }
-      // 2) park this warp's state in scratch buffer (piece_seq & 1); wait
-      //    until the combiner of the piece two back has released it
+      uint64_t h2[F / 4];
+#pragma unroll
+      for (int f = 0; f < F / 4; ++f) {
+        const uint64_t keep = b1 ? h1[f + F / 4] : h1[f], send = b1 ? h1[f] : h1[f + F / 4];
+        const float2 sp = unpair(send);
+        const float rx = __shfl_xor_sync(0xffffffffu, sp.x, 2 * C::LPR);
+        const float ry = __shfl_xor_sync(0xffffffffu, sp.y, 2 * C::LPR);
+        h2[f] = fadd2(keep, pair_f32(rx, ry));
+      }
+      // 2) park the state in scratch buffer (piece_seq & 1), once the
+      //    combine of the piece two back has released it
       const int buf = piece_seq & 1;
+      const uint32_t use_parity = (piece_seq >> 1) & 1;
       if (piece_seq >= 2) {
-        bool fr = mbar_wait(sfree0 + 8 * buf, ((piece_seq >> 1) - 1) & 1, a.timeout_ns, a.status,
+        bool fr = mbar_wait(sfree0 + 8 * buf, use_parity ^ 1, a.timeout_ns, a.status,
                             kDevTimeoutDecodeFull, abort_flag);
         fr = __all_sync(0xffffffffu, fr);
         if (!fr) break;
@@ -450,175 +611,128 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       float* sm_m = sb;              // [warps][G]
       float* sm_l = sb + C::MG;      // [warps][G]
       float* sm_o = sb + 2 * C::MG;  // [warps][G][D], 16-byte aligned
-      if (lane < C::LPR) {
+      if (rg == 0 && (sub & ((1 << C::SHIFT) - 1)) == 0) {  // one lane per head x
+        sm_m[warp * G + x] = m;
+        sm_l[warp * G + x] = l;
+      }
+      {
+        // the lane's quarter: pairs base + f of the slot-major accumulators
+        const int base = (b0 ? F / 2 : 0) + (b1 ? F / 4 : 0);
+        if constexpr (F / 4 == 1) {
+          const int j = base / NP, k = base % NP;
+          const int d = (sub + 8 * (k / 4)) * 8 + 2 * (k % 4);
+          *reinterpret_cast<float2*>(sm_o + (warp * G + (j ^ x)) * D + d) = unpair(h2[0]);
+        } else {
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          if (lane == 0) {
-            sm_m[warp * G + h] = m[h];
-            sm_l[warp * G + h] = l[h];
+          for (int f = 0; f < F / 4; f += 2) {
+            const int fl = base + f;
+            const int j = fl / NP, k = fl % NP;  // k even: the pair and the next share a chunk
+            const int d = (sub + 8 * (k / 4)) * 8 + 2 * (k % 4);
+            const float2 v0 = unpair(h2[f]);
+            const float2 v1 = unpair(h2[f + 1]);
+            *reinterpret_cast<float4*>(sm_o + (warp * G + (j ^ x)) * D + d) =
+                make_float4(v0.x, v0.y, v1.x, v1.y);
           }
-#pragma unroll
-          for (int ch = 0; ch < C::NCH; ++ch)
-#pragma unroll
-            for (int k = 0; k < 4; k += 2) {
-              const float2 v0 = unpair(o[h][ch * 4 + k]);
-              const float2 v1 = unpair(o[h][ch * 4 + k + 1]);
-              *reinterpret_cast<float4*>(sm_o + (warp * G + h) * D + (sub + 8 * ch) * 8 + 2 * k) =
-                  make_float4(v0.x, v0.y, v1.x, v1.y);
-            }
         }
       }
-      // 3) the last warp to finish this piece combines it
       __syncwarp();
-      int last = 0;
-      if (lane == 0) {
-        __threadfence_block();
-        last = (atomicAdd(arrivals + buf, 1) == kDecWarps - 1) ? 1 : 0;
-        if (last) {
-          arrivals[buf] = 0;
-          __threadfence_block();
-        }
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (!last) continue;
-
-      // ---- combiner warp: 7 warp states -> the piece's result
-      const int kvh = hd.kh / a.head_groups;
-      const int hg = hd.kh % a.head_groups;
-      const size_t bh0 = static_cast<size_t>(hd.b) * a.Hq + kvh * g_total + hg * G;
-      float Mh[G], Lh[G], fw[G][kDecWarps];
+      if (lane == 0) mbar_arrive(parked0 + 8 * buf);
+      // 3) every consumer warp combines a slice of the G x D results once all
+      //    of them have parked
+      bool pk = mbar_wait(parked0 + 8 * buf, use_parity, a.timeout_ns, a.status,
+                          kDevTimeoutDecodeFull, abort_flag);
+      pk = __all_sync(0xffffffffu, pk);
+      if (!pk) break;
+      {
+        const int kvh = hd.kh / a.head_groups;
+        const int hg = hd.kh % a.head_groups;
+        const size_t bh0 = static_cast<size_t>(hd.b) * a.Hq + kvh * g_total + hg * G;
+        for (int t = warp * 32 + lane; t < G * D / 4; t += kDecWarps * 32) {
+          const int h = (t * 4) / D, d = (t * 4) % D;
+          float M = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float M = -INFINITY;
+          for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sm_m[w * G + h]);
+          const bool empty = (M == -INFINITY);
+          float Ls = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, sm_m[w * G + h]);
-        float Ls = 0.f;
-#pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) {
-          fw[h][w] = (M == -INFINITY) ? 0.f : ex2(sm_m[w * G + h] - M);
-          Ls = fmaf(sm_l[w * G + h], fw[h][w], Ls);
-        }
-        Mh[h] = M;
-        Lh[h] = Ls;
-      }
-      // lane handles elements lane*4 .. lane*4+3 of every 128-element block
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const bool empty = (Mh[h] == -INFINITY);
-        const float inv = empty ? 0.f : 1.f / Lh[h];
-#pragma unroll
-        for (int d0 = 0; d0 < D; d0 += 128) {
-          const int d = d0 + lane * 4;
-          if (d < D) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int w = 0; w < kDecWarps; ++w) {
-              const float4 v = *reinterpret_cast<const float4*>(sm_o + (w * G + h) * D + d);
-              acc.x = fmaf(v.x, fw[h][w], acc.x);
-              acc.y = fmaf(v.y, fw[h][w], acc.y);
-              acc.z = fmaf(v.z, fw[h][w], acc.z);
-              acc.w = fmaf(v.w, fw[h][w], acc.w);
-            }
-            acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-            if (hd.nsp == 1) {
-              __nv_bfloat16* dst = a.out + (bh0 + h) * D + d;
-              *reinterpret_cast<uint2*>(dst) =
-                  make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-            } else {
-              *reinterpret_cast<float4*>(a.part_o + ((bh0 + h) * a.max_slots + hd.slot) * D + d) =
-                  acc;
-            }
+          for (int w = 0; w < kDecWarps; ++w) {
+            const float fw = empty ? 0.f : ex2(sm_m[w * G + h] - M);
+            Ls = fmaf(sm_l[w * G + h], fw, Ls);
+            const float4 v = *reinterpret_cast<const float4*>(sm_o + (w * G + h) * D + d);
+            acc.x = fmaf(v.x, fw, acc.x);
+            acc.y = fmaf(v.y, fw, acc.y);
+            acc.z = fmaf(v.z, fw, acc.z);
+            acc.w = fmaf(v.w, fw, acc.w);
           }
-        }
-        if (lane == 0) {
+          const float inv = empty ? 0.f : 1.f / Ls;
+          acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
           if (hd.nsp == 1) {
-            if (a.lse != nullptr)
-              a.lse[bh0 + h] = empty ? INFINITY : (Mh[h] + log2f(Lh[h])) * kLn2;
+            __nv_bfloat16* dst = a.out + (bh0 + h) * D + d;
+            *reinterpret_cast<uint2*>(dst) =
+                make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+            if (d == 0 && a.lse != nullptr)
+              a.lse[bh0 + h] = empty ? INFINITY : (M + log2f(Ls)) * kLn2;
           } else {
-            a.part_lse[(bh0 + h) * a.max_slots + hd.slot] =
-                empty ? -INFINITY : Mh[h] + log2f(Lh[h]);
+            *reinterpret_cast<float4*>(a.part_o + ((bh0 + h) * a.max_slots + hd.slot) * D + d) = acc;
+            if (d == 0)
+              a.part_lse[(bh0 + h) * a.max_slots + hd.slot] = empty ? -INFINITY : M + log2f(Ls);
           }
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(sfree0 + 8 * buf);  // scratch buffer free again
+      if (lane == 0) {
+        mbar_arrive(sfree0 + 8 * buf);  // this warp is done with the buffer
+        if (warp == 0 && hd.nsp > 1) {
+          const int i = (*n_pending)++;
+          if (i < 2) pending[i] = Pending{static_cast<int>(hd.b * KH + hd.kh), hd.nsp, hd.b, hd.kh};
+        }
+      }
     }
   }
   __syncthreads();
+  // ---- count this CTA's split pieces; the CTA that finishes a unit's last
+  // piece merges the unit (every partial of it is visible by then)
+  const int np = min(*n_pending, 2);
+  if (np == 0 || *abort_flag) return;
+  volatile int* merge_mask = n_pending + 1;
+  if (tid == 0) {
+    __threadfence();  // the partials of this CTA, written before the barrier, first
+    const unsigned c0 = atomicAdd(a.counters + pending[0].unit, 1u);
+    const unsigned c1 = np > 1 ? atomicAdd(a.counters + pending[1].unit, 1u) : 0u;
+    int mm = c0 == static_cast<unsigned>(pending[0].nsp - 1) ? 1 : 0;
+    if (np > 1 && c1 == static_cast<unsigned>(pending[1].nsp - 1)) mm |= 2;
+    if (mm) __threadfence();
+    *merge_mask = mm;
+  }
+  __syncthreads();
+  const int mm = *merge_mask;
+  // the G rows of each unit to merge, one warp per row
+  const int n0 = (mm & 1) ? G : 0;
+  const int nrows = n0 + ((mm & 2) ? G : 0);
+  for (int t = warp; t < nrows; t += kDecWarps + 1) {
+    const Pending p = pending[t < n0 ? 0 : 1];
+    const int h = t < n0 ? t : t - n0;
+    const int kvh = p.kh / a.head_groups;
+    const int hg = p.kh % a.head_groups;
+    const size_t bh0 = static_cast<size_t>(p.b) * a.Hq + kvh * g_total + hg * G;
+    merge_row<D>(a, bh0 + h, p.nsp, lane);
+  }
 }
 
-// One warp per (batch, query head). Recomputes the piece count of its unit
-// from the same prefix sums; a unit cut into one piece was written by stage
-// 1, a batch of length 0 gets out = 0 and lse = +inf, the rest are merged
-// with all loads of a batch of pieces issued before any is used.
+// When no sequence has a key stage 1 is not launched: every row gets out = 0
+// and lse = +inf here (one warp per (batch, query head)).
 template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant__ DecodeArgs a) {
+__global__ void __launch_bounds__(128) decode_empty_kernel(const __grid_constant__ DecodeArgs a) {
   constexpr int EPL = D / 32;  // output elements per lane
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (row >= a.B * a.Hq) return;
-  const int b = row / a.Hq;
-  const int h = row % a.Hq;
-  const int g_total = a.Hq / a.Hkv;
-  const long long KH = static_cast<long long>(a.Hkv) * a.head_groups;
-  const long long kh = static_cast<long long>(h / g_total) * a.head_groups + (h % g_total) / a.G;
-  const long long L = a.prefix[b + 1] - a.prefix[b];
   __nv_bfloat16* dst = a.out + static_cast<size_t>(row) * D + lane * EPL;
-  if (L == 0) {
-    if constexpr (EPL == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
-    else *reinterpret_cast<uint32_t*>(dst) = 0u;
-    if (lane == 0 && a.lse != nullptr) a.lse[row] = INFINITY;
-    return;
-  }
-  const long long u0 = KH * a.prefix[b] + kh * L;
-  const int nsp = static_cast<int>((u0 + L - 1) / a.rows_per_cta - u0 / a.rows_per_cta + 1);
-  if (nsp <= 1) return;
-  const float* pl = a.part_lse + static_cast<size_t>(row) * a.max_slots;
-  const float* po = a.part_o + static_cast<size_t>(row) * a.max_slots * D + lane * EPL;
-  float M = -INFINITY;
-  for (int k = lane; k < nsp; k += 32) M = fmaxf(M, __ldcg(pl + k));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  const bool invalid = (M == -INFINITY);
-  float acc[EPL], W = 0.f;
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-  if (!invalid) {
-    for (int k0 = 0; k0 < nsp; k0 += 8) {
-      // all loads of up to 8 pieces in flight before any is used
-      float lk[8], v[8][EPL];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const bool in = k0 + u < nsp;
-        lk[u] = in ? __ldcg(pl + k0 + u) : -INFINITY;
-        if constexpr (EPL == 4) {
-          const float4 t = in ? __ldcg(reinterpret_cast<const float4*>(po + static_cast<size_t>(k0 + u) * D))
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-          v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
-        } else {
-          const float2 t = in ? __ldcg(reinterpret_cast<const float2*>(po + static_cast<size_t>(k0 + u) * D))
-                              : make_float2(0.f, 0.f);
-          v[u][0] = t.x; v[u][1] = t.y;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float wk = ex2(lk[u] - M);  // empty or absent piece: 0
-        W += wk;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wk, v[u][e], acc[e]);
-      }
-    }
-  }
-  const float inv = invalid ? 0.f : 1.f / W;
-  if constexpr (EPL == 4) {
-    *reinterpret_cast<uint2*>(dst) =
-        make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
-  } else {
-    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-  }
-  if (lane == 0 && a.lse != nullptr) a.lse[row] = invalid ? INFINITY : (M + log2f(W)) * kLn2;
+  if constexpr (EPL == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
+  else *reinterpret_cast<uint32_t*>(dst) = 0u;
+  if (lane == 0 && a.lse != nullptr) a.lse[row] = INFINITY;
 }
 
 template <int D, int G>
@@ -689,6 +803,12 @@ cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
   da.max_blocks = x.max_blocks;
   da.block_size = x.block_size;
   da.real_len = x.lens_dev;
+  if (x.block_table != nullptr && x.lens_dev == nullptr)
+    for (int b = 0; b < x.B; ++b)
+      da.pad16[b] = static_cast<unsigned char>(x.prefix_host[b + 1] - x.prefix_host[b] -
+                                               x.lens_host[b]);
+  da.counters = x.counters;
+  da.has_empty = x.has_empty ? 1 : 0;
 
   if (x.total > 0) {
     CUtensorMap maps[4];  // K, V with 112-row boxes; K, V with 16-row boxes
@@ -714,7 +834,7 @@ cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     count_launches(1);
   }
-  if (!x.needs_merge) return cudaSuccess;
+  if (x.total > 0 || x.B == 0) return cudaSuccess;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((x.B * x.Hq + 3) / 4);
@@ -726,8 +846,8 @@ cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = (x.D == 128) ? cudaLaunchKernelEx(&cfg, decode_merge_kernel<128>, da)
-                                     : cudaLaunchKernelEx(&cfg, decode_merge_kernel<64>, da);
+  const cudaError_t e = (x.D == 128) ? cudaLaunchKernelEx(&cfg, decode_empty_kernel<128>, da)
+                                     : cudaLaunchKernelEx(&cfg, decode_empty_kernel<64>, da);
   if (e == cudaSuccess) count_launches(1);
   return e;
 }

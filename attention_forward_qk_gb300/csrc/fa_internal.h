@@ -43,11 +43,12 @@ struct DecodeLaunch {
   long long total;            // rows of the work space (KV heads x head groups x sum L_b)
   long long rows_per_cta;     // contiguous share of each CTA
   int max_slots;              // piece slots per (batch, head) in the partial buffers
-  bool needs_merge;           // some sequence has more than one piece, or length 0
   const long long* prefix_host;  // [B + 1] prefix sums of the lengths
   const long long* prefix_dev;   // the same in the workspace, or null (then in params)
   float* part_o;            // [B, Hq, max_slots, D]
   float* part_lse;          // [B, Hq, max_slots] (log2 domain)
+  unsigned int* counters;   // [B * units per batch] pieces finished, zeroed before the launch
+  bool has_empty;           // some sequence has length 0
   // paged K/V (block_table != null): k, v are block pools of num_blocks blocks
   // of block_size rows in `layout` (BSND: PA_BBND, BNSD: PA_BNBD), logical
   // row r of batch b lives in block block_table[b * max_blocks + r / block_size];
@@ -55,7 +56,8 @@ struct DecodeLaunch {
   // lens_host / lens_dev give the real ones
   const int32_t* block_table;
   int max_blocks, num_blocks, block_size;
-  const int* lens_dev;      // [B] real lengths in the workspace (paged only)
+  const int* lens_dev;      // [B] real lengths in the workspace (paged, B > kDecodeParamBatches)
+  const int64_t* lens_host; // [B] real lengths (paged only)
   void* out;
   float* lse;
   uint32_t* status;

@@ -12,8 +12,10 @@ prefill) under "workloads".
 
 Timing: W untimed warm-up steps, then exactly K steps, each bracketed by
 CUDA events on the launching stream; L2 is flushed (512 MB write) between
-steps, outside the events. The main kernel of each step is timed by events
-the library records around it (fa_set_main_kernel_events). Multi-GPU: one
+steps, outside the events. The main kernel is timed in a second pass of K
+steps by events the library records right around it
+(fa_set_main_kernel_events); they are kept out of the first pass, whose
+step times they would inflate. Multi-GPU: one
 process per GPU under torchrun; every rank runs its own replica of the
 workload (weak scaling, no collective on the data path), the per-rank time
 is max-reduced. With --impl reference the fp64 CPU oracle is timed instead
@@ -319,9 +321,16 @@ class L2Flush:
         torch.sum(self.r, dim=0, keepdim=True, out=self.sink)
 
 
-def time_steps(runner, steps, warmup, flush, fn=None):
+def time_steps(runner, steps, warmup, flush, fn=None, kernel=True):
     """Per-step CUDA-event times (ms) of `fn` (default runner.step) and of the
-    main kernel inside it; L2 flushed before every step, outside the events."""
+    main kernel inside it; L2 flushed before every step, outside the events.
+
+    Two timed passes of `steps` steps each: the step times come from the
+    first, where nothing but the two bracketing events is recorded; the main
+    kernel's times from the second, where the library also records an event
+    right before and after that kernel (an event between two launches breaks
+    their programmatic overlap and costs stream time, so it would inflate the
+    step time of the first pass). Launches are counted in the first pass."""
     import torch
     F = runner.F
     fn = fn or runner.step
@@ -329,23 +338,35 @@ def time_steps(runner, steps, warmup, flush, fn=None):
         flush()
         fn()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
-    for e in evs:  # create the handles
-        for x in e:
-            x.record()
-    torch.cuda.synchronize()
+
+    def new_events(n):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n)] for _ in range(steps)]
+        for e in evs:  # create the handles
+            for x in e:
+                x.record()
+        torch.cuda.synchronize()
+        return evs
+
+    evs = new_events(2)
     l0 = F.fa_kernel_launch_count()
     for e in evs:
         flush()
-        F.fa_set_main_kernel_events(e[2], e[3])
         e[0].record()
         fn()
         e[1].record()
-    F.fa_set_main_kernel_events(None, None)
     torch.cuda.synchronize()
     launches = F.fa_kernel_launch_count() - l0
     step_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    main_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    main_ms = []
+    if kernel:
+        kev = new_events(2)
+        for e in kev:
+            flush()
+            F.fa_set_main_kernel_events(e[0], e[1])
+            fn()
+        F.fa_set_main_kernel_events(None, None)
+        torch.cuda.synchronize()
+        main_ms = [e[0].elapsed_time(e[1]) for e in kev]
     return step_ms, main_ms, launches
 
 
@@ -496,7 +517,7 @@ def run_gpu(args):
     host_lse = torch.empty(main.lse.shape, dtype=torch.float32, pin_memory=True)
     e2e_steps = max(3, min(args.steps, 20))
     e_ms, _, _ = time_steps(main, e2e_steps, 2, flush,
-                            fn=lambda: main.e2e_step(host_out, host_lse))
+                            fn=lambda: main.e2e_step(host_out, host_lse), kernel=False)
     e2e_ms = sum(e_ms) / len(e_ms)
     (e2e_ms,) = max_over_ranks([e2e_ms], world, dev)
     e2e_val, _ = value_of(w.kind, main.units["step"] * world, e2e_ms)

@@ -202,6 +202,23 @@ def test_gqa_decode_workload(cuda_device):
     assert torch.equal(lse, lse2)
 
 
+def test_decode_reuses_a_dirty_workspace(cuda_device):
+    # The pieces of a sequence cut across CTAs are counted in the workspace and
+    # merged by the CTA that finishes the last one: one workspace, filled with
+    # 0xFF bytes first, serves calls whose lengths cut the sequences into
+    # different numbers of pieces (and some into none), each exact.
+    B, Hq, Hkv, S, D = 4, 32, 8, 4096, 128
+    size = F.fa_decode_workspace_size(B, S, Hq, Hkv, D, 0)
+    ws = torch.full((size,), 255, dtype=torch.uint8, device="cuda")
+    for seed, lo, hi in [(11, 1, 4096), (12, 3000, 4096), (13, 0, 60), (14, 1, 4096)]:
+        x = workloads.make_decode(B, Hq, Hkv, S, D, "BNSD", seed=seed, len_lo=lo, len_hi=hi)
+        q, k, v = _gpu(x["q"]), _gpu(x["k"]), _gpu(x["v"])
+        out, lse = F.fa_decode(q, k, v, x["lengths"], scale=0.09, workspace=ws)
+        torch.cuda.synchronize()
+        ro, rl = oracle.decode(x["q"], x["k"], x["v"], x["lengths"], scale=0.09)
+        compare(out, lse, ro, rl, "BNSD")
+
+
 @pytest.fixture(scope="module")
 def long_decode():
     w = workloads.WORKLOADS["long_decode"]
