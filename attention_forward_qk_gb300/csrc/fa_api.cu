@@ -265,7 +265,7 @@ const char* fa_status_string(int s) {
     case FA_OK: return "FA_OK";
     case FA_ERR_NULLPTR: return "FA_ERR_NULLPTR: a required pointer is NULL";
     case FA_ERR_PARAM_INVALID: return "FA_ERR_PARAM_INVALID: argument outside the contract";
-    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be 64 or 128";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be 64 or 128 (or 256 for decode)";
     case FA_ERR_WORKSPACE_TOO_SMALL: return "FA_ERR_WORKSPACE_TOO_SMALL";
     case FA_ERR_RUNTIME: return "FA_ERR_RUNTIME: a CUDA call failed";
     case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT: a kernel wait expired";
@@ -308,7 +308,7 @@ fa_status decode_plan_impl(int64_t B, int64_t S_kv_max, int64_t num_heads, int64
   if (B < 0 || S_kv_max < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
       num_heads % num_kv_heads != 0 || num_splits < 0 || num_sms <= 0 || S_kv_max > kMaxDim)
     return FA_ERR_PARAM_INVALID;
-  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
   int64_t sum = 0;
   for (int64_t b = 0; b < B; ++b) {
     if (lens[b] < 0 || lens[b] > S_kv_max) return FA_ERR_PARAM_INVALID;
@@ -352,15 +352,16 @@ size_t fa_decode_workspace_size(int64_t B, int64_t S_kv_max, int64_t num_heads,
   return decode_ws(B, num_heads, D, max_slots_bound(S_kv_max, num_splits)).total;
 }
 
+// Head dims: 64 and 128 everywhere; 256 for decode as well.
 static fa_status check_common(int64_t B, int64_t S_q, int64_t S_kv, int64_t Hq, int64_t& Hkv,
-                              int64_t D, float scale, int layout) {
+                              int64_t D, float scale, int layout, bool decode = false) {
   if (Hkv == 0) Hkv = Hq;
   if (B < 0 || S_q < 0 || S_kv < 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return FA_ERR_PARAM_INVALID;
   if (Hq % Hkv != 0) return FA_ERR_PARAM_INVALID;
   if (layout != FA_LAYOUT_BNSD && layout != FA_LAYOUT_BSND) return FA_ERR_PARAM_INVALID;
   if (!isfinite(scale)) return FA_ERR_PARAM_INVALID;
   if (B > kMaxDim || S_q > kMaxDim || S_kv > kMaxDim || Hq > 65535) return FA_ERR_PARAM_INVALID;
-  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && !(decode && D == 256)) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
@@ -559,7 +560,7 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
       lens == nullptr)
     return FA_ERR_NULLPTR;
   int64_t Hkv = num_kv_heads;
-  fa_status st = check_common(B, 1, S_kv_max, num_heads, Hkv, D, scale, layout);
+  fa_status st = check_common(B, 1, S_kv_max, num_heads, Hkv, D, scale, layout, true);
   if (st != FA_OK) return st;
   if (num_splits < 0) return FA_ERR_PARAM_INVALID;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||

@@ -54,34 +54,41 @@ namespace {
 constexpr int kDecWarps = 7;                       // consumer warps
 constexpr int kDecThreads = (kDecWarps + 1) * 32;  // + one producer warp
 constexpr int kRingBytes = 172032;                 // K/V ring (168 KB)
-constexpr int kQBytes = 1024;                      // q of one piece (G * D * 2 <= 1 KB)
 constexpr int kMaxStages = 6;
-constexpr int kTailBox = 16;  // rows per box of a piece's last, partial stage
 constexpr float kLn2 = 0.69314718055994530942f;
 
 template <int D, int G>
 struct DecCfg {
-  static constexpr int LPR = 8;                     // lanes per K/V row
-  static constexpr int NCH = D / 64;                // 16-byte chunks of a row per lane
-  static constexpr int RPW = 32 / LPR;              // rows per warp per step
-  static constexpr int R = kDecodeStageRows;        // rows per stage (112)
-  static constexpr int RPWS = R / kDecWarps;        // rows per warp per stage (16)
+  // lanes per K/V row: 8 (D = 64: one 16-byte chunk each; D = 128: two),
+  // 16 for D = 256 (two chunks each), so that q and o of a GQA group of up to
+  // four heads fit the registers
+  static constexpr int LPR = D == 256 ? 16 : 8;
+  static constexpr int LOG_LPR = D == 256 ? 4 : 3;
+  static constexpr int NCH = D / (8 * LPR);         // 16-byte chunks of a row per lane
+  static constexpr int RPW = 32 / LPR;              // rows per warp per step (row groups)
+  // rows per stage: 112, or 56 for D = 256 (three stages in the ring)
+  static constexpr int R = D == 256 ? 56 : kDecodeStageRows;
+  static constexpr int TAIL = D == 256 ? 8 : 16;    // rows per box of a partial stage
+  static constexpr int RPWS = R / kDecWarps;        // rows per warp per stage (16 or 8)
   static constexpr int STEPS = RPWS / RPW;          // 4
   static constexpr int TILE_BYTES = R * D * 2;
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int NST = kRingBytes / STAGE_BYTES;  // 3 (D = 128) or 6 (D = 64)
+  static constexpr int NST = kRingBytes / STAGE_BYTES;  // 3 (D = 128, 256) or 6 (D = 64)
   static constexpr int NP = 4 * NCH;                // fp32 pairs per lane per head
   static constexpr int LG = G >= 8 ? 3 : G >= 4 ? 2 : G >= 2 ? 1 : 0;  // log2(G)
-  static constexpr int SHIFT = 3 - LG;              // head of lane `sub`: sub >> SHIFT
+  static constexpr int SHIFT = LOG_LPR - LG;        // head of lane `sub`: sub >> SHIFT
+  static constexpr int QB = G * D * 2 > 1024 ? 2048 : 1024;  // q of one piece
   // one scratch buffer: m[warps][G] and l[warps][G], each padded to a
   // multiple of 4 floats so that o[warps][G][D] and the next buffer stay
-  // 16-byte aligned for the float4 accesses
+  // 16-byte aligned for the float4 accesses; two buffers unless D = 256
+  static constexpr int NSB = D == 256 ? 1 : 2;
   static constexpr int MG = (kDecWarps * G + 3) / 4 * 4;
   static constexpr int SCRATCH_FLOATS = 2 * MG + kDecWarps * G * D;
-  static constexpr int SMEM = kRingBytes + 2 * SCRATCH_FLOATS * 4 + kMaxStages * kQBytes + 1024;
+  static constexpr int SMEM = kRingBytes + NSB * SCRATCH_FLOATS * 4 + kMaxStages * QB + 1024;
   static_assert(SCRATCH_FLOATS % 4 == 0, "scratch alignment");
   static_assert(NST <= kMaxStages, "ring slots");
-  static_assert(R % (kDecWarps * RPW) == 0, "stage rows");
+  static_assert(R % (kDecWarps * RPW) == 0 && R % TAIL == 0, "stage rows");
+  static_assert(SMEM <= 232448, "shared memory");
 };
 
 // Where the length prefix sums live: launch parameters for small batches,
@@ -172,10 +179,14 @@ __device__ __forceinline__ void merge_row(const DecodeArgs& a, size_t row, int n
     for (int u = 0; u < 8; ++u) {
       const bool in = k0 + u < nsp;
       lk[u] = in ? __ldcg(pl + k0 + u) : -INFINITY;
-      if constexpr (EPL == 4) {
-        const float4 t = in ? __ldcg(reinterpret_cast<const float4*>(po + static_cast<size_t>(k0 + u) * D))
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-        v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+      if constexpr (EPL % 4 == 0) {
+#pragma unroll
+        for (int e = 0; e < EPL; e += 4) {
+          const float4 t =
+              in ? __ldcg(reinterpret_cast<const float4*>(po + static_cast<size_t>(k0 + u) * D + e))
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[u][e] = t.x; v[u][e + 1] = t.y; v[u][e + 2] = t.z; v[u][e + 3] = t.w;
+        }
       } else {
         const float2 t = in ? __ldcg(reinterpret_cast<const float2*>(po + static_cast<size_t>(k0 + u) * D))
                             : make_float2(0.f, 0.f);
@@ -202,9 +213,11 @@ __device__ __forceinline__ void merge_row(const DecodeArgs& a, size_t row, int n
   const bool invalid = (M == -INFINITY);
   const float inv = invalid ? 0.f : 1.f / W;
   __nv_bfloat16* dst = a.out + row * D + lane * EPL;
-  if constexpr (EPL == 4) {
-    *reinterpret_cast<uint2*>(dst) =
-        make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  if constexpr (EPL % 4 == 0) {
+#pragma unroll
+    for (int e = 0; e < EPL; e += 4)
+      *reinterpret_cast<uint2*>(dst + e) = make_uint2(pack_bf16x2(acc[e] * inv, acc[e + 1] * inv),
+                                                      pack_bf16x2(acc[e + 2] * inv, acc[e + 3] * inv));
   } else {
     *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
   }
@@ -227,9 +240,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float* scratch = reinterpret_cast<float*>(smem + kRingBytes);  // 2 buffers
-  unsigned char* qbuf = smem + kRingBytes + 2 * C::SCRATCH_FLOATS * 4;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(qbuf + kMaxStages * kQBytes);
+  float* scratch = reinterpret_cast<float*>(smem + kRingBytes);  // NSB buffers
+  unsigned char* qbuf = smem + kRingBytes + C::NSB * C::SCRATCH_FLOATS * 4;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qbuf + kMaxStages * C::QB);
   // bars: full[kMaxStages], empty[kMaxStages], scratch free[2], scratch parked[2]
   SlotHeader* hdr = reinterpret_cast<SlotHeader*>(bars + 2 * kMaxStages + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(hdr + kMaxStages);
@@ -342,16 +355,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           if (a.block_table != nullptr) {
             // paged: 16-row boxes (pieces and lengths are multiples of 16 rows in
             // the work space, blocks are multiples of 16 rows), each from its block
-            const int nb = (rows_here + kTailBox - 1) / kTailBox;
-            mbar_expect_tx(full0 + 8 * slot, 2 * nb * kTailBox * D * 2 + q_bytes);
+            const int nb = (rows_here + C::TAIL - 1) / C::TAIL;
+            mbar_expect_tx(full0 + 8 * slot, 2 * nb * C::TAIL * D * 2 + q_bytes);
             const int32_t* bt = a.block_table + static_cast<size_t>(h.b) * a.max_blocks;
             for (int t = 0; t < nb; ++t) {
-              const int lr = row + t * kTailBox;
+              const int lr = row + t * C::TAIL;
               const int blk = __ldg(bt + lr / a.block_size);
               const int in_blk = lr % a.block_size;
-              tma_load_4d(dst + t * kTailBox * D * 2, &tm_k16, full0 + 8 * slot, 0, in_blk, kvh,
+              tma_load_4d(dst + t * C::TAIL * D * 2, &tm_k16, full0 + 8 * slot, 0, in_blk, kvh,
                           blk);
-              tma_load_4d(dst + C::TILE_BYTES + t * kTailBox * D * 2, &tm_v16, full0 + 8 * slot,
+              tma_load_4d(dst + C::TILE_BYTES + t * C::TAIL * D * 2, &tm_v16, full0 + 8 * slot,
                           0, in_blk, kvh, blk);
             }
           } else if (rows_here == C::R) {
@@ -360,19 +373,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             tma_load_4d(dst + C::TILE_BYTES, &tm_v, full0 + 8 * slot, 0, row, kvh, h.b);
           } else {
             // partial last stage: 16-row boxes, only as many as the piece needs
-            const int nb = (rows_here + kTailBox - 1) / kTailBox;
-            mbar_expect_tx(full0 + 8 * slot, 2 * nb * kTailBox * D * 2 + q_bytes);
+            const int nb = (rows_here + C::TAIL - 1) / C::TAIL;
+            mbar_expect_tx(full0 + 8 * slot, 2 * nb * C::TAIL * D * 2 + q_bytes);
             for (int t = 0; t < nb; ++t) {
-              tma_load_4d(dst + t * kTailBox * D * 2, &tm_k16, full0 + 8 * slot, 0,
-                          row + t * kTailBox, kvh, h.b);
-              tma_load_4d(dst + C::TILE_BYTES + t * kTailBox * D * 2, &tm_v16, full0 + 8 * slot,
-                          0, row + t * kTailBox, kvh, h.b);
+              tma_load_4d(dst + t * C::TAIL * D * 2, &tm_k16, full0 + 8 * slot, 0,
+                          row + t * C::TAIL, kvh, h.b);
+              tma_load_4d(dst + C::TILE_BYTES + t * C::TAIL * D * 2, &tm_v16, full0 + 8 * slot,
+                          0, row + t * C::TAIL, kvh, h.b);
             }
           }
           if (s == 0) {
             const __nv_bfloat16* qsrc =
                 a.q + (static_cast<size_t>(h.b) * a.Hq + kvh * g_total + hg * G) * D;
-            bulk_load(smem_u32(qbuf + slot * kQBytes), qsrc, q_bytes, full0 + 8 * slot);
+            bulk_load(smem_u32(qbuf + slot * C::QB), qsrc, q_bytes, full0 + 8 * slot);
           }
         }
       }
@@ -435,7 +448,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         row_begin = hd.row0;
         row_end = hd.row0 + hd.vend;  // rows past a paged length hold no key
         mask_row = a.key_mask ? a.key_mask + static_cast<size_t>(hd.b) * a.S_kv : nullptr;
-        const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(qbuf + slot * kQBytes);
+        const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(qbuf + slot * C::QB);
         m = -INFINITY;
         l = 0.f;
 #pragma unroll
@@ -444,7 +457,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           for (int k = 0; k < NP; ++k) o[j][k] = 0ull;
 #pragma unroll
           for (int ch = 0; ch < C::NCH; ++ch) {
-            const uint4 u = *reinterpret_cast<const uint4*>(qs + (j ^ x) * D + (sub + 8 * ch) * 8);
+            const uint4 u = *reinterpret_cast<const uint4*>(qs + (j ^ x) * D + (sub + C::LPR * ch) * 8);
             const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -475,7 +488,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         uint64_t kp[NP];
 #pragma unroll
         for (int ch = 0; ch < C::NCH; ++ch) {
-          const uint4 u = *reinterpret_cast<const uint4*>(Ks + r * D + (sub + 8 * ch) * 8);
+          const uint4 u = *reinterpret_cast<const uint4*>(Ks + r * D + (sub + C::LPR * ch) * 8);
           kp[ch * 4 + 0] = bf16x2_pair(u.x);
           kp[ch * 4 + 1] = bf16x2_pair(u.y);
           kp[ch * 4 + 2] = bf16x2_pair(u.z);
@@ -511,7 +524,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             part[j] += __shfl_xor_sync(0xffffffffu, part[j + half], (C::LPR / 2) >> lv);
         }
 #pragma unroll
-        for (int lv = C::LG; lv < 3; ++lv)
+        for (int lv = C::LG; lv < C::LOG_LPR; ++lv)
           part[0] += __shfl_xor_sync(0xffffffffu, part[0], (C::LPR / 2) >> lv);
         s[i] = ok ? part[0] : -INFINITY;
       }
@@ -521,8 +534,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       float mx = s[0];
 #pragma unroll
       for (int i = 1; i < C::STEPS; ++i) mx = fmaxf(mx, s[i]);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, C::LPR));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2 * C::LPR));
+#pragma unroll
+      for (int off = C::LPR; off < 32; off <<= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
       const float mn = fmaxf(m, mx);
       const float m_use = (mn == -INFINITY) ? 0.f : mn;
       const float alpha = ex2(m - m_use);  // 0 when m was -inf
@@ -550,7 +564,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         uint64_t vp[NP];
 #pragma unroll
         for (int ch = 0; ch < C::NCH; ++ch) {
-          uint4 u = *reinterpret_cast<const uint4*>(Vs + r * D + (sub + 8 * ch) * 8);
+          uint4 u = *reinterpret_cast<const uint4*>(Vs + r * D + (sub + C::LPR * ch) * 8);
           if (!dense && !valid[i]) u = make_uint4(0u, 0u, 0u, 0u);  // stale rows never enter a product
           vp[ch * 4 + 0] = bf16x2_pair(u.x);
           vp[ch * 4 + 1] = bf16x2_pair(u.y);
@@ -571,12 +585,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
       // ================================================= end of the piece
       // 1) this warp's state: m is shared by the row groups, l and o add up.
-      //    The accumulators are halved twice across the row groups (lanes
-      //    xor 8, xor 16): a lane keeps one half and adds the partner's copy
-      //    of it, so that it ends with a quarter of them, summed over the warp.
-      l += __shfl_xor_sync(0xffffffffu, l, C::LPR);
-      l += __shfl_xor_sync(0xffffffffu, l, 2 * C::LPR);
+      //    The accumulators are halved across the row groups (lanes xor LPR,
+      //    then xor 2 LPR when there are four): a lane keeps one half and adds
+      //    the partner's copy of it, so that it ends with 1/RPW of them,
+      //    summed over the warp.
+#pragma unroll
+      for (int off = C::LPR; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
       constexpr int F = G * NP;  // accumulator pairs of a lane, slot-major
+      constexpr int FQ = F / C::RPW;  // pairs a lane keeps
       const bool b0 = (rg & 1) != 0, b1 = (rg & 2) != 0;
       uint64_t h1[F / 2];
 #pragma unroll
@@ -588,20 +604,26 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const float ry = __shfl_xor_sync(0xffffffffu, sp.y, C::LPR);
         h1[f] = fadd2(keep, pair_f32(rx, ry));
       }
-      uint64_t h2[F / 4];
+      uint64_t hq[FQ];
+      if constexpr (C::RPW == 4) {
 #pragma unroll
-      for (int f = 0; f < F / 4; ++f) {
-        const uint64_t keep = b1 ? h1[f + F / 4] : h1[f], send = b1 ? h1[f] : h1[f + F / 4];
-        const float2 sp = unpair(send);
-        const float rx = __shfl_xor_sync(0xffffffffu, sp.x, 2 * C::LPR);
-        const float ry = __shfl_xor_sync(0xffffffffu, sp.y, 2 * C::LPR);
-        h2[f] = fadd2(keep, pair_f32(rx, ry));
+        for (int f = 0; f < F / 4; ++f) {
+          const uint64_t keep = b1 ? h1[f + F / 4] : h1[f], send = b1 ? h1[f] : h1[f + F / 4];
+          const float2 sp = unpair(send);
+          const float rx = __shfl_xor_sync(0xffffffffu, sp.x, 2 * C::LPR);
+          const float ry = __shfl_xor_sync(0xffffffffu, sp.y, 2 * C::LPR);
+          hq[f] = fadd2(keep, pair_f32(rx, ry));
+        }
+      } else {
+#pragma unroll
+        for (int f = 0; f < FQ; ++f) hq[f] = h1[f];
       }
-      // 2) park the state in scratch buffer (piece_seq & 1), once the
-      //    combine of the piece two back has released it
-      const int buf = piece_seq & 1;
-      const uint32_t use_parity = (piece_seq >> 1) & 1;
-      if (piece_seq >= 2) {
+      // 2) park the state in scratch buffer piece_seq % NSB, once the combine
+      //    of the piece that used it last has released it
+      const int buf = piece_seq % C::NSB;
+      const int use = piece_seq / C::NSB;
+      const uint32_t use_parity = use & 1;
+      if (use >= 1) {
         bool fr = mbar_wait(sfree0 + 8 * buf, use_parity ^ 1, a.timeout_ns, a.status,
                             kDevTimeoutDecodeFull, abort_flag);
         fr = __all_sync(0xffffffffu, fr);
@@ -616,20 +638,20 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         sm_l[warp * G + x] = l;
       }
       {
-        // the lane's quarter: pairs base + f of the slot-major accumulators
+        // the lane's share: pairs base + f of the slot-major accumulators
         const int base = (b0 ? F / 2 : 0) + (b1 ? F / 4 : 0);
-        if constexpr (F / 4 == 1) {
+        if constexpr (FQ == 1) {
           const int j = base / NP, k = base % NP;
-          const int d = (sub + 8 * (k / 4)) * 8 + 2 * (k % 4);
-          *reinterpret_cast<float2*>(sm_o + (warp * G + (j ^ x)) * D + d) = unpair(h2[0]);
+          const int d = (sub + C::LPR * (k / 4)) * 8 + 2 * (k % 4);
+          *reinterpret_cast<float2*>(sm_o + (warp * G + (j ^ x)) * D + d) = unpair(hq[0]);
         } else {
 #pragma unroll
-          for (int f = 0; f < F / 4; f += 2) {
+          for (int f = 0; f < FQ; f += 2) {
             const int fl = base + f;
             const int j = fl / NP, k = fl % NP;  // k even: the pair and the next share a chunk
-            const int d = (sub + 8 * (k / 4)) * 8 + 2 * (k % 4);
-            const float2 v0 = unpair(h2[f]);
-            const float2 v1 = unpair(h2[f + 1]);
+            const int d = (sub + C::LPR * (k / 4)) * 8 + 2 * (k % 4);
+            const float2 v0 = unpair(hq[f]);
+            const float2 v1 = unpair(hq[f + 1]);
             *reinterpret_cast<float4*>(sm_o + (warp * G + (j ^ x)) * D + d) =
                 make_float4(v0.x, v0.y, v1.x, v1.y);
           }
@@ -730,8 +752,8 @@ __global__ void __launch_bounds__(128) decode_empty_kernel(const __grid_constant
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (row >= a.B * a.Hq) return;
   __nv_bfloat16* dst = a.out + static_cast<size_t>(row) * D + lane * EPL;
-  if constexpr (EPL == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
-  else *reinterpret_cast<uint32_t*>(dst) = 0u;
+#pragma unroll
+  for (int e = 0; e < EPL; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = 0u;
   if (lane == 0 && a.lse != nullptr) a.lse[row] = INFINITY;
 }
 
@@ -811,24 +833,29 @@ cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
   da.has_empty = x.has_empty ? 1 : 0;
 
   if (x.total > 0) {
-    CUtensorMap maps[4];  // K, V with 112-row boxes; K, V with 16-row boxes
+    // K, V with stage-high boxes (112 rows, 56 for D = 256); K, V with the
+    // boxes of a partial stage (16 rows, 8 for D = 256)
+    CUtensorMap maps[4];
+    const int stage_rows = x.D == 256 ? 56 : kDecodeStageRows;
+    const int tail_rows = x.D == 256 ? 8 : 16;
     // a paged cache is a batch of num_blocks sequences of block_size rows
     const int nbat = x.block_table != nullptr ? x.num_blocks : x.B;
     const int S_map = x.block_table != nullptr ? x.block_size : std::max(x.S_kv, 1);
-    // (the 112-row maps are not used for a paged cache, whose blocks may be shorter)
-    const int box_rows = x.block_table != nullptr ? kTailBox : kDecodeStageRows;
+    // (the stage-high maps are not used for a paged cache, whose blocks may be shorter)
+    const int box_rows = x.block_table != nullptr ? tail_rows : stage_rows;
     if (!encode_bf16_map(&maps[0], x.k, x.layout, nbat, x.Hkv, S_map, x.D, x.D, box_rows,
                          CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_bf16_map(&maps[1], x.v, x.layout, nbat, x.Hkv, S_map, x.D, x.D, box_rows,
                          CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_bf16_map(&maps[2], x.k, x.layout, nbat, x.Hkv, S_map, x.D, x.D, kTailBox,
+        !encode_bf16_map(&maps[2], x.k, x.layout, nbat, x.Hkv, S_map, x.D, x.D, tail_rows,
                          CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_bf16_map(&maps[3], x.v, x.layout, nbat, x.Hkv, S_map, x.D, x.D, kTailBox,
+        !encode_bf16_map(&maps[3], x.v, x.layout, nbat, x.Hkv, S_map, x.D, x.D, tail_rows,
                          CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
     const int grid = static_cast<int>((x.total + x.rows_per_cta - 1) / x.rows_per_cta);
     main_kernel_begin(stream);
-    const cudaError_t e = (x.D == 128) ? launch_decode_d<128>(G, grid, maps, da, stream)
+    const cudaError_t e = x.D == 256   ? launch_decode_d<256>(G, grid, maps, da, stream)
+                          : x.D == 128 ? launch_decode_d<128>(G, grid, maps, da, stream)
                                        : launch_decode_d<64>(G, grid, maps, da, stream);
     main_kernel_end(stream);
     if (e != cudaSuccess) return e;
@@ -846,7 +873,8 @@ cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = (x.D == 128) ? cudaLaunchKernelEx(&cfg, decode_empty_kernel<128>, da)
+  const cudaError_t e = x.D == 256   ? cudaLaunchKernelEx(&cfg, decode_empty_kernel<256>, da)
+                        : x.D == 128 ? cudaLaunchKernelEx(&cfg, decode_empty_kernel<128>, da)
                                      : cudaLaunchKernelEx(&cfg, decode_empty_kernel<64>, da);
   if (e == cudaSuccess) count_launches(1);
   return e;

@@ -37,7 +37,8 @@
  *     (aclnnIncreFlashAttention guide §四 actualSeqLengths and §1.1).
  *   - A query row with no valid key gets out = 0 and lse = +inf (FlashAttn
  *     guide §1.7, row invalid).
- *   - Head dimension D must be 64 or 128.
+ *   - Head dimension D must be 64 or 128; decode (fa_decode, fa_decode_paged,
+ *     fa_decode_noalloc) also takes 256.
  *   - Two-stage use as in aclnnIncreFlashAttention guide §三: ask for the
  *     workspace size, allocate it on the device, then call. The caller owns
  *     every buffer; the library allocates no device memory and keeps no
@@ -45,7 +46,9 @@
  *   - All device work is enqueued on `stream` (a cudaStream_t; NULL = the
  *     legacy default stream) and runs asynchronously. Argument errors are
  *     detected and returned before anything is enqueued.
- *   - Results are deterministic: no atomics, fixed reduction order.
+ *   - Results are deterministic: every reduction runs in a fixed order (in
+ *     decode, atomic counters only decide which CTA merges a sequence's pieces,
+ *     not the order in which they are summed).
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -65,7 +68,8 @@ typedef enum {
   FA_OK = 0,
   FA_ERR_NULLPTR = 1,             /* a required pointer is NULL */
   FA_ERR_PARAM_INVALID = 2,       /* a size, layout, mode or length is outside the contract */
-  FA_ERR_UNSUPPORTED = 3,         /* allowed by the pages but not built here (D not 64/128) */
+  FA_ERR_UNSUPPORTED = 3,         /* allowed by the pages but not built here (D not 64/128, or
+                                     256 outside decode) */
   FA_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes below the size query's answer */
   FA_ERR_RUNTIME = 5,             /* a CUDA call failed (launch, copy, device query) */
   FA_ERR_DEVICE_TIMEOUT = 6       /* a kernel's bounded wait expired; outputs are undefined */
@@ -177,8 +181,11 @@ size_t fa_decode_workspace_size(int64_t B, int64_t S_kv_max, int64_t num_heads,
  *   lse                 NULL or device fp32 [B, num_heads]
  *   workspace           device, >= fa_decode_workspace_size(..., num_splits)
  *                       bytes, 256-byte aligned
- * The lengths are read on the host during the call; a small table derived
- * from them is copied into the workspace on `stream`. */
+ * The lengths are read on the host during the call. On `stream` the call
+ * clears the per-sequence piece counters in the workspace, copies the
+ * lengths' prefix sums there when B > 1024 (else they travel in the launch
+ * parameters), and launches one kernel: the CTA that finishes the last piece
+ * of a sequence cut into several merges them. */
 fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* key_mask,
                     const int64_t* actual_seq_lengths, int64_t B, int64_t S_kv_max,
                     int64_t num_heads, int64_t num_kv_heads, int64_t D, float scale, int layout,

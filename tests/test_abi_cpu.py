@@ -164,6 +164,16 @@ def test_decode_zero_batch_is_noop(lib):
     assert _dec(lib, B=0, lens=[]) == _lib.FA_OK
 
 
+def test_head_dim_256_is_a_decode_only_extension(lib):
+    # decode takes D = 256 (the plan and the size query too); prefill does not
+    assert _dec(lib, D=256, B=0, lens=[]) == _lib.FA_OK
+    assert _dec(lib, D=192, B=0, lens=[]) == _lib.FA_ERR_UNSUPPORTED
+    assert F.fa_decode_workspace_size(2, 4096, 16, 4, 256, 0) > 0
+    rc, n, mx = _plan([4096, 100], 4096, 16, 4, D=256)
+    assert rc >= 224 and n >= 1 and mx >= 1
+    assert _fwd(lib, D=256) == _lib.FA_ERR_UNSUPPORTED
+
+
 def _plan(lens, S, Hq, Hkv, sms=152, splits=0, D=128):
     return F.fa_decode_plan(lens, S, Hq, Hkv, D, sms, splits)
 

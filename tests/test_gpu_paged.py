@@ -66,6 +66,9 @@ CASES = [
     (4, 8, 1, 128, [0, 200, 17, 1500], 32, "PA_BNBD", 0),
     (2, 8, 2, 128, [3000, 2999], 1024, "PA_BBND", 8),
     (1, 32, 8, 128, [8192], 128, "PA_BNBD", 64),
+    # head dim 256: 56-row stages, 8-row boxes
+    (3, 16, 4, 256, [777, 16, 2048], 16, "PA_BBND", 0),
+    (2, 8, 8, 256, [1500, 90], 48, "PA_BNBD", 3),
 ]
 
 

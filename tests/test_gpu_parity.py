@@ -166,6 +166,10 @@ DECODE_CASES = [
     (5, 6, 3, 333, 128, "BSND", 0, 333, 4, False),
     (1, 4, 4, 4096, 64, "BNSD", 4096, 4096, 7, True),
     (2, 32, 1, 513, 128, "BNSD", 1, 513, 0, False),
+    # head dim 256 (decode only): G = 4, 1 and 2 heads per CTA
+    (3, 16, 4, 700, 256, "BNSD", 0, 700, 0, False),
+    (2, 8, 8, 2500, 256, "BSND", 1, 2500, 5, True),
+    (4, 16, 8, 1200, 256, "BNSD", 100, 1200, 0, False),
 ]
 
 
@@ -217,6 +221,14 @@ def test_decode_reuses_a_dirty_workspace(cuda_device):
         torch.cuda.synchronize()
         ro, rl = oracle.decode(x["q"], x["k"], x["v"], x["lengths"], scale=0.09)
         compare(out, lse, ro, rl, "BNSD")
+
+
+def test_d256_decode_workload(cuda_device):
+    w = workloads.WORKLOADS["d256_decode"]
+    x = workloads.make(w)
+    out, lse = run_decode(x, scale=w.scale)
+    ro, rl = oracle.decode(x["q"], x["k"], x["v"], x["lengths"], scale=w.scale, layout=w.layout)
+    compare(out, lse, ro, rl, w.layout)
 
 
 @pytest.fixture(scope="module")

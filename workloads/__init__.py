@@ -103,6 +103,12 @@ WORKLOADS: dict[str, Workload] = {
         "varlen_prefill", "prefill", B=16, Hq=32, Hkv=8, S_q=8192, S_kv=8192, D=128,
         layout="TND", causal=True, seed=108, len_lo=512, len_hi=8192, packed=True,
         note="16 packed sequences (TND), lengths ~U[512,8192], Hq=32 Hkv=8 D=128, causal"),
+    # Beyond the five: the GQA decode workload with head dim 256 (FlashAttn
+    # guide §3 tiling for D = 256).
+    "d256_decode": Workload(
+        "d256_decode", "decode", B=8, Hq=32, Hkv=8, S_q=1, S_kv=8192, D=256,
+        layout="BNSD", seed=109, len_lo=1024, len_hi=8192, garbage=True,
+        note="B=8 Hq=32 Hkv=8 D=256 BNSD, cache padded to 8192, L_b~U[1024,8192]"),
     # Beyond the five: the GQA decode workload with its cache paged (FlashAttn
     # guide §1.2, PA_BBND, 128-row blocks in shuffled order).
     "paged_decode": Workload(
