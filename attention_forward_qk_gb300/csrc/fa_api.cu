@@ -71,18 +71,19 @@ struct PrefillWs {
   size_t sched, varlen, lens, bits, total;
 };
 
-// Work items of a prefill launch: 256 query rows of one (batch, query head).
-int64_t prefill_items(int64_t B, int64_t S_q, int64_t num_heads) {
-  return B * num_heads * ceil_div(S_q, 256);
+// Work items of a prefill launch: 256 query rows (128 for D = 256) of one
+// (batch, query head).
+int64_t prefill_items(int64_t B, int64_t S_q, int64_t num_heads, int64_t D) {
+  return B * num_heads * ceil_div(S_q, prefill_item_rows(D));
 }
 
 // [status, item counter | pad][schedule: offsets of kMaxPrefillCtas + 1 CTAs,
 // then the item lists][packed-sequence table][lengths][per-tile key validity]
-PrefillWs prefill_ws(int64_t B, int64_t S_q, int64_t S_kv, int64_t num_heads) {
+PrefillWs prefill_ws(int64_t B, int64_t S_q, int64_t S_kv, int64_t num_heads, int64_t D) {
   PrefillWs w;
   size_t off = kAlign;  // status word
   w.sched = off;
-  off += align_up(sizeof(int32_t) * (kMaxPrefillCtas + 1 + prefill_items(B, S_q, num_heads)));
+  off += align_up(sizeof(int32_t) * (kMaxPrefillCtas + 1 + prefill_items(B, S_q, num_heads, D)));
   w.varlen = off;  // packed sequences only: [4][B] offsets and lengths
   off += align_up(sizeof(int32_t) * 4 * B);
   w.lens = off;
@@ -104,14 +105,15 @@ PrefillWs prefill_ws(int64_t B, int64_t S_q, int64_t S_kv, int64_t num_heads) {
 // tiles under the causal or window limits plus a constant for its start-up.
 // Layout: offsets[grid + 1] into the lists, then the item lists (int32).
 // lq, lkv: per-sequence lengths of packed sequences (else null); items past a
-// sequence's query rows do not exist and are not scheduled.
+// sequence's query rows do not exist and are not scheduled. IR: query rows
+// per item, BN: keys per KV tile (prefill_item_rows, prefill_kv_tile).
 void build_prefill_schedule(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t S_kv,
-                            int64_t win_left, int64_t win_right, int grid,
-                            std::vector<int32_t>& sched, const int32_t* lq = nullptr,
-                            const int32_t* lkv = nullptr) {
+                            int64_t win_left, int64_t win_right, int grid, int64_t IR,
+                            int64_t BN, std::vector<int32_t>& sched,
+                            const int32_t* lq = nullptr, const int32_t* lkv = nullptr) {
   const int64_t g = Hq / Hkv;
-  const int64_t nq = ceil_div(S_q, 256);
-  const int64_t n_tiles = ceil_div(std::max<int64_t>(S_kv, 1), 128);
+  const int64_t nq = ceil_div(S_q, IR);
+  const int64_t n_tiles = ceil_div(std::max<int64_t>(S_kv, 1), BN);
   const int64_t per_unit = nq * g;
   const int64_t units = B * Hkv;
   const int64_t n_items = units * per_unit;
@@ -120,19 +122,20 @@ void build_prefill_schedule(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int
     const int64_t qp = nq - 1 - (w % per_unit) / g;
     const int64_t b = (w / per_unit) / Hkv;
     const int64_t sq = lq ? lq[b] : S_q;
-    const int64_t nt = lkv ? ceil_div(static_cast<int64_t>(lkv[b]), 128) : n_tiles;
-    if (qp * 256 >= sq) return -1;
+    const int64_t nt = lkv ? ceil_div(static_cast<int64_t>(lkv[b]), BN) : n_tiles;
+    if (qp * IR >= sq) return -1;
     int64_t lo_u = nt, hi_u = 0;
-    for (int t = 0; t < 2; ++t) {
-      const int64_t r0 = qp * 256 + t * 128;
+    for (int64_t t = 0; t < IR / 128; ++t) {
+      const int64_t r0 = qp * IR + t * 128;
       if (t == 1 && r0 >= sq) break;
       int64_t lo = 0, hi = nt;
-      if (win_left >= 0) lo = std::max<int64_t>(0, r0 - win_left) / 128;
-      if (win_right >= 0) hi = std::min(hi, (r0 + 127 + win_right) / 128 + 1);
+      if (win_left >= 0) lo = std::max<int64_t>(0, r0 - win_left) / BN;
+      if (win_right >= 0) hi = std::min(hi, (r0 + 127 + win_right) / BN + 1);
       lo_u = std::min(lo_u, lo);
       hi_u = std::max(hi_u, hi);
     }
-    return std::max<int64_t>(0, hi_u - lo_u) + 3;
+    // KV tiles (of 128 keys' worth of work) plus a constant for the start-up
+    return std::max<int64_t>(0, hi_u - lo_u) * BN / 128 + 3;
   };
   std::vector<std::vector<int32_t>> lists(grid);
   // min-heap of (load, cta)
@@ -265,7 +268,7 @@ const char* fa_status_string(int s) {
     case FA_OK: return "FA_OK";
     case FA_ERR_NULLPTR: return "FA_ERR_NULLPTR: a required pointer is NULL";
     case FA_ERR_PARAM_INVALID: return "FA_ERR_PARAM_INVALID: argument outside the contract";
-    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be 64 or 128 (or 256 for decode)";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim must be 64, 128 or 256";
     case FA_ERR_WORKSPACE_TOO_SMALL: return "FA_ERR_WORKSPACE_TOO_SMALL";
     case FA_ERR_RUNTIME: return "FA_ERR_RUNTIME: a CUDA call failed";
     case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT: a kernel wait expired";
@@ -277,8 +280,7 @@ size_t fa_forward_workspace_size(int64_t B, int64_t S_q, int64_t S_kv, int64_t n
                                  int64_t num_kv_heads, int64_t D) {
   if (B < 0 || S_q < 0 || S_kv < 0 || num_heads < 0 || num_kv_heads < 0 || D < 0) return 0;
   (void)num_kv_heads;
-  (void)D;
-  return prefill_ws(B, S_q, S_kv, num_heads).total;
+  return prefill_ws(B, S_q, S_kv, num_heads, D).total;
 }
 
 namespace {
@@ -352,16 +354,16 @@ size_t fa_decode_workspace_size(int64_t B, int64_t S_kv_max, int64_t num_heads,
   return decode_ws(B, num_heads, D, max_slots_bound(S_kv_max, num_splits)).total;
 }
 
-// Head dims: 64 and 128 everywhere; 256 for decode as well.
+// Head dims: 64, 128 and 256.
 static fa_status check_common(int64_t B, int64_t S_q, int64_t S_kv, int64_t Hq, int64_t& Hkv,
-                              int64_t D, float scale, int layout, bool decode = false) {
+                              int64_t D, float scale, int layout) {
   if (Hkv == 0) Hkv = Hq;
   if (B < 0 || S_q < 0 || S_kv < 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return FA_ERR_PARAM_INVALID;
   if (Hq % Hkv != 0) return FA_ERR_PARAM_INVALID;
   if (layout != FA_LAYOUT_BNSD && layout != FA_LAYOUT_BSND) return FA_ERR_PARAM_INVALID;
   if (!isfinite(scale)) return FA_ERR_PARAM_INVALID;
   if (B > kMaxDim || S_q > kMaxDim || S_kv > kMaxDim || Hq > 65535) return FA_ERR_PARAM_INVALID;
-  if (D != 64 && D != 128 && !(decode && D == 256)) return FA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
@@ -398,7 +400,7 @@ fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok
   if (lens != nullptr)
     for (int64_t b = 0; b < B; ++b)
       if (lens[b] < 0 || lens[b] > S_kv) return FA_ERR_PARAM_INVALID;
-  const PrefillWs ws = prefill_ws(B, S_q, S_kv, num_heads);
+  const PrefillWs ws = prefill_ws(B, S_q, S_kv, num_heads, D);
   if (workspace_bytes < ws.total) return FA_ERR_WORKSPACE_TOO_SMALL;
   if (B == 0 || S_q == 0) return FA_OK;
 
@@ -406,21 +408,22 @@ fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok
   unsigned char* wsb = static_cast<unsigned char*>(workspace);
   const int sms = device_sm_count();
   if (sms <= 0) return FA_ERR_RUNTIME;
-  const int64_t n_items = prefill_items(B, S_q, num_heads);
+  const int64_t n_items = prefill_items(B, S_q, num_heads, D);
+  const int64_t IR = prefill_item_rows(D), BN = prefill_kv_tile(D);
   const int grid = static_cast<int>(
       std::min<int64_t>(std::min<int64_t>(n_items, sms), kMaxPrefillCtas));
   // the schedule depends on the shapes only; the last one is kept per thread
   struct SchedKey {
-    int64_t B, Hq, Hkv, S_q, S_kv, wl, wr;
+    int64_t B, Hq, Hkv, S_q, S_kv, wl, wr, D;
     int grid;
     bool operator==(const SchedKey& o) const {
       return B == o.B && Hq == o.Hq && Hkv == o.Hkv && S_q == o.S_q && S_kv == o.S_kv &&
-             wl == o.wl && wr == o.wr && grid == o.grid;
+             wl == o.wl && wr == o.wr && D == o.D && grid == o.grid;
     }
   };
-  thread_local SchedKey sched_key{-1, 0, 0, 0, 0, 0, 0, 0};
+  thread_local SchedKey sched_key{-1, 0, 0, 0, 0, 0, 0, 0, 0};
   thread_local std::vector<int32_t> sched;
-  const SchedKey key{B, num_heads, Hkv, S_q, S_kv, win_left, win_right, grid};
+  const SchedKey key{B, num_heads, Hkv, S_q, S_kv, win_left, win_right, D, grid};
   std::vector<int32_t> vtab;  // packed sequences: [4][B] q off, q len, kv off, kv len
   if (cu_q != nullptr) {
     vtab.resize(4 * B);
@@ -431,11 +434,12 @@ fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok
       vtab[3 * B + b] = static_cast<int32_t>(cu_kv[b + 1] - cu_kv[b]);
     }
     // depends on the lengths: built for every call
-    build_prefill_schedule(B, num_heads, Hkv, S_q, S_kv, win_left, win_right, grid, sched,
-                           vtab.data() + B, vtab.data() + 3 * B);
-    sched_key = SchedKey{-1, 0, 0, 0, 0, 0, 0, 0};
+    build_prefill_schedule(B, num_heads, Hkv, S_q, S_kv, win_left, win_right, grid, IR, BN,
+                           sched, vtab.data() + B, vtab.data() + 3 * B);
+    sched_key = SchedKey{-1, 0, 0, 0, 0, 0, 0, 0, 0};
   } else if (!(key == sched_key)) {
-    build_prefill_schedule(B, num_heads, Hkv, S_q, S_kv, win_left, win_right, grid, sched);
+    build_prefill_schedule(B, num_heads, Hkv, S_q, S_kv, win_left, win_right, grid, IR, BN,
+                           sched);
     sched_key = key;
   }
   // header: zeroed status word, the schedule, the packed-sequence table, then
@@ -560,7 +564,7 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
       lens == nullptr)
     return FA_ERR_NULLPTR;
   int64_t Hkv = num_kv_heads;
-  fa_status st = check_common(B, 1, S_kv_max, num_heads, Hkv, D, scale, layout, true);
+  fa_status st = check_common(B, 1, S_kv_max, num_heads, Hkv, D, scale, layout);
   if (st != FA_OK) return st;
   if (num_splits < 0) return FA_ERR_PARAM_INVALID;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||

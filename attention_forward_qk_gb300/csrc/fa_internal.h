@@ -24,6 +24,12 @@ inline int decode_heads_per_cta(int64_t g, int64_t D) {
   return (g % 4 == 0) ? 4 : (g % 2 == 0) ? 2 : 1;
 }
 
+// Prefill tiling: query rows of one work item (two 128-row tiles; one for
+// D = 256, whose O accumulator takes 256 TMEM columns) and keys per KV tile
+// (64 for D = 256, so that five K/V tiles and the Q tile fit shared memory).
+inline int prefill_item_rows(int64_t D) { return D == 256 ? 128 : 256; }
+inline int prefill_kv_tile(int64_t D) { return D == 256 ? 64 : 128; }
+
 // Decode stage height in rows, and the batch count up to which the length
 // prefix sums travel as launch parameters (larger batches use the workspace).
 constexpr int kDecodeStageRows = 112;

@@ -20,6 +20,9 @@
 //   warp 10    MMA issue stream of Q1 (the two streams take turns)
 //   warp 11    idle (it completes the third warpgroup for setmaxnreg)
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
+// D = 256 (FlashAttn guide §3's largest head dim): one 128-row Q tile per
+// work item (O0 takes [256,512)), 64-key KV tiles, warps 4-7 and the Q1
+// issue stream idle.
 // P_t (bf16, two per column) overwrites the first 64 columns of S_t and is
 // the A operand of O_t += P_t V_j straight from TMEM.
 // The MMA warp interleaves the two tiles (S0 S1 | PV0 S0' | PV1 S1' | ...)
@@ -42,7 +45,7 @@ namespace fa {
 namespace {
 
 constexpr int kBM = 128;        // query rows per Q tile
-constexpr int kBN = 128;        // keys per KV tile
+constexpr int kBitsTile = 128;  // keys per entry of the key-validity table
 constexpr int kRing = 5;        // K/V ring slots (tiles of K or V)
 constexpr int kThreads = 384;   // three warpgroups
 constexpr int kProducerWarp = 8;
@@ -54,16 +57,25 @@ constexpr int kSoftmaxRegs = 216;
 constexpr int kControlRegs = 72;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when m grows by > 2^8
 
+// D = 64, 128: two Q tiles per work item and 128-key KV tiles. D = 256: one
+// Q tile (its O accumulator takes 256 TMEM columns) and 64-key KV tiles, so
+// that the Q tile and five K/V tiles fit in shared memory.
 template <int D>
 struct PCfg {
-  static constexpr int kTileBytes = kBM * D * 2;  // one Q, K or V tile
-  static constexpr int kSubBytes = kBM * 128;     // one 64-column swizzle slab (16 KB)
+  static constexpr int QT = D == 256 ? 1 : 2;           // Q tiles per work item
+  static constexpr int BN = D == 256 ? 64 : 128;        // keys per KV tile
+  static constexpr int NQ4 = BN / 32;                   // 32-key groups of a KV tile
+  static constexpr int kQTileBytes = kBM * D * 2;       // one Q tile
+  static constexpr int kKvTileBytes = BN * D * 2;       // one K or V tile
+  static constexpr int kQSub = kBM * 128;               // a Q tile's 64-column swizzle slab
+  static constexpr int kKvSub = BN * 128;               // a K/V tile's 64-column slab
   static constexpr int kQOff = 0;
-  static constexpr int kRingOff = 2 * kTileBytes;
-  static constexpr int kBarOff = kRingOff + kRing * kTileBytes;
+  static constexpr int kRingOff = QT * kQTileBytes;
+  static constexpr int kBarOff = kRingOff + kRing * kKvTileBytes;
   // barriers + alignment slack; at least 116 KB so that two CTAs never share
   // an SM (each allocates all 512 TMEM columns)
   static constexpr int kSmemBytes = (kBarOff + 256 + 1024) > 118784 ? (kBarOff + 256 + 1024) : 118784;
+  static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
 struct PrefillArgs {
@@ -78,7 +90,7 @@ struct PrefillArgs {
   uint64_t timeout_ns;
   int B, Hq, Hkv, S_q, S_kv;
   int win_left, win_right;    // key j is seen by query i iff i - wl <= j <= i + wr; -1 = no limit
-  int n_qpairs, n_kv_tiles, n_items;
+  int n_qpairs, n_kv_tiles, n_items;  // work items per (batch, head), KV tiles, all items
   long long out_row_stride, out_head_stride, out_batch_stride;  // elements
   float scale_log2;
 };
@@ -98,30 +110,41 @@ enum : int {
   kNumBars = kBarDrain + 2
 };
 
+// KV tiles of BN keys; with BN = 64 a tile is half an entry of the 128-key
+// validity table.
+template <int BN>
 struct TileSeq {
+  static constexpr bool half = BN == 64;
   const uint32_t* bits;  // this batch's rows of the tile table, or null
   int begin;             // first KV tile any Q tile of the item needs
   int end;               // one past the last KV tile any Q tile of the item needs
+  // validity words of KV tile j (4 for 128 keys, the first 2 used for 64)
+  __device__ __forceinline__ uint4 words(int j) const {
+    if constexpr (!half) return __ldg(reinterpret_cast<const uint4*>(bits) + j);
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(bits) + j);
+    return make_uint4(w.x, w.y, 0u, 0u);
+  }
   __device__ __forceinline__ int next(int j) const {
     for (j = max(j, begin); j < end; ++j) {
       if (bits == nullptr) return j;
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(bits) + j);
+      const uint4 w = words(j);
       if ((w.x | w.y | w.z | w.w) != 0u) return j;
     }
     return end;
   }
   __device__ __forceinline__ bool full(int j) const {
     if (bits == nullptr) return true;
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(bits) + j);
-    return (w.x & w.y & w.z & w.w) == 0xFFFFFFFFu;
+    const uint4 w = words(j);
+    return half ? (w.x & w.y) == 0xFFFFFFFFu : (w.x & w.y & w.z & w.w) == 0xFFFFFFFFu;
   }
 };
 
-// One work item: 256 consecutive query rows (two 128-row tiles) of one
-// (batch, query head). Items are numbered KV-head-major: all query pairs of
+// One work item: 256 consecutive query rows (two 128-row tiles; 128 rows,
+// one tile, for D = 256) of one (batch, query head). Items are numbered KV-head-major: all query pairs of
 // the g query heads of one (batch, KV head) are consecutive, heaviest (last)
 // pairs first and heads innermost, so the items in flight at any time read
 // the same K/V tiles out of L2.
+template <int D>
 struct WorkItem {
   int b, kvh, h, q_row0;
   int S_q, S_kv, n_kv;   // this sequence's query rows, keys and KV tiles
@@ -129,11 +152,14 @@ struct WorkItem {
   int tma_b;             // batch coordinate of its tiles (0 when packed)
   bool has_t1;
   int lo_t[2], n_t[2];  // KV tiles [lo_t, n_t) each Q tile needs
-  TileSeq seq;
+  TileSeq<PCfg<D>::BN> seq;
 };
 
-__device__ __forceinline__ WorkItem work_item(const PrefillArgs& a, int w) {
-  WorkItem it;
+template <int D>
+__device__ __forceinline__ WorkItem<D> work_item(const PrefillArgs& a, int w) {
+  using C = PCfg<D>;
+  constexpr int kBN = C::BN;
+  WorkItem<D> it;
   const int g = a.Hq / a.Hkv;
   const int per_kv = a.n_qpairs * g;
   const int bkv = w / per_kv;
@@ -142,7 +168,7 @@ __device__ __forceinline__ WorkItem work_item(const PrefillArgs& a, int w) {
   it.b = bkv / a.Hkv;
   it.kvh = bkv % a.Hkv;
   it.h = it.kvh * g + rem % g;
-  it.q_row0 = qp * 2 * kBM;
+  it.q_row0 = qp * C::QT * kBM;
   if (a.varlen != nullptr) {
     it.q_base = __ldg(a.varlen + it.b);
     it.S_q = __ldg(a.varlen + a.B + it.b);
@@ -158,7 +184,7 @@ __device__ __forceinline__ WorkItem work_item(const PrefillArgs& a, int w) {
     it.n_kv = a.n_kv_tiles;
     it.tma_b = it.b;
   }
-  it.has_t1 = it.q_row0 + kBM < it.S_q;
+  it.has_t1 = C::QT == 2 && it.q_row0 + kBM < it.S_q;
   for (int t = 0; t < 2; ++t) {
     // rows r0 .. r0+127 see keys r0 - wl .. r0 + 127 + wr (window, causal = (-1, 0))
     const int r0 = it.q_row0 + t * kBM;
@@ -169,7 +195,12 @@ __device__ __forceinline__ WorkItem work_item(const PrefillArgs& a, int w) {
     it.lo_t[t] = min(lo, n);
     it.n_t[t] = n;
   }
-  it.seq.bits = a.tile_bits ? a.tile_bits + static_cast<size_t>(it.b) * a.n_kv_tiles * 4 : nullptr;
+  // the validity table has one entry per 128 keys of the padded sequence
+  // (no table for packed sequences)
+  constexpr int kPerEntry = kBitsTile / kBN;
+  it.seq.bits = a.tile_bits ? a.tile_bits + static_cast<size_t>(it.b) *
+                                                ((a.n_kv_tiles + kPerEntry - 1) / kPerEntry) * 4
+                            : nullptr;
   // the union of the two ranges (contiguous: the second tile's range is the
   // first one shifted by one tile)
   it.seq.begin = it.n_t[1] > it.lo_t[1] ? min(it.lo_t[0], it.lo_t[1]) : it.lo_t[0];
@@ -182,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
   using C = PCfg<D>;
+  constexpr int kBN = C::BN;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -245,9 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; ok; ++r) {
       const int w = item_of(r);
       if (w >= a.n_items) break;
-      const WorkItem wi = work_item(a, w);
+      const WorkItem<D> wi = work_item<D>(a, w);
       const int kvh = wi.kvh;
-      const TileSeq& seq = wi.seq;
+      const auto& seq = wi.seq;
       if (r > 0) {
         // the Q region is free once both streams' S products of the last item are done
         ok = mbar_wait(bar(kBarQFree), (r - 1) & 1, a.timeout_ns, a.status, kDevTimeoutQ,
@@ -257,10 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (lane == 0) {
         const int nq = wi.has_t1 ? 2 : 1;
-        mbar_expect_tx(bar(kBarQ), nq * C::kTileBytes);
+        mbar_expect_tx(bar(kBarQ), nq * C::kQTileBytes);
         for (int t = 0; t < nq; ++t)
           for (int s = 0; s < D / 64; ++s)
-            tma_load_4d(smem_u32(smem + C::kQOff + t * C::kTileBytes + s * C::kSubBytes), &tm_q,
+            tma_load_4d(smem_u32(smem + C::kQOff + t * C::kQTileBytes + s * C::kQSub), &tm_q,
                         bar(kBarQ), s * 64, wi.q_base + wi.q_row0 + t * kBM, wi.h, wi.tma_b);
       }
       __syncwarp();
@@ -275,14 +307,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
         }
-        const uint32_t dst = smem_u32(smem + C::kRingOff + slot * C::kTileBytes);
+        const uint32_t dst = smem_u32(smem + C::kRingOff + slot * C::kKvTileBytes);
         const CUtensorMap* map = kv == 0 ? &tm_k : &tm_v;
         if (kv == 1 && fix_v) {
           // land V on the side barrier, zero the rows of excluded keys, publish
           if (lane == 0) {
-            mbar_expect_tx(bar(kBarFix), C::kTileBytes);
+            mbar_expect_tx(bar(kBarFix), C::kKvTileBytes);
             for (int s = 0; s < D / 64; ++s)
-              tma_load_4d(dst + s * C::kSubBytes, map, bar(kBarFix), s * 64,
+              tma_load_4d(dst + s * C::kKvSub, map, bar(kBarFix), s * 64,
                           wi.kv_base + j * kBN, kvh, wi.tma_b);
           }
           ++item;
@@ -291,9 +323,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __all_sync(0xffffffffu, ok);
           ++fixes;
           if (!ok) break;
-          const uint4 w = __ldg(reinterpret_cast<const uint4*>(seq.bits) + j);
-          uint4* tile = reinterpret_cast<uint4*>(smem + C::kRingOff + slot * C::kTileBytes);
-          // 128 rows x (D/64 slabs) x 8 chunks of 16 B; a row of a slab is 128
+          const uint4 w = seq.words(j);
+          uint4* tile = reinterpret_cast<uint4*>(smem + C::kRingOff + slot * C::kKvTileBytes);
+          // kBN rows x (D/64 slabs) x 8 chunks of 16 B; a row of a slab is 128
           // contiguous bytes whatever the swizzle
           for (int idx = lane; idx < kBN * (D / 64) * 8; idx += 32) {
             const int r = idx / ((D / 64) * 8);
@@ -301,16 +333,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = rest / 8, ch = rest % 8;
             const uint32_t word = r < 64 ? (r < 32 ? w.x : w.y) : (r < 96 ? w.z : w.w);
             if (((word >> (r & 31)) & 1u) == 0u)
-              tile[(s * C::kSubBytes + r * 128) / 16 + ch] = make_uint4(0u, 0u, 0u, 0u);
+              tile[(s * C::kKvSub + r * 128) / 16 + ch] = make_uint4(0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kBarKvFull + slot));
         } else {
           if (lane == 0) {
-            mbar_expect_tx(bar(kBarKvFull + slot), C::kTileBytes);
+            mbar_expect_tx(bar(kBarKvFull + slot), C::kKvTileBytes);
             for (int s = 0; s < D / 64; ++s)
-              tma_load_4d(dst + s * C::kSubBytes, map, bar(kBarKvFull + slot), s * 64,
+              tma_load_4d(dst + s * C::kKvSub, map, bar(kBarKvFull + slot), s * 64,
                           wi.kv_base + j * kBN, kvh, wi.tma_b);
           }
           ++item;
@@ -360,20 +392,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Descriptor bases built once; an MMA adds a constant to the 14-bit
       // address field (addresses stay below 256 KB, so the add never carries
       // out of the field). K-major tiles advance 32 B per 16-element k-step
-      // inside a 128-byte swizzle row and 16 KB per 64-column slab; the
-      // MN-major V operand advances 16 keys = 2 KB per k-step.
-      const uint64_t dq = smem_desc_sw128(q_base + t * C::kTileBytes, 16, 1024);
+      // inside a 128-byte swizzle row and one slab (kBM or kBN rows of 128 B)
+      // per 64 columns; the MN-major V operand advances 16 keys = 2 KB per
+      // k-step.
+      const uint64_t dq = smem_desc_sw128(q_base + t * C::kQTileBytes, 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(ring_base, 16, 1024);
-      const uint64_t dv0 = smem_desc_sw128(ring_base, C::kSubBytes, 1024);
-      constexpr uint32_t kSlotStep = C::kTileBytes >> 4;
+      const uint64_t dv0 = smem_desc_sw128(ring_base, C::kKvSub, 1024);
+      constexpr uint32_t kSlotStep = C::kKvTileBytes >> 4;
       const uint32_t s_tmem = tmem + t * 128;
       const uint32_t o_tmem = tmem + 256 + t * 128;
       auto issue_s = [&](int slot) {
         const uint64_t bk = dk0 + static_cast<uint64_t>(slot) * kSlotStep;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk / 4) * C::kSubBytes + (kk % 4) * 32) >> 4;
-          umma_ss(s_tmem, dq + off, bk + off, idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t offq = ((kk / 4) * C::kQSub + (kk % 4) * 32) >> 4;
+          const uint32_t offk =
+              C::kQSub == C::kKvSub ? offq : ((kk / 4) * C::kKvSub + (kk % 4) * 32) >> 4;
+          umma_ss(s_tmem, dq + offq, bk + offk, idesc_s, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int slot, bool first) {
@@ -404,8 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; ok; ++r) {
         const int w = item_of(r);
         if (w >= a.n_items) break;
-        const WorkItem wi = work_item(a, w);
-        const TileSeq& seq = wi.seq;
+        const WorkItem<D> wi = work_item<D>(a, w);
+        const auto& seq = wi.seq;
         // this stream's KV tiles: those of the item's sequence in [lo, n)
         const int lo = t == 0 ? wi.lo_t[0] : wi.lo_t[1];
         const int n = t == 0 ? wi.n_t[0] : wi.n_t[1];
@@ -493,11 +528,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c = a.scale_log2;
     int k = 0;  // S_t tiles consumed so far (all work items)
     bool ok = true;
-    for (int r = 0; ok; ++r) {
+    // with one Q tile per item (D = 256) the second warpgroup has no rows
+    for (int r = 0; ok && (C::QT == 2 || t == 0); ++r) {
       const int w = item_of(r);
       if (w >= a.n_items) break;
-      const WorkItem wi = work_item(a, w);
-      const TileSeq& seq = wi.seq;
+      const WorkItem<D> wi = work_item<D>(a, w);
+      const auto& seq = wi.seq;
       const int q_row0 = wi.q_row0;
       const int row = q_row0 + t * kBM + row_in_tile;
       float m_run = -INFINITY;  // reference max, log2 domain
@@ -510,7 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[4][32];
+      constexpr int NQ4 = C::NQ4;
+      uint32_t sr[NQ4][32];
       // per-element path: masked tiles, and a negative scale (whose row max is
       // the scale times the row min)
       const int r0 = q_row0 + t * kBM;
@@ -520,11 +557,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       float tmax = -INFINITY;
       if (masked) {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(s_tmem + q4 * 32, sr[q4]);
+        for (int q4 = 0; q4 < NQ4; ++q4) tmem_ld32(s_tmem + q4 * 32, sr[q4]);
         tmem_ld_wait();
         uint32_t words[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
         if (seq.bits != nullptr) {
-          const uint4 w = __ldg(reinterpret_cast<const uint4*>(seq.bits) + j);
+          const uint4 w = seq.words(j);
           words[0] = w.x; words[1] = w.y; words[2] = w.z; words[3] = w.w;
         }
         // this row's keys of the tile, [lo_k, hi_k) relative to its first key:
@@ -536,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (a.win_right >= 0) hi_k = min(hi_k, row + a.win_right + 1 - base);
           const int lo_k = a.win_left >= 0 ? row - a.win_left - base : 0;
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
+          for (int q4 = 0; q4 < NQ4; ++q4) {
             const int lo_i = min(max(lo_k - q4 * 32, 0), 32);
             const int hi_i = min(max(hi_k - q4 * 32, 0), 32);
             const uint32_t below_hi = hi_i >= 32 ? 0xFFFFFFFFu : ((1u << hi_i) - 1u);
@@ -546,16 +583,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < NQ4; ++q4) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const bool valid = (words[q4] >> i) & 1u;
             const float tv = valid ? __uint_as_float(sr[q4][i]) * c : -INFINITY;
             sr[q4][i] = __float_as_uint(tv);
-            mx[q4] = fmaxf(mx[q4], tv);
+            mx[q4 % 4] = fmaxf(mx[q4 % 4], tv);
           }
         }
         tmax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      } else if constexpr (NQ4 == 2) {
+        // 64 keys: both halves in one round of TMEM loads
+        float mx[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+        tmem_ld32(s_tmem, sr[0]);
+        tmem_ld32(s_tmem + 32, sr[NQ4 - 1]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q4 = 0; q4 < NQ4; ++q4)
+#pragma unroll
+          for (int i = 0; i < 32; i += 2)
+            mx[(q4 * 16 + i / 2) % 8] = fmax3(mx[(q4 * 16 + i / 2) % 8], __uint_as_float(sr[q4][i]),
+                                              __uint_as_float(sr[q4][i + 1]));
+        tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * c;
       } else {
         // row max with 8 independent accumulators; the first half's max runs
         // while the second half is still being read out of TMEM
@@ -596,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t c2 = masked ? pair_f32(1.f, 1.f) : pair_f32(c, c);
       const uint64_t nm2 = pair_f32(-m_use, -m_use);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      for (int half = 0; half < NQ4 / 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq) {
@@ -639,34 +691,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      // the whole O row in one round of TMEM loads, then O_t is free for the
-      // next item's products
-      uint32_t orr[D / 32][32];
+      // the O row in rounds of up to 128 columns of TMEM loads (one round
+      // unless D = 256); O_t is free for the next item's products as soon as
+      // the last round is read
+      constexpr int kRound = D < 128 ? D / 32 : D == 256 ? 2 : 4;
+      uint32_t orr[kRound][32];
 #pragma unroll
-      for (int q4 = 0; q4 < D / 32; ++q4) tmem_ld32(o_tmem + q4 * 32, orr[q4]);
+      for (int q4 = 0; q4 < kRound; ++q4) tmem_ld32(o_tmem + q4 * 32, orr[q4]);
       tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(bar(kBarODrained + t));
+      if (kRound == D / 32) {
+        tc_fence_before();
+        mbar_arrive(bar(kBarODrained + t));
+      }
       const bool row_ok = row < wi.S_q;
       const bool invalid = (l_run == 0.f);
       const float inv_l = invalid ? 0.f : 1.f / l_run;
       __nv_bfloat16* dst = a.out + static_cast<long long>(wi.tma_b) * a.out_batch_stride +
                            static_cast<long long>(wi.h) * a.out_head_stride +
                            static_cast<long long>(wi.q_base + row) * a.out_row_stride;
-      if (row_ok) {
 #pragma unroll
-        for (int q4 = 0; q4 < D / 32; ++q4) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + q4 * 32);
-          // an invalid row writes exact zeros: its O columns may never have
-          // been written by an MMA
+      for (int q0 = 0; q0 < D / 32; q0 += kRound) {
+        if (q0 > 0) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
-            float f[8];
+          for (int q4 = 0; q4 < kRound; ++q4) tmem_ld32(o_tmem + (q0 + q4) * 32, orr[q4]);
+          tmem_ld_wait();
+          if (q0 + kRound == D / 32) {
+            tc_fence_before();
+            mbar_arrive(bar(kBarODrained + t));
+          }
+        }
+        if (row_ok) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              f[e] = invalid ? 0.f : __uint_as_float(orr[q4][i + e]) * inv_l;
-            d4[i / 8] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                                   pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+          for (int q4 = 0; q4 < kRound; ++q4) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + (q0 + q4) * 32);
+            // an invalid row writes exact zeros: its O columns may never have
+            // been written by an MMA
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                f[e] = invalid ? 0.f : __uint_as_float(orr[q4][i + e]) * inv_l;
+              d4[i / 8] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                     pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+            }
           }
         }
       }
@@ -699,7 +767,7 @@ __global__ void tile_bits_kernel(const uint8_t* __restrict__ key_mask, const int
                                  int S_kv, int n_tiles, uint32_t* __restrict__ bits) {
   const int tile = blockIdx.x;
   const int b = blockIdx.y;
-  const int key = tile * kBN + threadIdx.x;
+  const int key = tile * kBitsTile + threadIdx.x;
   bool valid = key < S_kv;
   if (valid && lens != nullptr) valid = key < lens[b];
   if (valid && key_mask != nullptr) valid = key_mask[static_cast<size_t>(b) * S_kv + key] == 0;
@@ -723,6 +791,7 @@ __global__ void wait_probe_kernel(uint32_t* status, uint64_t timeout_ns) {
 template <int D>
 cudaError_t launch_prefill_d(const PrefillLaunch& x, cudaStream_t stream) {
   using C = PCfg<D>;
+  constexpr int kBN = C::BN;
   static bool configured = false;  // benign race: idempotent attribute set
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
@@ -759,7 +828,7 @@ cudaError_t launch_prefill_d(const PrefillLaunch& x, cudaStream_t stream) {
   pa.S_kv = x.S_kv;
   pa.win_left = x.win_left;
   pa.win_right = x.win_right;
-  pa.n_qpairs = (x.S_q + 2 * kBM - 1) / (2 * kBM);
+  pa.n_qpairs = (x.S_q + C::QT * kBM - 1) / (C::QT * kBM);
   pa.n_kv_tiles = (x.S_kv + kBN - 1) / kBN;
   pa.n_items = pa.n_qpairs * x.B * x.Hq;
   if (x.layout == FA_LAYOUT_BNSD) {
@@ -781,13 +850,16 @@ cudaError_t launch_prefill_d(const PrefillLaunch& x, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillLaunch& x, cudaStream_t stream) {
-  return x.D == 128 ? launch_prefill_d<128>(x, stream) : launch_prefill_d<64>(x, stream);
+  return x.D == 256   ? launch_prefill_d<256>(x, stream)
+         : x.D == 128 ? launch_prefill_d<128>(x, stream)
+                      : launch_prefill_d<64>(x, stream);
 }
 
 cudaError_t launch_tile_bits(const uint8_t* key_mask, const int* lens_dev, int B, int S_kv,
                              uint32_t* bits, cudaStream_t stream) {
-  const int n_tiles = (S_kv + kBN - 1) / kBN;
-  tile_bits_kernel<<<dim3(n_tiles, B), kBN, 0, stream>>>(key_mask, lens_dev, S_kv, n_tiles, bits);
+  const int n_tiles = (S_kv + kBitsTile - 1) / kBitsTile;
+  tile_bits_kernel<<<dim3(n_tiles, B), kBitsTile, 0, stream>>>(key_mask, lens_dev, S_kv, n_tiles,
+                                                               bits);
   return cudaGetLastError();
 }
 

@@ -525,8 +525,8 @@ def run_gpu(args):
     others = {}
     if not args.only:
         for name in ("long_decode", "causal_prefill", "gqa_masked_prefill", "tiny_prefill",
-                     "window_prefill", "varlen_prefill", "paged_decode", "d256_decode",
-                     "gqa_decode"):
+                     "window_prefill", "varlen_prefill", "d256_prefill", "paged_decode",
+                     "d256_decode", "gqa_decode"):
             if name == args.workload:
                 continue
             wo = workloads.WORKLOADS[name]

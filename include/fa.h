@@ -37,8 +37,8 @@
  *     (aclnnIncreFlashAttention guide §四 actualSeqLengths and §1.1).
  *   - A query row with no valid key gets out = 0 and lse = +inf (FlashAttn
  *     guide §1.7, row invalid).
- *   - Head dimension D must be 64 or 128; decode (fa_decode, fa_decode_paged,
- *     fa_decode_noalloc) also takes 256.
+ *   - Head dimension D must be 64, 128 or 256 (FlashAttn guide §3 lists
+ *     D in {64, 128, 256}).
  *   - Two-stage use as in aclnnIncreFlashAttention guide §三: ask for the
  *     workspace size, allocate it on the device, then call. The caller owns
  *     every buffer; the library allocates no device memory and keeps no
@@ -68,8 +68,7 @@ typedef enum {
   FA_OK = 0,
   FA_ERR_NULLPTR = 1,             /* a required pointer is NULL */
   FA_ERR_PARAM_INVALID = 2,       /* a size, layout, mode or length is outside the contract */
-  FA_ERR_UNSUPPORTED = 3,         /* allowed by the pages but not built here (D not 64/128, or
-                                     256 outside decode) */
+  FA_ERR_UNSUPPORTED = 3,         /* allowed by the pages but not built here (D not 64/128/256) */
   FA_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes below the size query's answer */
   FA_ERR_RUNTIME = 5,             /* a CUDA call failed (launch, copy, device query) */
   FA_ERR_DEVICE_TIMEOUT = 6       /* a kernel's bounded wait expired; outputs are undefined */

@@ -95,7 +95,7 @@ def _dec(lib, **kw):
     (dict(ws=None), _lib.FA_ERR_NULLPTR),
     (dict(Hq=3, Hkv=2), _lib.FA_ERR_PARAM_INVALID),
     (dict(D=96), _lib.FA_ERR_UNSUPPORTED),
-    (dict(D=256), _lib.FA_ERR_UNSUPPORTED),
+    (dict(D=512), _lib.FA_ERR_UNSUPPORTED),
     (dict(layout=2), _lib.FA_ERR_PARAM_INVALID),
     (dict(mask_mode=4), _lib.FA_ERR_PARAM_INVALID),
     (dict(mask_mode=3, S_q=64, S_kv=128), _lib.FA_ERR_PARAM_INVALID),
@@ -164,14 +164,23 @@ def test_decode_zero_batch_is_noop(lib):
     assert _dec(lib, B=0, lens=[]) == _lib.FA_OK
 
 
-def test_head_dim_256_is_a_decode_only_extension(lib):
-    # decode takes D = 256 (the plan and the size query too); prefill does not
+def test_head_dim_256_is_accepted(lib):
+    # D = 256 for decode (the plan and the size query too) and for prefill
     assert _dec(lib, D=256, B=0, lens=[]) == _lib.FA_OK
     assert _dec(lib, D=192, B=0, lens=[]) == _lib.FA_ERR_UNSUPPORTED
     assert F.fa_decode_workspace_size(2, 4096, 16, 4, 256, 0) > 0
     rc, n, mx = _plan([4096, 100], 4096, 16, 4, D=256)
     assert rc >= 224 and n >= 1 and mx >= 1
-    assert _fwd(lib, D=256) == _lib.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, D=256, B=0) == _lib.FA_OK
+    assert _fwd(lib, D=192, B=0) == _lib.FA_ERR_UNSUPPORTED
+
+
+def test_prefill_workspace_counts_work_items_of_the_head_dim():
+    # D = 256 items are 128 query rows (one Q tile), others 256: the schedule
+    # part of the workspace holds twice as many items
+    w128 = F.fa_forward_workspace_size(2, 4096, 4096, 16, 16, 128)
+    w256 = F.fa_forward_workspace_size(2, 4096, 4096, 16, 16, 256)
+    assert w256 - w128 == 4 * 2 * 16 * (4096 // 128 - 4096 // 256)
 
 
 def _plan(lens, S, Hq, Hkv, sms=152, splits=0, D=128):

@@ -74,6 +74,11 @@ PREFILL_CASES = [
     (2, 8, 1, 512, 512, 128, "BNSD", False, 700, None),
     (1, 4, 4, 1000, 1000, 128, "BSND", True, None, [999]),
     (2, 2, 2, 129, 129, 64, "BSND", True, 128, None),
+    # head dim 256: one 128-row Q tile per work item, 64-key KV tiles
+    (1, 2, 2, 300, 300, 256, "BNSD", False, None, None),
+    (2, 4, 2, 520, 520, 256, "BSND", True, None, None),
+    (2, 8, 2, 384, 384, 256, "BNSD", True, 200, None),
+    (2, 2, 1, 200, 333, 256, "BSND", False, 100, [333, 64]),
 ]
 
 
@@ -137,7 +142,8 @@ def _sample_rows(S, pads, seed, n=24):
     return sorted(rows)
 
 
-@pytest.mark.parametrize("name", ["tiny_prefill", "causal_prefill", "gqa_masked_prefill"])
+@pytest.mark.parametrize("name", ["tiny_prefill", "causal_prefill", "gqa_masked_prefill",
+                                  "d256_prefill"])
 def test_prefill_workloads(cuda_device, name):
     w = workloads.WORKLOADS[name]
     x = workloads.make(w)

@@ -48,6 +48,8 @@ CASES = [
     ([300, 5], [0, 17], 2, 2, 128, False),
     ([1000], [1000], 8, 2, 128, True),
     ([255, 256, 257, 511, 512, 513], [255, 256, 257, 511, 512, 513], 4, 4, 64, True),
+    ([100, 300, 1, 257], [100, 300, 1, 257], 4, 2, 256, True),
+    ([50, 700, 129], [200, 30, 1000], 2, 1, 256, False),
 ]
 
 

@@ -26,6 +26,8 @@ CASES = [
     (1, 4, 4, 384, 128, "BNSD", (1000, 1000), None, None),
     (1, 2, 2, 257, 128, "BNSD", (300, -1), None, None),
     (2, 4, 4, 129, 64, "BSND", (5, 300), 64, None),
+    (1, 4, 2, 600, 256, "BNSD", (100, 30), None, None),
+    (2, 2, 2, 300, 256, "BSND", (63, 0), 40, None),
 ]
 
 

@@ -91,6 +91,12 @@ WORKLOADS: dict[str, Workload] = {
         "gqa_masked_prefill", "prefill", B=2, Hq=64, Hkv=8, S_q=8192, S_kv=8192, D=128,
         layout="BNSD", causal=True, seed=105, max_pad=1024,
         note="B=2 Hq=64 Hkv=8 S=8192 D=128 BNSD causal AND key padding p_b~U[0,1024]"),
+    # Beyond the five: causal GQA prefill with head dim 256 (FlashAttn guide
+    # §3 tiling for D = 256).
+    "d256_prefill": Workload(
+        "d256_prefill", "prefill", B=4, Hq=16, Hkv=8, S_q=4096, S_kv=4096, D=256,
+        layout="BSND", causal=True, seed=110,
+        note="B=4 Hq=16 Hkv=8 S=4096 D=256 BSND causal"),
     # Beyond the five: the sliding-window mask (FlashAttn guide §1.5, mode 4)
     # on a long GQA prefill, each query seeing itself and the 1023 keys before.
     "window_prefill": Workload(
