@@ -51,10 +51,8 @@ constexpr int kThreads = 384;   // three warpgroups
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;     // MMA issue for Q0 (warp 10 for Q1); warp 11 idle
 // Register split (setmaxnreg): the launch gives 168 per thread (384 x 168 =
-// 64512); the softmax warpgroups take 216 each and the load/MMA warpgroup 72:
-// 128 x (216 + 216 + 72) = 64512.
-constexpr int kSoftmaxRegs = 216;
-constexpr int kControlRegs = 72;
+// 64512), shared out between the two softmax warpgroups and the load/MMA
+// warpgroup (PCfg::kSoftmaxRegs, kControlRegs).
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only when m grows by > 2^8
 
 // D = 64, 128: two Q tiles per work item and 128-key KV tiles. D = 256: one
@@ -76,6 +74,12 @@ struct PCfg {
   // an SM (each allocates all 512 TMEM columns)
   static constexpr int kSmemBytes = (kBarOff + 256 + 1024) > 118784 ? (kBarOff + 256 + 1024) : 118784;
   static_assert(kSmemBytes <= 232448, "shared memory");
+  // register split (setmaxnreg) of the softmax and load/MMA warpgroups; the
+  // D = 256 issue stream keeps 16 more registers:
+  // 128 x (216 + 216 + 72) = 128 x (208 + 208 + 88) = 64512
+  static constexpr int kSoftmaxRegs = D == 256 ? 208 : 216;
+  static constexpr int kControlRegs = D == 256 ? 88 : 72;
+  static_assert(2 * kSoftmaxRegs + kControlRegs == 504, "register split");
 };
 
 struct PrefillArgs {
@@ -261,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp >= 8) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kControlRegs));
   if (warp == kProducerWarp) {
     // ================================================================ TMA
     // Every lane waits on the same barriers and the warp votes on the result,
@@ -432,6 +436,101 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
+      if constexpr (C::QT == 1) {
+        // One Q tile per item (D = 256): a single issue stream with the S tile
+        // double-buffered in TMEM (buffers [0, kBN) and [kBN, 2 kBN), by KV tile
+        // parity). S of tile g+2 goes into the buffer of tile g right behind
+        // PV of tile g, so the softmax of tile g+1 runs while the tensor core
+        // does PV(g) and S(g+2). kBarSFull/kBarPReady + buffer hand the tiles
+        // over; kBarOFinal + 1 completes once per P·V (the softmax waits on it
+        // before it rescales O). The second issue warp has no work.
+        if (t == 0) {
+          int item = 0;  // ring items consumed so far
+          int g = 0;     // KV tiles processed so far (all work items)
+          bool ok = true;
+          for (int r = 0; ok; ++r) {
+            const int w = item_of(r);
+            if (w >= a.n_items) break;
+            const WorkItem<D> wi = work_item<D>(a, w);
+            const auto& seq = wi.seq;
+            ok = mbar_wait(bar(kBarQ), r & 1, a.timeout_ns, a.status, kDevTimeoutQ, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            int js = seq.next(0);  // next tile whose S is issued
+            int jp = js;           // next tile whose P·V is issued
+            int n_s = 0, n_p = 0;  // S and P·V products of this item so far
+            auto issue_next_s = [&]() -> bool {
+              const int it_k = item + 2 * n_s;  // ring items go K, V, K, V, ...
+              const int slot = it_k % kRing;
+              if (!mbar_wait(bar(kBarKvFull + slot), (it_k / kRing) & 1, a.timeout_ns, a.status,
+                             kDevTimeoutKvFull, abort_flag))
+                return false;
+              tc_fence_after();
+              const int b = (g + n_s) & 1;
+              const uint64_t bk = dk0 + static_cast<uint64_t>(slot) * kSlotStep;
+              // the 16 Q descriptors are recomputed per tile, not kept live
+              // (they would take 32 of this warp's 72 registers)
+              uint64_t dqv = dq;
+              asm volatile("" : "+l"(dqv));
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t offq = ((kk / 4) * C::kQSub + (kk % 4) * 32) >> 4;
+                const uint32_t offk = ((kk / 4) * C::kKvSub + (kk % 4) * 32) >> 4;
+                umma_ss(tmem + b * kBN, dqv + offq, bk + offk, idesc_s, kk > 0 ? 1u : 0u);
+              }
+              umma_commit(bar(kBarSFull + b));
+              umma_commit(bar(kBarKvEmpty + slot));  // the slot counts two releases
+              umma_commit(bar(kBarKvEmpty + slot));
+              ++n_s;
+              js = seq.next(js + 1);
+              if (!(js < seq.end)) {  // Q is free once the item's last S is issued
+                umma_commit(bar(kBarQFree));
+                umma_commit(bar(kBarQFree));
+              }
+              return true;
+            };
+            if (!(js < seq.end)) {
+              // the item sees no key
+              umma_commit(bar(kBarQFree));
+              umma_commit(bar(kBarQFree));
+              umma_commit(bar(kBarOFinal));
+              continue;
+            }
+            ok = issue_next_s();
+            if (ok && js < seq.end) ok = issue_next_s();
+            while (ok && jp < seq.end) {
+              const int b = (g + n_p) & 1;
+              const int iv = item + 2 * n_p + 1;
+              const int v_slot = iv % kRing;
+              ok = mbar_wait(bar(kBarKvFull + v_slot), (iv / kRing) & 1, a.timeout_ns, a.status,
+                             kDevTimeoutKvFull, abort_flag);
+              if (ok)
+                ok = mbar_wait(bar(kBarPReady + b), ((g + n_p) >> 1) & 1, a.timeout_ns, a.status,
+                               kDevTimeoutPReady, abort_flag);
+              if (ok && n_p == 0 && r > 0)
+                // O of the previous item must be read out before it is overwritten
+                ok = mbar_wait(bar(kBarODrained), (r - 1) & 1, a.timeout_ns, a.status,
+                               kDevTimeoutOFinal, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              const uint64_t bv = dv0 + static_cast<uint64_t>(v_slot) * kSlotStep;
+#pragma unroll
+              for (int kk = 0; kk < kBN / 16; ++kk)
+                umma_ts(o_tmem, tmem + b * kBN + kk * 8, bv + ((kk * 16 * 128) >> 4), idesc_pv,
+                        (n_p == 0 && kk == 0) ? 0u : 1u);
+              umma_commit(bar(kBarOFinal + 1));  // this P·V is done
+              umma_commit(bar(kBarKvEmpty + v_slot));
+              umma_commit(bar(kBarKvEmpty + v_slot));
+              ++n_p;
+              jp = seq.next(jp + 1);
+              if (!(jp < seq.end)) umma_commit(bar(kBarOFinal));
+              if (js < seq.end) ok = issue_next_s();
+            }
+            item += 2 * n_s;
+            g += n_s;
+          }
+        }
+      } else {
       int item = 0;      // ring items consumed so far
       int pv_count = 0;  // P_t tiles consumed so far (all work items)
       int u = 0;         // issue rounds so far (both streams run the same rounds)
@@ -513,17 +612,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           j = jn;
         }
       }
+      }
     }
     __syncwarp();
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kSoftmaxRegs));
     // ============================================================ softmax
     const int t = warp / 4;          // Q tile of this warpgroup
     const int wl = warp % 4;         // TMEM lane quarter
     const int row_in_tile = wl * 32 + lane;
     const uint32_t lane_bits = static_cast<uint32_t>(wl * 32) << 16;
-    const uint32_t s_tmem = tmem + lane_bits + t * 128;
+    const uint32_t s_tmem_t = tmem + lane_bits + t * 128;
     const uint32_t o_tmem = tmem + lane_bits + 256 + t * 128;
     const float c = a.scale_log2;
     int k = 0;  // S_t tiles consumed so far (all work items)
@@ -541,7 +641,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lo_mine = t == 0 ? wi.lo_t[0] : wi.lo_t[1];
       const int n_mine = t == 0 ? wi.n_t[0] : wi.n_t[1];
       for (int j = seq.next(lo_mine); j < n_mine; j = seq.next(j + 1), ++k) {
-      ok = mbar_wait(bar(kBarSFull + t), k & 1, a.timeout_ns, a.status, kDevTimeoutSFull,
+      // S of this tile: the Q tile's buffer, or with one Q tile per item the
+      // buffer of this KV tile's parity
+      const int sb = C::QT == 1 ? (k & 1) : t;
+      const uint32_t s_tmem = C::QT == 1 ? tmem + lane_bits + (k & 1) * kBN : s_tmem_t;
+      ok = mbar_wait(bar(kBarSFull + sb), C::QT == 1 ? (k >> 1) & 1 : k & 1, a.timeout_ns, a.status, kDevTimeoutSFull,
                      abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -669,6 +773,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float rsum = (rsa.x + rsa.y) + (rsb.x + rsb.y);
       l_run = l_run * alpha + rsum;
       if (k > 0 && __any_sync(0xffffffffu, need)) {
+        if constexpr (C::QT == 1) {
+          // the previous tile's P·V may still be running: wait until it is done
+          ok = mbar_wait(bar(kBarOFinal + 1), (k - 1) & 1, a.timeout_ns, a.status,
+                         kDevTimeoutOFinal, abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+        }
         // O_t was complete when S_t(j) landed (tcgen05 ops retire in order)
 #pragma unroll
         for (int q4 = 0; q4 < D / 32; ++q4) {
@@ -682,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(kBarPReady + t));
+      mbar_arrive(bar(kBarPReady + sb));
       }
       if (!ok) break;
       // ---- epilogue: out = O / l, lse = ln2 * (m + log2 l)
