@@ -237,6 +237,37 @@ def test_d256_decode_workload(cuda_device):
     compare(out, lse, ro, rl, w.layout)
 
 
+def test_decode_replays_from_a_cuda_graph(cuda_device):
+    # One fa_decode call captured into a CUDA graph (the counter clear and the
+    # kernel), replayed with new cache contents: every replay is exact, so the
+    # per-sequence piece counters start from zero each time.
+    B, Hq, Hkv, S, D = 4, 32, 8, 4096, 128
+    lens = [4096, 1500, 3333, 77]
+    x = workloads.make_decode(B, Hq, Hkv, S, D, "BNSD", seed=21, lengths=lens)
+    q, k, v = _gpu(x["q"]), _gpu(x["k"]), _gpu(x["v"])
+    out = torch.empty_like(q)
+    lse = torch.empty(B, Hq, 1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(F.fa_decode_workspace_size(B, S, Hq, Hkv, D, 0), dtype=torch.uint8,
+                     device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        F.fa_decode(q, k, v, lens, scale=0.1, out=out, lse=lse, workspace=ws, stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        F.fa_decode(q, k, v, lens, scale=0.1, out=out, lse=lse, workspace=ws, stream=s)
+    for seed in (22, 23, 24):
+        y = workloads.make_decode(B, Hq, Hkv, S, D, "BNSD", seed=seed, lengths=lens)
+        q.copy_(_gpu(y["q"]))
+        k.copy_(_gpu(y["k"]))
+        v.copy_(_gpu(y["v"]))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        ro, rl = oracle.decode(y["q"], y["k"], y["v"], lens, scale=0.1)
+        compare(out, lse, ro, rl, "BNSD")
+
+
 @pytest.fixture(scope="module")
 def long_decode():
     w = workloads.WORKLOADS["long_decode"]
