@@ -237,6 +237,16 @@ def test_d256_decode_workload(cuda_device):
     compare(out, lse, ro, rl, w.layout)
 
 
+@pytest.mark.parametrize("B", [257, 1030])
+def test_decode_many_sequences(cuda_device, B):
+    # the lengths' prefix sums travel in the larger parameter block (B <= 1024)
+    # or in the workspace (B > 1024)
+    x = workloads.make_decode(B, 4, 2, 64, 64, "BSND", seed=B, len_lo=0, len_hi=64)
+    out, lse = run_decode(x, scale=0.125)
+    ro, rl = oracle.decode(x["q"], x["k"], x["v"], x["lengths"], scale=0.125, layout="BSND")
+    compare(out, lse, ro, rl, "BSND")
+
+
 def test_decode_replays_from_a_cuda_graph(cuda_device):
     # One fa_decode call captured into a CUDA graph (the counter clear and the
     # kernel), replayed with new cache contents: every replay is exact, so the
