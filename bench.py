@@ -232,6 +232,7 @@ class Runner:
                     if p:
                         km[b, w.S_kv - p:] = 1
                 self.km = km.to(dev)
+        self.splits = 0  # fa_decode's num_splits (0 = one share per SM)
         self.table = None
         if w.block_size is not None:
             # scatter the cache into a pool of blocks in a seeded random order
@@ -272,10 +273,11 @@ class Runner:
                                 out=self.out, lse=self.lse, workspace=self.ws)
         elif self.kind == "decode" and self.table is not None:
             F.fa_decode_paged(self.q, self.k, self.v, self.table, w.block_size, self.lens,
-                              scale=w.scale, out=self.out, lse=self.lse, workspace=self.ws)
+                              scale=w.scale, num_splits=self.splits, out=self.out, lse=self.lse,
+                              workspace=self.ws)
         elif self.kind == "decode":
             F.fa_decode(self.q, self.k, self.v, self.lens, scale=w.scale, layout=w.layout,
-                        out=self.out, lse=self.lse, workspace=self.ws)
+                        num_splits=self.splits, out=self.out, lse=self.lse, workspace=self.ws)
         elif w.window is not None:
             F.fa_forward_window(self.q, self.k, self.v, w.window[0], w.window[1],
                                 key_mask=self.km, scale=w.scale, layout=w.layout, out=self.out,
@@ -468,6 +470,43 @@ def cpu_baseline(w, budget_s=12.0):
                       f"{el:.1f} s"}
 
 
+def decode_sweeps(args, dev, flush, peaks, peak_kind):
+    """The long decode workload with the K/V rows cut into a fixed number of
+    pieces per sequence (num_splits 128 ... 1024) beside the default of one
+    equal share per SM, and the GQA decode workload with L2 left warm between
+    steps (its valid K/V rows, about 120 MB, then partly hit in the 126 MB L2)."""
+    import torch
+    out = {"long_decode_num_splits": {}, "gqa_decode_warm_l2": None}
+    wl = workloads.WORKLOADS["long_decode"]
+    r = Runner(wl, dev)
+    for n in (0, 128, 256, 512, 1024):
+        r.splits = n
+        r.ws = torch.empty(r.F.fa_decode_workspace_size(wl.B, wl.S_kv, wl.Hq, wl.Hkv, wl.D, n),
+                           dtype=torch.uint8, device=dev)
+        r.step()
+        s_ms, m_ms, _ = time_steps(r, args.steps, args.warmup, flush)
+        o_ms, o_k = sum(s_ms) / len(s_ms), sum(m_ms) / len(m_ms)
+        v, u = value_of("decode", r.units["step"], o_ms)
+        rf = roofline("decode", r.units["main"], o_k, peaks, peak_kind, "long_decode")
+        out["long_decode_num_splits"][str(n) if n else "0 (one share per SM)"] = {
+            "value": v, "unit": u, "ms_per_step": o_ms, "kernel_frac": rf["frac"]}
+    del r
+    torch.cuda.empty_cache()
+    wg = workloads.WORKLOADS["gqa_decode"]
+    r = Runner(wg, dev)
+    r.step()
+    s_ms, m_ms, _ = time_steps(r, args.steps, args.warmup, lambda: None)
+    o_ms, o_k = sum(s_ms) / len(s_ms), sum(m_ms) / len(m_ms)
+    v, u = value_of("decode", r.units["step"], o_ms)
+    rf = roofline("decode", r.units["main"], o_k, peaks, peak_kind, "gqa_decode")
+    out["gqa_decode_warm_l2"] = {"value": v, "unit": u, "ms_per_step": o_ms,
+                                 "kernel_frac": rf["frac"],
+                                 "l2": "not flushed between steps"}
+    del r
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -522,7 +561,7 @@ def run_gpu(args):
     (e2e_ms,) = max_over_ranks([e2e_ms], world, dev)
     e2e_val, _ = value_of(w.kind, main.units["step"] * world, e2e_ms)
 
-    others = {}
+    others, sweeps = {}, None
     if not args.only:
         for name in ("long_decode", "causal_prefill", "gqa_masked_prefill", "tiny_prefill",
                      "window_prefill", "varlen_prefill", "d256_prefill", "paged_decode",
@@ -542,6 +581,7 @@ def run_gpu(args):
                                                  name)}
             del r
             torch.cuda.empty_cache()
+        sweeps = decode_sweeps(args, dev, flush, peaks, peak_kind)
 
     if rank == 0:
         line = {
@@ -568,6 +608,7 @@ def run_gpu(args):
             "gpu_launches": int(launches),
             "clocks": clocks,
             "workloads": others,
+            "decode_sweeps": sweeps,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
