@@ -287,14 +287,15 @@ namespace {
 fa_status decode_plan_impl(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t num_kv_heads,
                            int64_t D, const int64_t* lens, int num_sms, int num_splits,
                            int64_t rc_align, int64_t* chunk_rows, int64_t* num_chunks,
-                           int64_t* max_chunks);
+                           int64_t* max_chunks, int64_t* piece_cost);
 }  // namespace
 
 fa_status fa_decode_plan(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t num_kv_heads,
                          int64_t D, const int64_t* lens, int num_sms, int num_splits,
                          int64_t* chunk_rows, int64_t* num_chunks, int64_t* max_chunks) {
+  int64_t pc = 0;
   return decode_plan_impl(B, S_kv_max, num_heads, num_kv_heads, D, lens, num_sms, num_splits, 1,
-                          chunk_rows, num_chunks, max_chunks);
+                          chunk_rows, num_chunks, max_chunks, &pc);
 }
 
 namespace {
@@ -303,7 +304,7 @@ namespace {
 fa_status decode_plan_impl(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t num_kv_heads,
                            int64_t D, const int64_t* lens, int num_sms, int num_splits,
                            int64_t rc_align, int64_t* chunk_rows, int64_t* num_chunks,
-                           int64_t* max_chunks) {
+                           int64_t* max_chunks, int64_t* piece_cost) {
   if (lens == nullptr || chunk_rows == nullptr || num_chunks == nullptr || max_chunks == nullptr)
     return FA_ERR_NULLPTR;
   if (num_kv_heads == 0) num_kv_heads = num_heads;
@@ -320,12 +321,26 @@ fa_status decode_plan_impl(int64_t B, int64_t S_kv_max, int64_t num_heads, int64
   const int64_t g = num_heads / num_kv_heads;
   const int64_t KH = num_kv_heads * (g / decode_heads_per_cta(g, D));
   const int64_t total = KH * sum;
+  // With more (non-empty) units than SMs a share holds several unit starts,
+  // each a piece end to pay for: the shares are then cut by cost, where a row
+  // costs 1 and every unit after the first adds pc (FlashAttn guide §4: split
+  // the work into sections of equal cost). Forced splits cut rows.
+  int64_t units = 0, last_unit = -1;
+  for (int64_t b = 0; b < B; ++b)
+    if (lens[b] > 0) {
+      units += KH;
+      last_unit = b * KH + KH - 1;
+    }
+  int64_t pc = 0;
+  if (num_splits == 0 && units > num_sms)
+    pc = std::max<int64_t>(kDecodePieceCostRows128 * 128 / D / rc_align, 1) * rc_align;
+  const int64_t cost = total + pc * std::max<int64_t>(last_unit, 0);
   int64_t rc;
   if (num_splits > 0) {
     rc = chunk_for_splits(std::max<int64_t>(S_kv_max, 1), num_splits);
   } else {
     // one equal share per SM (at least a couple of stages each)
-    rc = std::max<int64_t>(ceil_div(std::max<int64_t>(total, 1), num_sms), kDecodeMinRowsPerCta);
+    rc = std::max<int64_t>(ceil_div(std::max<int64_t>(cost, 1), num_sms), kDecodeMinRowsPerCta);
   }
   rc = ceil_div(rc, rc_align) * rc_align;
   int64_t mx = 0, prefix = 0;
@@ -333,14 +348,15 @@ fa_status decode_plan_impl(int64_t B, int64_t S_kv_max, int64_t num_heads, int64
     const int64_t L = lens[b];
     if (L > 0) {
       for (int64_t kh = 0; kh < KH; ++kh) {
-        const int64_t u0 = KH * prefix + kh * L;
-        mx = std::max(mx, (u0 + L - 1) / rc - u0 / rc + 1);
+        const int64_t c0 = KH * prefix + kh * L + pc * (b * KH + kh);  // cost of its first row
+        mx = std::max(mx, (c0 + L - 1) / rc - c0 / rc + 1);
       }
     }
     prefix += L;
   }
   *chunk_rows = rc;
-  *num_chunks = ceil_div(total, rc);
+  *num_chunks = total > 0 ? ceil_div(cost, rc) : 0;
+  *piece_cost = pc;
   *max_chunks = mx;
   return FA_OK;
 }
@@ -587,9 +603,9 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
   }
   const int sms = device_sm_count();
   if (sms <= 0) return FA_ERR_RUNTIME;
-  int64_t rc = 0, n_ctas = 0, max_slots = 0;
+  int64_t rc = 0, n_ctas = 0, max_slots = 0, pc = 0;
   st = decode_plan_impl(B, S_kv_max, num_heads, Hkv, D, wlens, sms, num_splits,
-                        pg != nullptr ? 16 : 1, &rc, &n_ctas, &max_slots);
+                        pg != nullptr ? 16 : 1, &rc, &n_ctas, &max_slots, &pc);
   if (st != FA_OK) return st;
   const int64_t slots = std::max<int64_t>(max_slots, 1);
   if (slots > max_slots_bound(S_kv_max, num_splits)) return FA_ERR_RUNTIME;  // cannot happen
@@ -651,6 +667,8 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
   x.scale = scale;
   x.total = total;
   x.rows_per_cta = rc;
+  x.piece_cost = pc;
+  x.n_ctas = n_ctas;
   x.max_slots = static_cast<int>(slots);
   x.prefix_host = prefix;
   x.prefix_dev = in_params ? nullptr : reinterpret_cast<const long long*>(wsb + ws.prefix);

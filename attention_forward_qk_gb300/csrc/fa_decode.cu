@@ -108,12 +108,13 @@ struct DecodeArgs {
   float* part_lse;   // [B][Hq][max_slots], log2 domain
   unsigned int* counters;  // [B * KH] pieces finished per unit (zero at launch)
   int has_empty;           // some sequence has length 0
+  int piece_cost;          // cost of a unit start after the first (0: shares of rows)
   __nv_bfloat16* out;
   float* lse;
   uint32_t* status;
   uint64_t timeout_ns;
   long long total;         // rows of the work space
-  long long rows_per_cta;  // Rc
+  long long rows_per_cta;  // Rc: cost of each CTA's share (a row costs 1)
   int B, Hq, Hkv, S_kv, max_slots, head_groups, G;
   float scale_log2;
   // paged K/V: block table [B][max_blocks] (null: contiguous cache), the
@@ -127,20 +128,23 @@ struct DecodeArgs {
   Prefix prefix;           // prefix[b] = sum of lengths of batches < b (work space)
 };
 
-// Largest b with KH * prefix[b] <= r (the batch whose rows hold r; batches
-// of length 0 own no row and are passed over). Small batches count the
-// prefix entries at or below r with independent loads, larger ones bisect.
-__device__ __forceinline__ int find_batch(const Prefix& p, int B, long long KH, long long r) {
+// Largest b with KH * (prefix[b] + pc * b) <= r: with pc = 0 the batch whose
+// rows hold row r (batches of length 0 own no row and are passed over), with
+// pc = the piece cost the batch whose range of costs holds cost r. Small
+// batches count the entries at or below r with independent loads, larger
+// ones bisect.
+__device__ __forceinline__ int find_batch(const Prefix& p, int B, long long KH, long long pc,
+                                          long long r) {
   if (B <= 64) {
     int b = 0;
 #pragma unroll 8
-    for (int i = 1; i < B; ++i) b += (KH * p[i] <= r) ? 1 : 0;
+    for (int i = 1; i < B; ++i) b += (KH * (p[i] + pc * i) <= r) ? 1 : 0;
     return b;
   }
   int lo = 0, hi = B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (KH * p[mid] <= r) lo = mid; else hi = mid - 1;
+    if (KH * (p[mid] + pc * mid) <= r) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
@@ -228,7 +232,10 @@ struct Pending {
   int unit, nsp, b, kh;
 };
 
-template <int D, int G>
+// kWeighted: the shares are cut in equal cost (piece_cost > 0), else in
+// equal rows. Two instantiations, so that the code of the common case carries
+// nothing of the other.
+template <int D, int G, bool kWeighted>
 __global__ void __launch_bounds__(kDecThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_k16,
@@ -277,14 +284,35 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
   if (warp == kDecWarps) {
     // ================================================================ producer
+    // The shares are equal in cost: a row costs 1 and, when piece_cost > 0,
+    // the start of every unit after the first costs piece_cost more (the
+    // piece end it brings), so that a share holding unit starts takes fewer
+    // rows. Row x of unit k costs x + piece_cost * k; CTA c holds the rows of
+    // cost [c Rc, (c+1) Rc).
     const long long Rc = a.rows_per_cta;
-    long long r = static_cast<long long>(blockIdx.x) * Rc;
-    const long long r1 = min(r + Rc, a.total);
+    const long long pc = kWeighted ? a.piece_cost : 0;
+    // the first row whose cost is at least T
+    auto row_at_cost = [&](long long T) -> long long {
+      const int b = find_batch(a.prefix, a.B, KH, pc, T);
+      const long long L = a.prefix[b + 1] - a.prefix[b];
+      const long long cb = KH * (a.prefix[b] + pc * b);  // cost of the batch's first row
+      const long long kh = min(KH - 1, div_nn(T - cb, L + pc));  // L + pc > 0 here
+      const long long off = T - cb - kh * (L + pc);
+      const long long u0 = KH * a.prefix[b] + kh * L;
+      return off < L ? u0 + off : u0 + L;  // in the gap before the next unit: its first row
+    };
+    const long long T0 = static_cast<long long>(blockIdx.x) * Rc;
+    long long r = T0;
+    long long r1 = min(T0 + Rc, a.total);
+    if constexpr (kWeighted) {
+      if (T0 > 0) r = row_at_cost(T0);
+      r1 = blockIdx.x + 1 == gridDim.x ? a.total : min(row_at_cost(T0 + Rc), a.total);
+    }
     // the next piece of this CTA's range [r, r1): its unit, rows and stages
     auto plan = [&](int piece, SlotHeader& h, int& kvh, int& hg) {
       h = SlotHeader{-1, 0, 1, 0, 0, 0, 0, 0, 0, 0};
       if (r >= r1) return;
-      const int b = find_batch(a.prefix, a.B, KH, r);
+      const int b = find_batch(a.prefix, a.B, KH, 0, r);
       const long long base = KH * a.prefix[b];
       const long long L = a.prefix[b + 1] - a.prefix[b];
       const long long kh = div_nn(r - base, L);
@@ -296,9 +324,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       h.kh = static_cast<int>(kh);
       h.row0 = static_cast<int>(r - u0);
       h.rows = static_cast<int>(rows);
-      const long long c0 = div_nn(u0, Rc);  // the CTA holding the unit's first row
+      const long long cu = kWeighted ? u0 + pc * (b * KH + kh) : u0;  // cost of its first row
+      const long long c0 = div_nn(cu, Rc);  // the CTA holding the unit's first row
       h.slot = static_cast<int>(blockIdx.x - c0);
-      h.nsp = static_cast<int>(div_nn(u1 - 1, Rc) - c0 + 1);
+      h.nsp = static_cast<int>(div_nn(cu + L - 1, Rc) - c0 + 1);
       h.nstage = static_cast<int>((rows + C::R - 1) / C::R);
       h.vend = h.rows;
       if (a.block_table != nullptr) {
@@ -762,9 +791,12 @@ cudaError_t launch_decode_dg(int grid, const CUtensorMap* m, const DecodeArgs& d
                              cudaStream_t stream) {
   static bool configured = false;  // benign race: idempotent attribute set
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DecCfg<D, G>::SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_kernel<D, G, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, DecCfg<D, G>::SMEM);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -778,7 +810,9 @@ cudaError_t launch_decode_dg(int grid, const CUtensorMap* m, const DecodeArgs& d
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<D, G>, m[0], m[1], m[2], m[3], da);
+  if (da.piece_cost != 0)
+    return cudaLaunchKernelEx(&cfg, decode_kernel<D, G, true>, m[0], m[1], m[2], m[3], da);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, G, false>, m[0], m[1], m[2], m[3], da);
 }
 
 template <int D>
@@ -810,6 +844,7 @@ cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
   da.timeout_ns = x.timeout_ns;
   da.total = x.total;
   da.rows_per_cta = x.rows_per_cta;
+  da.piece_cost = static_cast<int>(x.piece_cost);
   da.B = x.B;
   da.Hq = x.Hq;
   da.Hkv = x.Hkv;
@@ -852,7 +887,7 @@ cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
         !encode_bf16_map(&maps[3], x.v, x.layout, nbat, x.Hkv, S_map, x.D, x.D, tail_rows,
                          CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
-    const int grid = static_cast<int>((x.total + x.rows_per_cta - 1) / x.rows_per_cta);
+    const int grid = static_cast<int>(x.n_ctas);
     main_kernel_begin(stream);
     const cudaError_t e = x.D == 256   ? launch_decode_d<256>(G, grid, maps, da, stream)
                           : x.D == 128 ? launch_decode_d<128>(G, grid, maps, da, stream)

@@ -36,6 +36,11 @@ constexpr int kDecodeStageRows = 112;
 constexpr int kDecodeParamBatches = 1024;
 // Smallest share of the work space one decode CTA is given.
 constexpr int kDecodeMinRowsPerCta = 224;
+// Cost of a piece end (park, combine, partial write) in K/V rows of D = 128
+// (scaled by 128 / D), charged when the shares are cut by cost instead of by
+// rows: only when there are more units than SMs, so that a share holds
+// several unit starts.
+constexpr int kDecodePieceCostRows128 = 96;
 // Largest persistent prefill grid the workspace's schedule has room for.
 constexpr int kMaxPrefillCtas = 1024;
 
@@ -47,7 +52,9 @@ struct DecodeLaunch {
   int B, Hq, Hkv, S_kv, D, layout;
   float scale;
   long long total;            // rows of the work space (KV heads x head groups x sum L_b)
-  long long rows_per_cta;     // contiguous share of each CTA
+  long long rows_per_cta;     // cost of each CTA's contiguous share (a row costs 1)
+  long long piece_cost;       // cost of a unit start after the first (0: shares of rows)
+  long long n_ctas;           // shares (CTAs)
   int max_slots;              // piece slots per (batch, head) in the partial buffers
   const long long* prefix_host;  // [B + 1] prefix sums of the lengths
   const long long* prefix_dev;   // the same in the workspace, or null (then in params)

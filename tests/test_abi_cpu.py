@@ -193,18 +193,35 @@ def _heads_per_cta(g, D):
     return 4 if g % 4 == 0 else 2 if g % 2 == 0 else 1
 
 
-def _pieces(lens, Hq, Hkv, D, rc):
-    """Brute force: pieces per (batch, KV head, head group) unit when the
-    units are laid end to end and cut every rc rows."""
+def _units(lens, Hq, Hkv, D):
     g = Hq // Hkv
-    KH = Hkv * (g // _heads_per_cta(g, D))
-    out, pos = [], 0
+    return Hkv * (g // _heads_per_cta(g, D))
+
+
+def _piece_cost(lens, Hq, Hkv, D, sms=152, splits=0):
+    """The extra cost of a unit start: charged only when the non-empty units
+    outnumber the SMs (96 rows at D = 128, scaled by 128 / D)."""
+    units = _units(lens, Hq, Hkv, D) * sum(1 for L in lens if L)
+    return 96 * 128 // D if splits == 0 and units > sms else 0
+
+
+def _pieces(lens, Hq, Hkv, D, rc, pc=0):
+    """Brute force: pieces per (batch, KV head, head group) unit when the
+    units are laid end to end, row by row, each row costing 1 and the start
+    of unit k adding pc * k, and the cost is cut every rc. Returns the
+    pieces of every non-empty unit, the total rows and the total cost."""
+    KH = _units(lens, Hq, Hkv, D)
+    out, pos, k = [], 0, 0
+    cost_end = 0
     for L in lens:
         for _ in range(KH):
             if L:
-                out.append(len(range(pos // rc, (pos + L - 1) // rc + 1)))
+                c0 = pos + pc * k
+                out.append(len(range(c0 // rc, (c0 + L - 1) // rc + 1)))
+                cost_end = c0 + L
             pos += L
-    return out, pos
+            k += 1
+    return out, pos, cost_end
 
 
 def test_plan_cuts_equal_shares(lib):
@@ -218,8 +235,9 @@ def test_plan_cuts_equal_shares(lib):
         Hq = Hkv * rng.choice([1, 2, 4, 8])
         D = rng.choice([64, 128])
         rc, n, mx = _plan(lens, S, Hq, Hkv, D=D)
-        pieces, total = _pieces(lens, Hq, Hkv, D, rc)
-        assert rc >= 224 and n == math.ceil(total / rc) and n <= 152
+        pc = _piece_cost(lens, Hq, Hkv, D)
+        pieces, total, cost = _pieces(lens, Hq, Hkv, D, rc, pc)
+        assert rc >= 224 and n == math.ceil(cost / rc) and n <= 152
         assert mx == (max(pieces) if pieces else 0)
         assert mx <= math.ceil(S / 224) + 1  # fits the size query's bound
 
@@ -233,6 +251,40 @@ def test_plan_one_share_per_sm():
     rc, n, mx = _plan([131072], 131072, 32, 32)
     assert n == 152 and mx == max(_pieces([131072], 32, 32, 128, rc)[0])
     assert mx <= math.ceil(131072 / rc) + 1
+
+
+def test_plan_weights_unit_starts():
+    # 64 sequences x 8 KV heads = 512 units > 152 SMs: the shares are cut by
+    # cost, a row costs 1 and each unit start after the first 96 rows more
+    lens = [(37 * b) % 2000 + 1 for b in range(64)]
+    rc, n, mx = _plan(lens, 2048, 32, 8)
+    pieces, total, cost = _pieces(lens, 32, 8, 128, rc, 96)
+    assert cost == total + 96 * (64 * 8 - 1)
+    assert rc == math.ceil(cost / 152) and n == 152 and mx == max(pieces)
+    # a share that holds unit starts holds fewer rows than one that does not:
+    # count the rows of every share by walking the rows with their costs
+    rows = [0] * n
+    starts = [0] * n
+    k = 0
+    for L in lens:
+        for _ in range(8):
+            c0 = sum(rows) + 96 * k
+            for i in range(L):
+                rows[(c0 + i) // rc] += 1
+            starts[c0 // rc] += 1
+            k += 1
+    assert sum(rows) == total
+    # every share but the last: its cost rc is its rows plus the piece costs
+    # in it, one per unit start in it (give or take one straddling a boundary)
+    for r, st in zip(rows[:-1], starts[:-1]):
+        assert rc - 96 * (st + 1) <= r <= rc - 96 * max(st - 1, 0)
+    assert max(starts) >= 3 and min(rows[:-1]) < max(rows[:-1]) - 96
+    # D = 64 (eight heads per CTA) charges 192 rows per unit start
+    rc64, n64, _ = _plan(lens, 2048, 64, 8, D=64)
+    assert rc64 == math.ceil((8 * sum(lens) + 192 * (64 * 8 - 1)) / 152) and n64 == 152
+    # forced splits cut rows and charge nothing
+    rc2, n2, _ = _plan(lens, 2048, 32, 8, splits=4)
+    assert (rc2, n2) == (512, math.ceil(8 * sum(lens) / 512))
 
 
 def test_plan_with_forced_splits():

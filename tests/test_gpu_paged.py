@@ -69,6 +69,9 @@ CASES = [
     # head dim 256: 56-row stages, 8-row boxes
     (3, 16, 4, 256, [777, 16, 2048], 16, "PA_BBND", 0),
     (2, 8, 8, 256, [1500, 90], 48, "PA_BNBD", 3),
+    # more units than SMs: shares cut by cost, still on 16-row boundaries
+    (40, 32, 8, 128, [(53 * b) % 700 + (b % 3) for b in range(40)], 16, "PA_BBND", 0),
+    (24, 16, 16, 64, [(97 * b) % 300 for b in range(24)], 32, "PA_BNBD", 0),
 ]
 
 
