@@ -565,7 +565,7 @@ def run_gpu(args):
     if not args.only:
         for name in ("long_decode", "causal_prefill", "gqa_masked_prefill", "tiny_prefill",
                      "window_prefill", "varlen_prefill", "d256_prefill", "paged_decode",
-                     "d256_decode", "gqa_decode"):
+                     "d256_decode", "batch_decode", "gqa_decode"):
             if name == args.workload:
                 continue
             wo = workloads.WORKLOADS[name]

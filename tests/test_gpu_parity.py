@@ -229,12 +229,33 @@ def test_decode_reuses_a_dirty_workspace(cuda_device):
         compare(out, lse, ro, rl, "BNSD")
 
 
-def test_d256_decode_workload(cuda_device):
-    w = workloads.WORKLOADS["d256_decode"]
+@pytest.mark.parametrize("name", ["d256_decode", "batch_decode"])
+def test_decode_workload(cuda_device, name):
+    w = workloads.WORKLOADS[name]
     x = workloads.make(w)
     out, lse = run_decode(x, scale=w.scale)
     ro, rl = oracle.decode(x["q"], x["k"], x["v"], x["lengths"], scale=w.scale, layout=w.layout)
     compare(out, lse, ro, rl, w.layout)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,layout,masked", [
+    # more (batch, KV head, head group) units than SMs: the shares are cut in
+    # equal cost, each unit start costing 96 * 128 / D rows
+    (48, 16, 4, 1500, 256, "BNSD", False),   # G = 4 at D = 256: 192 units
+    (8, 32, 32, 3000, 128, "BSND", True),    # G = 1: 256 units, with a key mask
+    (32, 64, 8, 1200, 64, "BNSD", False),    # G = 8 at D = 64: 256 units
+    (160, 4, 1, 900, 128, "BSND", False),    # one unit per sequence, 160 units
+])
+def test_decode_shares_by_cost(cuda_device, B, Hq, Hkv, S, D, layout, masked):
+    x = workloads.make_decode(B, Hq, Hkv, S, D, layout, seed=B + D, len_lo=0, len_hi=S)
+    km = None
+    if masked:
+        g = torch.Generator().manual_seed(B)
+        km = (torch.rand(B, S, generator=g) < 0.2).to(torch.uint8)
+    out, lse = run_decode(x, scale=D ** -0.5, key_mask=km)
+    ro, rl = oracle.decode(x["q"], x["k"], x["v"], x["lengths"], scale=D ** -0.5,
+                           layout=layout, key_mask=km)
+    compare(out, lse, ro, rl, layout)
 
 
 @pytest.mark.parametrize("B", [257, 1030])

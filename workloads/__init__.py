@@ -115,6 +115,13 @@ WORKLOADS: dict[str, Workload] = {
         "d256_decode", "decode", B=8, Hq=32, Hkv=8, S_q=1, S_kv=8192, D=256,
         layout="BNSD", seed=109, len_lo=1024, len_hi=8192, garbage=True,
         note="B=8 Hq=32 Hkv=8 D=256 BNSD, cache padded to 8192, L_b~U[1024,8192]"),
+    # Beyond the five: a serving-size decode batch, 64 sequences of the GQA
+    # decode workload's head layout (512 (batch, KV head) units, more than
+    # SMs: the split cuts the shares by cost).
+    "batch_decode": Workload(
+        "batch_decode", "decode", B=64, Hq=32, Hkv=8, S_q=1, S_kv=4096, D=128,
+        layout="BNSD", seed=111, len_lo=256, len_hi=4096, garbage=True,
+        note="B=64 Hq=32 Hkv=8 D=128 BNSD, cache padded to 4096, L_b~U[256,4096]"),
     # Beyond the five: the GQA decode workload with its cache paged (FlashAttn
     # guide §1.2, PA_BBND, 128-row blocks in shuffled order).
     "paged_decode": Workload(
