@@ -42,6 +42,9 @@ SIGNATURES = {
     "fa_forward_varlen_workspace_size": (_sz, [_i64] * 6),
     "fa_forward_varlen": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _i64, _i64, _i64,
                                          _i64, ctypes.c_float, _vp, _vp, _vp, _sz, _vp]),
+    "fa_forward_varlen_window": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                                _i64, _i64, ctypes.c_float, _vp, _vp, _vp, _sz,
+                                                _vp]),
     "fa_forward_window": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _i64, _i64,
                                          _i64, _i64, _i64, ctypes.c_float, ctypes.c_int, _vp,
                                          _vp, _vp, _sz, _vp]),

@@ -528,11 +528,15 @@ size_t fa_forward_varlen_workspace_size(int64_t B, int64_t max_seqlen_q, int64_t
   return fa_forward_workspace_size(B, max_seqlen_q, max_seqlen_kv, num_heads, num_kv_heads, D);
 }
 
-fa_status fa_forward_varlen(const void* q, const void* k, const void* v,
-                            const int64_t* cu_seqlens_q, const int64_t* cu_seqlens_kv,
-                            int mask_mode, int64_t B, int64_t num_heads, int64_t num_kv_heads,
-                            int64_t D, float scale, void* out, float* lse, void* workspace,
-                            size_t workspace_bytes, void* stream) {
+namespace {
+// fa_forward_varlen and fa_forward_varlen_window: the offsets checked, then
+// the window (-1, -1) no mask, (-1, 0) causal
+fa_status forward_varlen_impl(const void* q, const void* k, const void* v,
+                              const int64_t* cu_seqlens_q, const int64_t* cu_seqlens_kv,
+                              bool mask_ok, int64_t win_left, int64_t win_right, int64_t B,
+                              int64_t num_heads, int64_t num_kv_heads, int64_t D, float scale,
+                              void* out, float* lse, void* workspace, size_t workspace_bytes,
+                              void* stream) {
   if (cu_seqlens_q == nullptr || cu_seqlens_kv == nullptr) return FA_ERR_NULLPTR;
   if (B < 0) return FA_ERR_PARAM_INVALID;
   if (cu_seqlens_q[0] != 0 || cu_seqlens_kv[0] != 0) return FA_ERR_PARAM_INVALID;
@@ -545,12 +549,34 @@ fa_status fa_forward_varlen(const void* q, const void* k, const void* v,
     max_kv = std::max(max_kv, lkv);
   }
   if (cu_seqlens_q[B] > kMaxDim || cu_seqlens_kv[B] > kMaxDim) return FA_ERR_PARAM_INVALID;
-  const bool mask_ok = mask_mode == FA_MASK_NONE || mask_mode == FA_MASK_CAUSAL;
-  const bool causal = mask_mode == FA_MASK_CAUSAL;
   // packed tensors [T, H, D] are BSND with one batch
-  return forward_impl(q, k, v, mask_ok, -1, causal ? 0 : -1, nullptr, nullptr, B, max_q, max_kv,
+  return forward_impl(q, k, v, mask_ok, win_left, win_right, nullptr, nullptr, B, max_q, max_kv,
                       num_heads, num_kv_heads, D, scale, FA_LAYOUT_BSND, out, lse, workspace,
                       workspace_bytes, stream, cu_seqlens_q, cu_seqlens_kv);
+}
+}  // namespace
+
+fa_status fa_forward_varlen(const void* q, const void* k, const void* v,
+                            const int64_t* cu_seqlens_q, const int64_t* cu_seqlens_kv,
+                            int mask_mode, int64_t B, int64_t num_heads, int64_t num_kv_heads,
+                            int64_t D, float scale, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  const bool mask_ok = mask_mode == FA_MASK_NONE || mask_mode == FA_MASK_CAUSAL;
+  const bool causal = mask_mode == FA_MASK_CAUSAL;
+  return forward_varlen_impl(q, k, v, cu_seqlens_q, cu_seqlens_kv, mask_ok, -1, causal ? 0 : -1,
+                             B, num_heads, num_kv_heads, D, scale, out, lse, workspace,
+                             workspace_bytes, stream);
+}
+
+fa_status fa_forward_varlen_window(const void* q, const void* k, const void* v,
+                                   const int64_t* cu_seqlens_q, const int64_t* cu_seqlens_kv,
+                                   int64_t win_left, int64_t win_right, int64_t B,
+                                   int64_t num_heads, int64_t num_kv_heads, int64_t D, float scale,
+                                   void* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  return forward_varlen_impl(q, k, v, cu_seqlens_q, cu_seqlens_kv, true, win_left, win_right, B,
+                             num_heads, num_kv_heads, D, scale, out, lse, workspace,
+                             workspace_bytes, stream);
 }
 
 fa_status fa_forward_window(const void* q, const void* k, const void* v, int64_t win_left,

@@ -142,6 +142,22 @@ def fa_forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, *, mask_mode=None, s
     """Prefill attention over packed variable-length sequences (TND): q, out
     [T_q, Hq, D]; k, v [T_kv, Hkv, D]; cu_seqlens_* host sequences of B + 1
     offsets. Returns (out, lse) with lse [T_q, Hq]."""
+    return _varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, None, mask_mode, scale, num_heads,
+                   out, lse, return_lse, workspace, stream)
+
+
+def fa_forward_varlen_window(q, k, v, cu_seqlens_q, cu_seqlens_kv, win_left, win_right, *,
+                             scale=1.0, num_heads=None, num_kv_heads=None, out=None, lse=None,
+                             return_lse=True, workspace=None, stream=None):
+    """fa_forward_varlen with a sliding window inside every sequence: row i
+    keeps key j iff (win_left < 0 or j >= i - win_left) and (win_right < 0 or
+    j <= i + win_right), both counted from the sequence's first token."""
+    return _varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, (int(win_left), int(win_right)), None,
+                   scale, num_heads, out, lse, return_lse, workspace, stream)
+
+
+def _varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, window, mask_mode, scale, num_heads, out, lse,
+            return_lse, workspace, stream):
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check_tensor(t, n)
     if q.dim() != 3 or k.dim() != 3 or tuple(v.shape) != tuple(k.shape):
@@ -171,11 +187,17 @@ def fa_forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, *, mask_mode=None, s
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     aq = (ctypes.c_int64 * (B + 1))(*cq)
     akv = (ctypes.c_int64 * (B + 1))(*ckv)
-    st = _lib.load().fa_forward_varlen(
-        q.data_ptr(), k.data_ptr(), v.data_ptr(), aq, akv, MASK_MODES.get(mask_mode, mask_mode),
-        B, Hq, Hkv, D, float(scale), out.data_ptr(), lse.data_ptr() if lse is not None else None,
-        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
-    check(st, "fa_forward_varlen")
+    tail = (B, Hq, Hkv, D, float(scale), out.data_ptr(),
+            lse.data_ptr() if lse is not None else None, workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    if window is None:
+        st = _lib.load().fa_forward_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), aq, akv,
+                                           MASK_MODES.get(mask_mode, mask_mode), *tail)
+        check(st, "fa_forward_varlen")
+    else:
+        st = _lib.load().fa_forward_varlen_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), aq,
+                                                  akv, window[0], window[1], *tail)
+        check(st, "fa_forward_varlen_window")
     return out, lse
 
 

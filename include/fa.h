@@ -143,6 +143,23 @@ fa_status fa_forward_varlen(const void* q, const void* k, const void* v,
                             int64_t D, float scale, void* out, float* lse, void* workspace,
                             size_t workspace_bytes, void* stream);
 
+/* fa_forward_varlen with a sliding window (FlashAttn guide §1.5, mask_mode 4)
+ * inside every packed sequence: query row i of a sequence keeps key j of the
+ * same sequence iff
+ *     (win_left  < 0 or j >= i - win_left) and (win_right < 0 or j <= i + win_right),
+ * i and j counted from the sequence's first token (top-left aligned, so
+ * (-1, 0) is causal and (-1, -1) no mask). A window needs equal q and kv
+ * lengths per sequence; widths below -1 are FA_ERR_PARAM_INVALID. KV tiles
+ * wholly outside every row's window are never loaded or multiplied. The
+ * workspace (fa_forward_varlen_workspace_size) and the other errors are those
+ * of fa_forward_varlen. */
+fa_status fa_forward_varlen_window(const void* q, const void* k, const void* v,
+                                   const int64_t* cu_seqlens_q, const int64_t* cu_seqlens_kv,
+                                   int64_t win_left, int64_t win_right, int64_t B,
+                                   int64_t num_heads, int64_t num_kv_heads, int64_t D, float scale,
+                                   void* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
 /* Fused attention forward with a sliding window (FlashAttn guide §1.5,
  * mask_mode 4: a band of win_left tokens before and win_right tokens after
  * each query). Query row i keeps key j iff

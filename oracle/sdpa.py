@@ -286,11 +286,12 @@ def merge_lse(lses, onorms):
 
 
 def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, *, scale: float = 1.0,
-                     causal: bool = False):
+                     causal: bool = False, window=None):
     """Packed variable-length sequences ([FA] §1.3 TND layout, §1.4
     cu_seqlens): q [T_q, Hq, D], k/v [T_kv, Hkv, D]; sequence b is q rows
     cu_q[b]..cu_q[b+1]-1 against k/v rows cu_kv[b]..cu_kv[b+1]-1, each an
-    independent attention (causal top-left aligned within the sequence).
+    independent attention (causal, or the sliding window of [FA] §1.5 given
+    as (win_left, win_right), top-left aligned within the sequence).
     Returns out [T_q, Hq, D] and lse [T_q, Hq] (the TND lse shape of [FA] §1.6).
     """
     qn, kn, vn = _as_f64(q), _as_f64(k), _as_f64(v)
@@ -304,7 +305,7 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, *, scale: float = 1.0
         if q1 == q0:
             continue
         o, l = attention(qn[None, q0:q1], kn[None, k0:k1], vn[None, k0:k1], scale=scale,
-                         layout="BSND", causal=causal)
+                         layout="BSND", causal=causal, window=window)
         out[q0:q1] = o[0]
         lse[q0:q1] = l[0].T
     return out, lse

@@ -378,3 +378,30 @@ def test_forward_varlen_rejects_before_any_cuda_call(lib, cq, ckv, kw, expect):
 def test_forward_varlen_null_offsets(lib):
     assert lib.fa_forward_varlen(P, P, P, None, None, 0, 1, 4, 2, 128, 0.1, P, None, WS,
                                  1 << 22, None) == _lib.FA_ERR_NULLPTR
+
+
+def _fwd_varlen_window(lib, cq, ckv, wl, wr, **kw):
+    args = dict(q=P, Hq=4, Hkv=2, D=128, ws_bytes=1 << 22)
+    args.update(kw)
+    aq = (ctypes.c_int64 * len(cq))(*cq)
+    akv = (ctypes.c_int64 * len(ckv))(*ckv)
+    return lib.fa_forward_varlen_window(args["q"], P, P, aq, akv, wl, wr, len(cq) - 1, args["Hq"],
+                                        args["Hkv"], args["D"], 0.1, P, None, WS,
+                                        args["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("cq,ckv,wl,wr,kw,expect", [
+    ([0, 5, 9], [0, 5, 8], 3, 0, {}, _lib.FA_ERR_PARAM_INVALID),   # a window, unequal lengths
+    ([0, 5], [0, 5], -2, 0, {}, _lib.FA_ERR_PARAM_INVALID),         # width below -1
+    ([0, 5], [0, 5], 0, -7, {}, _lib.FA_ERR_PARAM_INVALID),
+    ([0, 5], [0, 5], 3, 0, dict(q=None), _lib.FA_ERR_NULLPTR),
+    ([0, 5], [0, 5], 3, 0, dict(D=80), _lib.FA_ERR_UNSUPPORTED),
+    ([0, 5], [0, 5], 3, 0, dict(ws_bytes=16), _lib.FA_ERR_WORKSPACE_TOO_SMALL),
+])
+def test_forward_varlen_window_rejects_before_any_cuda_call(lib, cq, ckv, wl, wr, kw, expect):
+    assert _fwd_varlen_window(lib, cq, ckv, wl, wr, **kw) == expect
+
+
+def test_forward_varlen_window_null_offsets(lib):
+    assert lib.fa_forward_varlen_window(P, P, P, None, None, 3, 0, 1, 4, 2, 128, 0.1, P, None,
+                                        WS, 1 << 22, None) == _lib.FA_ERR_NULLPTR

@@ -64,6 +64,34 @@ def test_varlen_matches_oracle(cuda_device, lq, lkv, Hq, Hkv, D, causal):
     _compare(out, lse, ro, rl)
 
 
+WINDOW_CASES = [
+    # lens, Hq, Hkv, D, (win_left, win_right)
+    ([700, 1, 300, 129], 4, 2, 128, (255, 0)),     # a causal band, shorter than a sequence
+    ([1000, 64, 513], 8, 2, 128, (100, 37)),       # both sides, not tile-aligned
+    ([600, 0, 90], 4, 4, 64, (-1, 200)),           # unbounded left, bounded right
+    ([777, 200], 4, 2, 256, (130, 0)),             # head dim 256 (64-key tiles)
+    ([300, 300], 2, 2, 128, (5000, 5000)),         # wider than every sequence: no mask
+]
+
+
+@pytest.mark.parametrize("lens,Hq,Hkv,D,window", WINDOW_CASES)
+def test_varlen_window_matches_oracle(cuda_device, lens, Hq, Hkv, D, window):
+    q, k, v, cq, ckv = _packed(lens, lens, Hq, Hkv, D, seed=sum(lens) + D + 7)
+    scale = 1.0 / math.sqrt(D)
+    out, lse = F.fa_forward_varlen_window(q.cuda(), k.cuda(), v.cuda(), cq.tolist(), ckv.tolist(),
+                                          window[0], window[1], scale=scale)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention_varlen(q, k, v, cq, ckv, scale=scale, window=window)
+    _compare(out, lse, ro, rl)
+
+
+def test_varlen_window_rejects_unequal_lengths(cuda_device):
+    q, k, v, cq, ckv = _packed([100, 50], [100, 60], 2, 2, 128, seed=3)
+    with pytest.raises(F.FaError) as e:
+        F.fa_forward_varlen_window(q.cuda(), k.cuda(), v.cuda(), cq.tolist(), ckv.tolist(), 10, 0)
+    assert e.value.status == 2  # FA_ERR_PARAM_INVALID
+
+
 def test_varlen_equal_lengths_match_padded_call_bitwise(cuda_device):
     """Equal lengths: the packed call and the BSND batch call compute the same
     tiles in the same order."""

@@ -406,3 +406,28 @@ def test_varlen_equal_lengths_match_padded_batch():
     o2, l2 = oracle.attention(x["q"], x["k"], x["v"], scale=0.2, layout="BSND", causal=True)
     np.testing.assert_array_equal(o1, o2.reshape(B * S, Hq, D))
     np.testing.assert_array_equal(l1, l2.transpose(0, 2, 1).reshape(B * S, Hq))
+
+
+def test_varlen_window_equals_per_sequence_bruteforce():
+    """A sliding window inside packed sequences ([FA] §1.5 with §1.3): each
+    sequence against the scalar-loop definition with its own window."""
+    g = torch.Generator().manual_seed(13)
+    lens = [6, 1, 9, 4]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    Hq, Hkv, D = 4, 2, 5
+    q = torch.randn(int(cu[-1]), Hq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(int(cu[-1]), Hkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(int(cu[-1]), Hkv, D, generator=g).to(torch.bfloat16)
+    for window in [(2, 0), (0, 1), (3, 2), (-1, 1)]:
+        out, lse = oracle.attention_varlen(q, k, v, cu, cu, scale=0.4, window=window)
+        for b in range(len(lens)):
+            sl = slice(cu[b], cu[b + 1])
+            ro, rl = oracle.attention_bruteforce(q[sl][None], k[sl][None], v[sl][None], scale=0.4,
+                                                 layout="BSND", window=window)
+            np.testing.assert_allclose(out[sl], ro[0], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse[sl], rl[0].T, rtol=0, atol=1e-12)
+    # (-1, 0) is causal
+    o1, l1 = oracle.attention_varlen(q, k, v, cu, cu, scale=0.4, window=(-1, 0))
+    o2, l2 = oracle.attention_varlen(q, k, v, cu, cu, scale=0.4, causal=True)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
