@@ -694,7 +694,12 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
   x.total = total;
   x.rows_per_cta = rc;
   x.piece_cost = pc;
-  x.n_ctas = n_ctas;
+  // a forced split count cuts fixed-size shares: one CTA per SM takes them in
+  // turn (no CTA more than half as many as it can record split pieces of)
+  x.loop_shares = num_splits > 0;
+  x.n_ctas = x.loop_shares ? std::max<int64_t>(std::min<int64_t>(n_ctas, sms),
+                                                ceil_div(n_ctas, kDecodeLoopSharesPerCta))
+                           : n_ctas;
   x.max_slots = static_cast<int>(slots);
   x.prefix_host = prefix;
   x.prefix_dev = in_params ? nullptr : reinterpret_cast<const long long*>(wsb + ws.prefix);
@@ -756,7 +761,8 @@ fa_status fa_workspace_status(void* workspace, void* stream) {
     return FA_ERR_RUNTIME;
   if (word != 0) {
     if (cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return FA_ERR_RUNTIME;
-    return FA_ERR_DEVICE_TIMEOUT;
+    // every code but the (impossible) pending-list overflow is an expired wait
+    return word == kDevPendingOverflow ? FA_ERR_RUNTIME : FA_ERR_DEVICE_TIMEOUT;
   }
   return FA_OK;
 }

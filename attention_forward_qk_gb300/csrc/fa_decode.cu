@@ -232,10 +232,20 @@ struct Pending {
   int unit, nsp, b, kh;
 };
 
-// kWeighted: the shares are cut in equal cost (piece_cost > 0), else in
-// equal rows. Two instantiations, so that the code of the common case carries
-// nothing of the other.
-template <int D, int G, bool kWeighted>
+// How the work space is cut into shares, one instantiation each so that the
+// code of the common case carries nothing of the others:
+//   kSharesRows  one share per CTA, equal in rows
+//   kSharesCost  one share per CTA, equal in cost (piece_cost > 0)
+//   kSharesLoop  fixed-size shares (a forced split count), more than CTAs:
+//                each CTA takes shares blockIdx.x, blockIdx.x + gridDim.x, ...
+//                and counts the split pieces of all of them at its end
+constexpr int kSharesRows = 0, kSharesCost = 1, kSharesLoop = 2;
+// split pieces a CTA can record in the loop mode (two per share at most; the
+// host gives no CTA more than half as many shares)
+constexpr int kMaxLoopPending = 512;
+constexpr int kLoopSmemExtra = 1024 + kMaxLoopPending * 16;
+
+template <int D, int G, int kShares>
 __global__ void __launch_bounds__(kDecThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_k16,
@@ -244,6 +254,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   using C = DecCfg<D, G>;
   constexpr int NP = C::NP;
   constexpr int NST = C::NST;
+  static_assert(kShares != kSharesLoop || C::SMEM + kLoopSmemExtra <= 232448, "shared memory");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -253,9 +264,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   // bars: full[kMaxStages], empty[kMaxStages], scratch free[2], scratch parked[2]
   SlotHeader* hdr = reinterpret_cast<SlotHeader*>(bars + 2 * kMaxStages + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(hdr + kMaxStages);
-  // split pieces of this CTA (at most its first and its last): counted at the end
+  // split pieces of this CTA (at most its first and its last; in the loop
+  // mode those of all its shares, after the barrier block): counted at the end
   int* n_pending = const_cast<int*>(abort_flag) + 1;
-  Pending* pending = reinterpret_cast<Pending*>(n_pending + 3);  // [2]
+  Pending* pending = kShares == kSharesLoop
+                         ? reinterpret_cast<Pending*>(qbuf + kMaxStages * C::QB + 1024)
+                         : reinterpret_cast<Pending*>(n_pending + 3);  // [2]
+  constexpr int kPendingCap = kShares == kSharesLoop ? kMaxLoopPending : 2;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -290,6 +305,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     // rows. Row x of unit k costs x + piece_cost * k; CTA c holds the rows of
     // cost [c Rc, (c+1) Rc).
     const long long Rc = a.rows_per_cta;
+    constexpr bool kWeighted = kShares == kSharesCost;
     const long long pc = kWeighted ? a.piece_cost : 0;
     // the first row whose cost is at least T
     auto row_at_cost = [&](long long T) -> long long {
@@ -304,6 +320,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const long long T0 = static_cast<long long>(blockIdx.x) * Rc;
     long long r = T0;
     long long r1 = min(T0 + Rc, a.total);
+    long long v = blockIdx.x;  // the share being planned
     if constexpr (kWeighted) {
       if (T0 > 0) r = row_at_cost(T0);
       r1 = blockIdx.x + 1 == gridDim.x ? a.total : min(row_at_cost(T0 + Rc), a.total);
@@ -311,6 +328,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     // the next piece of this CTA's range [r, r1): its unit, rows and stages
     auto plan = [&](int piece, SlotHeader& h, int& kvh, int& hg) {
       h = SlotHeader{-1, 0, 1, 0, 0, 0, 0, 0, 0, 0};
+      if constexpr (kShares == kSharesLoop) {
+        while (r >= r1) {  // this share is done: the CTA's next one
+          v += gridDim.x;
+          if (v * Rc >= a.total) return;
+          r = v * Rc;
+          r1 = min(r + Rc, a.total);
+        }
+      }
       if (r >= r1) return;
       const int b = find_batch(a.prefix, a.B, KH, 0, r);
       const long long base = KH * a.prefix[b];
@@ -326,7 +351,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       h.rows = static_cast<int>(rows);
       const long long cu = kWeighted ? u0 + pc * (b * KH + kh) : u0;  // cost of its first row
       const long long c0 = div_nn(cu, Rc);  // the CTA holding the unit's first row
-      h.slot = static_cast<int>(blockIdx.x - c0);
+      h.slot = static_cast<int>(v - c0);
       h.nsp = static_cast<int>(div_nn(cu + L - 1, Rc) - c0 + 1);
       h.nstage = static_cast<int>((rows + C::R - 1) / C::R);
       h.vend = h.rows;
@@ -736,7 +761,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         mbar_arrive(sfree0 + 8 * buf);  // this warp is done with the buffer
         if (warp == 0 && hd.nsp > 1) {
           const int i = (*n_pending)++;
-          if (i < 2) pending[i] = Pending{static_cast<int>(hd.b * KH + hd.kh), hd.nsp, hd.b, hd.kh};
+          if (i < kPendingCap)
+            pending[i] = Pending{static_cast<int>(hd.b * KH + hd.kh), hd.nsp, hd.b, hd.kh};
+          else
+            record_error(a.status, kDevPendingOverflow);  // the host plan prevents this
         }
       }
     }
@@ -744,6 +772,32 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   __syncthreads();
   // ---- count this CTA's split pieces; the CTA that finishes a unit's last
   // piece merges the unit (every partial of it is visible by then)
+  if constexpr (kShares == kSharesLoop) {
+    // many pieces: every thread counts some; a unit to merge is marked by a
+    // negative nsp, then its G rows are merged one warp per row
+    const int np = min(*n_pending, kPendingCap);
+    if (np == 0 || *abort_flag) return;
+    if (tid < np) __threadfence();  // the partials of this CTA, written before the barrier
+    bool merges = false;
+    for (int e = tid; e < np; e += kDecThreads) {
+      const unsigned c = atomicAdd(a.counters + pending[e].unit, 1u);
+      if (c == static_cast<unsigned>(pending[e].nsp - 1)) {
+        pending[e].nsp = -pending[e].nsp;
+        merges = true;
+      }
+    }
+    if (merges) __threadfence();  // the other CTAs' partials of those units, before reading them
+    __syncthreads();
+    for (int t = warp; t < np * G; t += kDecWarps + 1) {
+      const Pending p = pending[t / G];
+      if (p.nsp >= 0) continue;
+      const int kvh = p.kh / a.head_groups;
+      const int hg = p.kh % a.head_groups;
+      const size_t bh0 = static_cast<size_t>(p.b) * a.Hq + kvh * g_total + hg * G;
+      merge_row<D>(a, bh0 + t % G, -p.nsp, lane);
+    }
+    return;
+  }
   const int np = min(*n_pending, 2);
   if (np == 0 || *abort_flag) return;
   volatile int* merge_mask = n_pending + 1;
@@ -787,16 +841,20 @@ __global__ void __launch_bounds__(128) decode_empty_kernel(const __grid_constant
 }
 
 template <int D, int G>
-cudaError_t launch_decode_dg(int grid, const CUtensorMap* m, const DecodeArgs& da,
+cudaError_t launch_decode_dg(int grid, bool loop, const CUtensorMap* m, const DecodeArgs& da,
                              cudaStream_t stream) {
   static bool configured = false;  // benign race: idempotent attribute set
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G, false>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G, kSharesRows>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DecCfg<D, G>::SMEM);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_kernel<D, G, true>,
+      e = cudaFuncSetAttribute(decode_kernel<D, G, kSharesCost>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, DecCfg<D, G>::SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_kernel<D, G, kSharesLoop>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               DecCfg<D, G>::SMEM + kLoopSmemExtra);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -810,21 +868,25 @@ cudaError_t launch_decode_dg(int grid, const CUtensorMap* m, const DecodeArgs& d
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (loop) {
+    cfg.dynamicSmemBytes = DecCfg<D, G>::SMEM + kLoopSmemExtra;
+    return cudaLaunchKernelEx(&cfg, decode_kernel<D, G, kSharesLoop>, m[0], m[1], m[2], m[3], da);
+  }
   if (da.piece_cost != 0)
-    return cudaLaunchKernelEx(&cfg, decode_kernel<D, G, true>, m[0], m[1], m[2], m[3], da);
-  return cudaLaunchKernelEx(&cfg, decode_kernel<D, G, false>, m[0], m[1], m[2], m[3], da);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<D, G, kSharesCost>, m[0], m[1], m[2], m[3], da);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, G, kSharesRows>, m[0], m[1], m[2], m[3], da);
 }
 
 template <int D>
-cudaError_t launch_decode_d(int G, int grid, const CUtensorMap* m, const DecodeArgs& da,
-                            cudaStream_t s) {
+cudaError_t launch_decode_d(int G, int grid, bool loop, const CUtensorMap* m,
+                            const DecodeArgs& da, cudaStream_t s) {
   switch (G) {
     case 8:
-      if constexpr (D == 64) return launch_decode_dg<D, 8>(grid, m, da, s);
+      if constexpr (D == 64) return launch_decode_dg<D, 8>(grid, loop, m, da, s);
       return cudaErrorInvalidValue;
-    case 4: return launch_decode_dg<D, 4>(grid, m, da, s);
-    case 2: return launch_decode_dg<D, 2>(grid, m, da, s);
-    default: return launch_decode_dg<D, 1>(grid, m, da, s);
+    case 4: return launch_decode_dg<D, 4>(grid, loop, m, da, s);
+    case 2: return launch_decode_dg<D, 2>(grid, loop, m, da, s);
+    default: return launch_decode_dg<D, 1>(grid, loop, m, da, s);
   }
 }
 
@@ -889,9 +951,10 @@ cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
       return cudaErrorInvalidValue;
     const int grid = static_cast<int>(x.n_ctas);
     main_kernel_begin(stream);
-    const cudaError_t e = x.D == 256   ? launch_decode_d<256>(G, grid, maps, da, stream)
-                          : x.D == 128 ? launch_decode_d<128>(G, grid, maps, da, stream)
-                                       : launch_decode_d<64>(G, grid, maps, da, stream);
+    const bool loop = x.loop_shares;
+    const cudaError_t e = x.D == 256   ? launch_decode_d<256>(G, grid, loop, maps, da, stream)
+                          : x.D == 128 ? launch_decode_d<128>(G, grid, loop, maps, da, stream)
+                                       : launch_decode_d<64>(G, grid, loop, maps, da, stream);
     main_kernel_end(stream);
     if (e != cudaSuccess) return e;
     count_launches(1);

@@ -41,6 +41,27 @@ constexpr int kDecodeMinRowsPerCta = 224;
 // rows: only when there are more units than SMs, so that a share holds
 // several unit starts.
 constexpr int kDecodePieceCostRows128 = 96;
+// Forced split counts: most fixed-size shares one CTA takes in turn (each
+// leaves at most two split pieces to count at the CTA's end).
+constexpr int kDecodeLoopSharesPerCta = 256;
+
+// Error codes written to the device status word (first one wins).
+enum DeviceError : uint32_t {
+  kDevOk = 0,
+  kDevTimeoutQ = 0x101,
+  kDevTimeoutKvFull = 0x102,
+  kDevTimeoutKvEmpty = 0x103,
+  kDevTimeoutSFull = 0x104,
+  kDevTimeoutPReady = 0x105,
+  kDevTimeoutOFinal = 0x106,
+  kDevTimeoutDrain = 0x107,
+  kDevTimeoutTurn = 0x108,
+  kDevTimeoutDecodeFull = 0x201,
+  kDevTimeoutDecodeEmpty = 0x202,
+  kDevPendingOverflow = 0x203,  // decode: more split pieces than a CTA can record
+  kDevTimeoutProbe = 0x301,
+};
+
 // Largest persistent prefill grid the workspace's schedule has room for.
 constexpr int kMaxPrefillCtas = 1024;
 
@@ -54,7 +75,8 @@ struct DecodeLaunch {
   long long total;            // rows of the work space (KV heads x head groups x sum L_b)
   long long rows_per_cta;     // cost of each CTA's contiguous share (a row costs 1)
   long long piece_cost;       // cost of a unit start after the first (0: shares of rows)
-  long long n_ctas;           // shares (CTAs)
+  long long n_ctas;           // CTAs to launch
+  bool loop_shares;           // fixed-size shares, more than CTAs (a forced split count)
   int max_slots;              // piece slots per (batch, head) in the partial buffers
   const long long* prefix_host;  // [B + 1] prefix sums of the lengths
   const long long* prefix_dev;   // the same in the workspace, or null (then in params)

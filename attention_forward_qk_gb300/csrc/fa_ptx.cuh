@@ -11,23 +11,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "fa_internal.h"
+
 namespace fa {
 
-// Error codes written to the device status word (first one wins).
-enum DeviceError : uint32_t {
-  kDevOk = 0,
-  kDevTimeoutQ = 0x101,
-  kDevTimeoutKvFull = 0x102,
-  kDevTimeoutKvEmpty = 0x103,
-  kDevTimeoutSFull = 0x104,
-  kDevTimeoutPReady = 0x105,
-  kDevTimeoutOFinal = 0x106,
-  kDevTimeoutDrain = 0x107,
-  kDevTimeoutTurn = 0x108,
-  kDevTimeoutDecodeFull = 0x201,
-  kDevTimeoutDecodeEmpty = 0x202,
-  kDevTimeoutProbe = 0x301,
-};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

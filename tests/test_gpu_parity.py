@@ -258,6 +258,34 @@ def test_decode_shares_by_cost(cuda_device, B, Hq, Hkv, S, D, layout, masked):
     compare(out, lse, ro, rl, layout)
 
 
+@pytest.mark.parametrize("splits", [128, 1024])
+def test_decode_forced_splits_many_shares_per_cta(cuda_device, splits):
+    # a forced split count cuts fixed-size shares (64 rows at 1024 splits):
+    # 2048 shares for 152 CTAs, each CTA taking its shares in turn
+    x = workloads.make_decode(2, 32, 8, 8192, 128, "BNSD", seed=splits, len_lo=5000,
+                              len_hi=8192)
+    out, lse = run_decode(x, scale=0.088, splits=splits)
+    ro, rl = oracle.decode(x["q"], x["k"], x["v"], x["lengths"], scale=0.088, layout="BNSD")
+    compare(out, lse, ro, rl, "BNSD")
+
+
+def test_decode_forced_splits_more_shares_than_ctas_can_hold(cuda_device):
+    # 1024 sequences x 4 heads, 10 shares of 64 rows each: 40 960 shares, more
+    # than 152 CTAs x 256 shares, so the grid grows past the SM count; checked
+    # on a sample of the sequences (the oracle runs per sequence)
+    B, H, S, D = 1024, 4, 640, 64
+    lens = [S] * B
+    lens[3] = lens[700] = 0
+    lens[5], lens[511], lens[1023] = 1, 63, 65
+    x = workloads.make_decode(B, H, H, S, D, "BSND", seed=77, lengths=lens, garbage=False)
+    out, lse = run_decode(x, scale=0.125, splits=10)
+    for b in [0, 3, 5, 6, 200, 511, 700, 701, 1000, 1023]:
+        sl = slice(b, b + 1)
+        ro, rl = oracle.decode(x["q"][sl], x["k"][sl], x["v"][sl], lens[sl], scale=0.125,
+                               layout="BSND")
+        compare(out[sl], lse[sl], ro, rl, "BSND")
+
+
 @pytest.mark.parametrize("B", [257, 1030])
 def test_decode_many_sequences(cuda_device, B):
     # the lengths' prefix sums travel in the larger parameter block (B <= 1024)
