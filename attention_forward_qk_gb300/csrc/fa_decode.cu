@@ -843,8 +843,8 @@ __global__ void __launch_bounds__(128) decode_empty_kernel(const __grid_constant
 template <int D, int G>
 cudaError_t launch_decode_dg(int grid, bool loop, const CUtensorMap* m, const DecodeArgs& da,
                              cudaStream_t stream) {
-  static bool configured = false;  // benign race: idempotent attribute set
-  if (!configured) {
+  static std::atomic<uint64_t> configured{0};  // devices with the attributes set
+  if (setup_needed(configured)) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, G, kSharesRows>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          DecCfg<D, G>::SMEM);
@@ -856,7 +856,7 @@ cudaError_t launch_decode_dg(int grid, bool loop, const CUtensorMap* m, const De
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                DecCfg<D, G>::SMEM + kLoopSmemExtra);
     if (e != cudaSuccess) return e;
-    configured = true;
+    setup_done(configured);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

@@ -5,9 +5,25 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "fa.h"
 
 namespace fa {
+
+// A kernel's one-time set-up (its shared-memory limit) is per device: `done`
+// holds one bit per device on which it has run. Racing first calls both run
+// the set-up, which is idempotent.
+inline bool setup_needed(const std::atomic<uint64_t>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return true;
+  return ((done.load(std::memory_order_acquire) >> dev) & 1u) == 0;
+}
+inline void setup_done(std::atomic<uint64_t>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64)
+    done.fetch_or(uint64_t{1} << dev, std::memory_order_release);
+}
 
 // Encode a 4-D TMA map over a bf16 tensor stored BNSD or BSND, with
 // dimensions ordered (D, S, N, B) so that one box is `box_s` rows of

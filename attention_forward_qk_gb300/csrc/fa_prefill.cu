@@ -904,13 +904,13 @@ template <int D>
 cudaError_t launch_prefill_d(const PrefillLaunch& x, cudaStream_t stream) {
   using C = PCfg<D>;
   constexpr int kBN = C::BN;
-  static bool configured = false;  // benign race: idempotent attribute set
-  if (!configured) {
+  static std::atomic<uint64_t> configured{0};  // devices with the attribute set
+  if (setup_needed(configured)) {
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured = true;
+    setup_done(configured);
   }
   CUtensorMap mq, mk, mv;
   // packed sequences: [T, H, D] tensors, one batch of T rows
