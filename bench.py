@@ -323,6 +323,12 @@ class L2Flush:
         torch.sum(self.r, dim=0, keepdim=True, out=self.sink)
 
 
+def median(xs):
+    s = sorted(xs)
+    n = len(s)
+    return (s[n // 2] + s[(n - 1) // 2]) / 2 if n else None
+
+
 def time_steps(runner, steps, warmup, flush, fn=None, kernel=True):
     """Per-step CUDA-event times (ms) of `fn` (default runner.step) and of the
     main kernel inside it; L2 flushed before every step, outside the events.
@@ -548,7 +554,7 @@ def run_gpu(args):
 
     ms = sum(step_ms) / len(step_ms)
     kms = sum(main_ms) / len(main_ms)
-    ms, kms = max_over_ranks([ms, kms], world, dev)
+    ms, kms, med_ms = max_over_ranks([ms, kms, median(step_ms)], world, dev)
     value, unit = value_of(w.kind, main.units["step"] * world, ms)
 
     # end to end through the public call: pinned host inputs in, results out
@@ -576,6 +582,7 @@ def run_gpu(args):
             o_k = sum(m_ms) / len(m_ms)
             v, u = value_of(wo.kind, r.units["step"], o_ms)
             others[name] = {"value": v, "unit": u, "ms_per_step": o_ms,
+                            "ms_per_step_median": median(s_ms),
                             "config": wo.note,
                             "roofline": roofline(wo.kind, r.units["main"], o_k, peaks, peak_kind,
                                                  name)}
@@ -592,6 +599,7 @@ def run_gpu(args):
             "steps": args.steps,
             "warmup": args.warmup,
             "ms_per_step": ms,
+            "ms_per_step_median": med_ms,
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
