@@ -405,3 +405,39 @@ def test_forward_varlen_window_rejects_before_any_cuda_call(lib, cq, ckv, wl, wr
 def test_forward_varlen_window_null_offsets(lib):
     assert lib.fa_forward_varlen_window(P, P, P, None, None, 3, 0, 1, 4, 2, 128, 0.1, P, None,
                                         WS, 1 << 22, None) == _lib.FA_ERR_NULLPTR
+
+
+C_CONSUMER = r"""
+#include <stdio.h>
+#include "fa.h"
+int main(void) {
+  int64_t lens[2] = {100, 7}, rc = 0, n = 0, mx = 0;
+  fa_status st = fa_decode_plan(2, 128, 8, 2, 128, lens, 152, 0, &rc, &n, &mx);
+  printf("%d %lld %lld %lld %zu\n", (int)st, (long long)rc, (long long)n, (long long)mx,
+         fa_decode_workspace_size(8, 8192, 32, 8, 128, 0));
+  printf("%s\n", fa_status_string(FA_ERR_UNSUPPORTED));
+  return st == FA_OK ? 0 : 1;
+}
+"""
+
+
+def test_header_is_plain_c_and_the_library_links_from_c(lib, tmp_path):
+    """include/fa.h compiles as strict C11 and a C program links the library
+    and calls its host-side entry points (no GPU needed)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_fa.c"
+    src.write_text(C_CONSUMER)
+    exe = tmp_path / "use_fa"
+    libdir = os.path.dirname(_lib.LIB_PATH)
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", os.path.dirname(HEADER), str(src), "-L", libdir, "-lfa_gb300",
+                    f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    st, rc, n, mx, ws = out[0].split()
+    assert (int(st), int(rc), int(n), int(mx)) == (0, 224, 1, 1)
+    assert int(ws) == F.fa_decode_workspace_size(8, 8192, 32, 8, 128, 0)
+    assert out[1] == lib.fa_status_string(_lib.FA_ERR_UNSUPPORTED).decode()
