@@ -7,11 +7,19 @@ from .fa import (  # noqa: F401
     FaError,
     fa_abi_version,
     fa_decode,
+    fa_decode_noalloc,
+    fa_decode_paged,
     fa_decode_plan,
     fa_decode_workspace_size,
     fa_forward,
+    fa_forward_varlen,
+    fa_forward_varlen_window,
+    fa_forward_varlen_workspace_size,
+    fa_forward_window,
     fa_forward_workspace_size,
+    fa_kernel_launch_count,
     fa_selftest_wait_timeout,
+    fa_set_main_kernel_events,
     fa_status_string,
     fa_workspace_status,
 )

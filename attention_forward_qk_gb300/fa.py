@@ -74,6 +74,12 @@ def fa_forward_workspace_size(B, S_q, S_kv, num_heads, num_kv_heads, D) -> int:
     return int(_lib.load().fa_forward_workspace_size(B, S_q, S_kv, num_heads, num_kv_heads, D))
 
 
+def fa_forward_varlen_workspace_size(B, max_seqlen_q, max_seqlen_kv, num_heads, num_kv_heads,
+                                     D) -> int:
+    return int(_lib.load().fa_forward_varlen_workspace_size(B, max_seqlen_q, max_seqlen_kv,
+                                                            num_heads, num_kv_heads, D))
+
+
 def fa_decode_workspace_size(B, S_kv_max, num_heads, num_kv_heads, D, num_splits=0) -> int:
     return int(_lib.load().fa_decode_workspace_size(B, S_kv_max, num_heads, num_kv_heads, D,
                                                     num_splits))
@@ -182,7 +188,7 @@ def _varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, window, mask_mode, scale, num_
         _check_tensor(lse, "lse", torch.float32)
     max_q = max([b - a for a, b in zip(cq[:-1], cq[1:])] + [0])
     max_kv = max([b - a for a, b in zip(ckv[:-1], ckv[1:])] + [0])
-    need = int(_lib.load().fa_forward_varlen_workspace_size(B, max_q, max_kv, Hq, Hkv, D))
+    need = fa_forward_varlen_workspace_size(B, max_q, max_kv, Hq, Hkv, D)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     aq = (ctypes.c_int64 * (B + 1))(*cq)

@@ -257,8 +257,8 @@ class Runner:
         lse_shape = (self.q.shape[0], w.Hq) if w.packed else (w.B, w.Hq, w.S_q)
         self.lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
         if w.packed:
-            n = F._lib.load().fa_forward_varlen_workspace_size(w.B, max(self.lens), max(self.lens),
-                                                               w.Hq, w.Hkv, w.D)
+            n = F.fa_forward_varlen_workspace_size(w.B, max(self.lens), max(self.lens), w.Hq,
+                                                   w.Hkv, w.D)
         elif w.kind == "decode":
             n = F.fa_decode_workspace_size(w.B, w.S_kv, w.Hq, w.Hkv, w.D, 0)
         else:

@@ -441,3 +441,14 @@ def test_header_is_plain_c_and_the_library_links_from_c(lib, tmp_path):
     assert (int(st), int(rc), int(n), int(mx)) == (0, 224, 1, 1)
     assert int(ws) == F.fa_decode_workspace_size(8, 8192, 32, 8, 128, 0)
     assert out[1] == lib.fa_status_string(_lib.FA_ERR_UNSUPPORTED).decode()
+
+
+def test_python_binding_has_every_declared_function():
+    """The binding carries the C ABI's names: every function fa.h declares
+    has a wrapper of the same name, exported by the package."""
+    import attention_forward_qk_gb300 as pkg
+    names = set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", open(HEADER).read()))
+    assert names and all(hasattr(F, n) for n in names), sorted(n for n in names if not hasattr(F, n))
+    assert all(hasattr(pkg, n) for n in names), sorted(n for n in names if not hasattr(pkg, n))
+    assert F.fa_forward_varlen_workspace_size(3, 100, 200, 8, 2, 128) == int(
+        _lib.load().fa_forward_varlen_workspace_size(3, 100, 200, 8, 2, 128))
