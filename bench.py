@@ -671,9 +671,19 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ramp-s", type=float, default=0.5,
                     help="untimed steps before the timed region, in seconds (clock ramp)")
+    ap.add_argument("--oracle-all", action="store_true",
+                    help="time the fp64 oracle on the five configurations (host cores only)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.oracle_all:
+        # the oracle's own throughput on each configuration, a bounded sample
+        # each (whole decode passes; sampled query rows for prefill)
+        for name in ("tiny_prefill", "gqa_decode", "long_decode", "causal_prefill",
+                     "gqa_masked_prefill"):
+            r = cpu_baseline(workloads.WORKLOADS[name], budget_s=10.0)
+            print(json.dumps({"workload": name, **r}), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
