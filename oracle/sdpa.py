@@ -286,15 +286,26 @@ def merge_lse(lses, onorms):
 
 
 def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, *, scale: float = 1.0,
-                     causal: bool = False, window=None):
+                     causal: bool = False, window=None, seqused_q=None, seqused_kv=None,
+                     key_mask=None):
     """Packed variable-length sequences ([FA] §1.3 TND layout, §1.4
     cu_seqlens): q [T_q, Hq, D], k/v [T_kv, Hkv, D]; sequence b is q rows
     cu_q[b]..cu_q[b+1]-1 against k/v rows cu_kv[b]..cu_kv[b+1]-1, each an
     independent attention (causal, or the sliding window of [FA] §1.5 given
     as (win_left, win_right), top-left aligned within the sequence).
+
+    seqused_q / seqused_kv ([FA] §1.4, one per sequence) truncate a
+    sequence's padding: when given together with cu_seqlens the shorter of
+    the two lengths holds. Keys past the used kv length do not exist (as keys
+    past actualSeqLengths, whatever they hold); query rows past the used q
+    length are truncated rows with no valid key, so they read out 0 and lse
+    +inf ([FA] §1.7 names seqused truncation among the causes of an invalid
+    row). key_mask: one flag per packed key row, [T_kv], nonzero = excluded
+    (the per-key mask of the padded layouts laid out as the keys are).
     Returns out [T_q, Hq, D] and lse [T_q, Hq] (the TND lse shape of [FA] §1.6).
     """
     qn, kn, vn = _as_f64(q), _as_f64(k), _as_f64(v)
+    km = _as_np(key_mask)
     T_q, Hq, D = qn.shape
     out = np.zeros((T_q, Hq, D))
     lse = np.full((T_q, Hq), np.inf)
@@ -302,10 +313,17 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, *, scale: float = 1.0
     for b in range(B):
         q0, q1 = int(cu_seqlens_q[b]), int(cu_seqlens_q[b + 1])
         k0, k1 = int(cu_seqlens_kv[b]), int(cu_seqlens_kv[b + 1])
-        if q1 == q0:
+        if seqused_q is not None:
+            q1 = min(q1, q0 + int(seqused_q[b]))  # the shorter length holds
+        n_kv = k1 - k0
+        if seqused_kv is not None:
+            n_kv = min(n_kv, int(seqused_kv[b]))
+        if q1 <= q0:
             continue
         o, l = attention(qn[None, q0:q1], kn[None, k0:k1], vn[None, k0:k1], scale=scale,
-                         layout="BSND", causal=causal, window=window)
+                         layout="BSND", causal=causal, window=window,
+                         key_mask=None if km is None else km[None, k0:k1],
+                         actual_seq_lengths=[n_kv])
         out[q0:q1] = o[0]
         lse[q0:q1] = l[0].T
     return out, lse

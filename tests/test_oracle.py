@@ -431,3 +431,81 @@ def test_varlen_window_equals_per_sequence_bruteforce():
     o2, l2 = oracle.attention_varlen(q, k, v, cu, cu, scale=0.4, causal=True)
     np.testing.assert_array_equal(o1, o2)
     np.testing.assert_array_equal(l1, l2)
+
+
+def _packed_inputs(seed, lq, lkv, Hq=4, Hkv=2, D=5):
+    g = torch.Generator().manual_seed(seed)
+    cq = np.concatenate([[0], np.cumsum(lq)]).astype(np.int64)
+    ckv = np.concatenate([[0], np.cumsum(lkv)]).astype(np.int64)
+    q = torch.randn(int(cq[-1]), Hq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(int(ckv[-1]), Hkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(int(ckv[-1]), Hkv, D, generator=g).to(torch.bfloat16)
+    km = (torch.rand(int(ckv[-1]), generator=g) < 0.3).to(torch.uint8)
+    return q, k, v, km, cq, ckv
+
+
+def test_varlen_seqused_and_key_mask_equal_per_sequence_bruteforce():
+    """seqused_q / seqused_kv ([FA] §1.4: the shorter of seqused and the
+    cu_seqlens span holds) and a per-packed-key mask: each sequence against
+    the scalar-loop definition with its used kv length as the actual length
+    and its slice of the mask; query rows past the used q length are
+    truncated rows (out 0, lse +inf, [FA] §1.7)."""
+    lq, lkv = [5, 3, 7, 4, 2], [5, 6, 7, 4, 3]
+    sq, skv = [3, 9, 7, 0, 2], [4, 2, 9, 4, 0]   # shorter and longer than the spans
+    q, k, v, km, cq, ckv = _packed_inputs(14, lq, lkv)
+    for causal in (False, True):
+        out, lse = oracle.attention_varlen(q, k, v, cq, ckv, scale=0.35, causal=causal,
+                                           seqused_q=sq, seqused_kv=skv, key_mask=km)
+        for b in range(len(lq)):
+            uq = min(lq[b], sq[b])
+            ukv = min(lkv[b], skv[b])
+            qs = q[cq[b]:cq[b] + uq][None]
+            ks, vs = k[ckv[b]:ckv[b + 1]][None], v[ckv[b]:ckv[b + 1]][None]
+            if uq > 0:
+                ro, rl = oracle.attention_bruteforce(qs, ks, vs, scale=0.35, layout="BSND",
+                                                     causal=causal, key_mask=km[None, ckv[b]:ckv[b + 1]],
+                                                     actual_seq_lengths=[ukv])
+                np.testing.assert_allclose(out[cq[b]:cq[b] + uq], ro[0], rtol=0, atol=1e-12)
+                lg, lr = lse[cq[b]:cq[b] + uq], rl[0].T
+                np.testing.assert_array_equal(np.isfinite(lg), np.isfinite(lr))
+                fin = np.isfinite(lr)
+                np.testing.assert_allclose(lg[fin], lr[fin], rtol=0, atol=1e-12)
+                assert np.all(lg[~fin] == np.inf)
+            # truncated rows
+            assert np.all(out[cq[b] + uq:cq[b + 1]] == 0)
+            assert np.all(lse[cq[b] + uq:cq[b + 1]] == np.inf)
+        # the sequence whose used kv length is 0 has only invalid rows
+        assert np.all(lse[cq[4]:cq[5]] == np.inf)
+
+
+def test_varlen_seqused_at_or_past_the_span_changes_nothing():
+    """seqused at least the cu_seqlens span (the span is then the shorter),
+    and an all-zero key mask, give exactly the plain packed result."""
+    lq, lkv = [4, 6, 3], [4, 6, 3]
+    q, k, v, _, cq, ckv = _packed_inputs(15, lq, lkv)
+    o1, l1 = oracle.attention_varlen(q, k, v, cq, ckv, scale=0.5, causal=True)
+    o2, l2 = oracle.attention_varlen(q, k, v, cq, ckv, scale=0.5, causal=True,
+                                     seqused_q=[4, 100, 3], seqused_kv=[9, 6, 1 << 20],
+                                     key_mask=torch.zeros(int(ckv[-1]), dtype=torch.uint8))
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_varlen_truncated_rows_and_keys_have_no_effect():
+    """Whatever the truncated query rows and the keys past seqused_kv hold
+    (NaN and Inf included), the result is the same; only q rows before the
+    used length and keys before it enter the arithmetic."""
+    lq, lkv = [6, 5], [7, 5]
+    sq, skv = [4, 5], [3, 2]
+    q, k, v, km, cq, ckv = _packed_inputs(16, lq, lkv)
+    o1, l1 = oracle.attention_varlen(q, k, v, cq, ckv, scale=0.5, seqused_q=sq, seqused_kv=skv,
+                                     key_mask=km)
+    q2, k2, v2 = q.clone(), k.clone(), v.clone()
+    for b in range(2):
+        q2[cq[b] + sq[b]:cq[b + 1]] = float("nan")
+        k2[ckv[b] + skv[b]:ckv[b + 1]] = float("inf")
+        v2[ckv[b] + skv[b]:ckv[b + 1]] = float("nan")
+    o2, l2 = oracle.attention_varlen(q2, k2, v2, cq, ckv, scale=0.5, seqused_q=sq,
+                                     seqused_kv=skv, key_mask=km)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
