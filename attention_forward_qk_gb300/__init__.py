@@ -8,11 +8,13 @@ from .fa import (  # noqa: F401
     fa_abi_version,
     fa_decode,
     fa_decode_noalloc,
+    fa_decode_noalloc_status,
     fa_decode_paged,
     fa_decode_plan,
     fa_decode_workspace_size,
     fa_forward,
     fa_forward_varlen,
+    fa_forward_varlen_ex,
     fa_forward_varlen_window,
     fa_forward_varlen_workspace_size,
     fa_forward_window,

@@ -45,6 +45,9 @@ SIGNATURES = {
     "fa_forward_varlen_window": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                                 _i64, _i64, ctypes.c_float, _vp, _vp, _vp, _sz,
                                                 _vp]),
+    "fa_forward_varlen_ex": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
+                                            _i64, _i64, _i64, _i64, ctypes.c_float, _vp, _vp,
+                                            _vp, _sz, _vp]),
     "fa_forward_window": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _i64, _i64,
                                          _i64, _i64, _i64, ctypes.c_float, ctypes.c_int, _vp,
                                          _vp, _vp, _sz, _vp]),
@@ -63,6 +66,7 @@ SIGNATURES = {
     "fa_decode_noalloc": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                                          ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp, _vp,
                                          _vp]),
+    "fa_decode_noalloc_status": (ctypes.c_int, [_vp]),
     "fa_set_main_kernel_events": (None, [_vp, _vp]),
     "fa_kernel_launch_count": (ctypes.c_uint64, []),
 }

@@ -84,8 +84,8 @@ PrefillWs prefill_ws(int64_t B, int64_t S_q, int64_t S_kv, int64_t num_heads, in
   size_t off = kAlign;  // status word
   w.sched = off;
   off += align_up(sizeof(int32_t) * (kMaxPrefillCtas + 1 + prefill_items(B, S_q, num_heads, D)));
-  w.varlen = off;  // packed sequences only: [4][B] offsets and lengths
-  off += align_up(sizeof(int32_t) * 4 * B);
+  w.varlen = off;  // packed sequences only: [5][B] offsets, used lengths, q spans
+  off += align_up(sizeof(int32_t) * 5 * B);
   w.lens = off;
   off += align_up(sizeof(int32_t) * B);
   w.bits = off;
@@ -240,19 +240,21 @@ void main_kernel_end(cudaStream_t stream) {
 }
 void count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
 
+// SM count per device ordinal, looked up once per device (a fixed table:
+// no heap allocation on any call)
 int device_sm_count() {
-  static std::mutex mu;
-  static std::vector<int> cache;
+  constexpr int kMaxCachedDevices = 64;
+  static std::atomic<int> cache[kMaxCachedDevices];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  std::lock_guard<std::mutex> lock(mu);
-  if (static_cast<int>(cache.size()) <= dev) cache.resize(dev + 1, 0);
-  if (cache[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cache[dev] = n;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < kMaxCachedDevices) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
   }
-  return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < kMaxCachedDevices) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 }  // namespace fa
@@ -388,14 +390,17 @@ namespace {
 // Shared by fa_forward and fa_forward_window: the window (-1, -1) is no mask,
 // (-1, 0) is causal.
 // cu_q, cu_kv: HOST prefix offsets of packed sequences (else null); then
-// S_q / S_kv are the longest sequences and the tensors are [T, H, D].
+// S_q / S_kv are the longest sequences, the tensors are [T, H, D], key_mask
+// (if any) is one flag per packed key [T_kv], and used_q / used_kv (HOST,
+// nullable) cut each sequence to the shorter of its span and the used length.
 fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok,
                        int64_t win_left, int64_t win_right, const uint8_t* key_mask,
                        const int64_t* lens,
                        int64_t B, int64_t S_q, int64_t S_kv, int64_t num_heads,
                        int64_t num_kv_heads, int64_t D, float scale, int layout, void* out,
                        float* lse, void* workspace, size_t workspace_bytes, void* stream,
-                       const int64_t* cu_q = nullptr, const int64_t* cu_kv = nullptr) {
+                       const int64_t* cu_q = nullptr, const int64_t* cu_kv = nullptr,
+                       const int64_t* used_q = nullptr, const int64_t* used_kv = nullptr) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || workspace == nullptr)
     return FA_ERR_NULLPTR;
   int64_t Hkv = num_kv_heads;
@@ -440,14 +445,24 @@ fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok
   thread_local SchedKey sched_key{-1, 0, 0, 0, 0, 0, 0, 0, 0};
   thread_local std::vector<int32_t> sched;
   const SchedKey key{B, num_heads, Hkv, S_q, S_kv, win_left, win_right, D, grid};
-  std::vector<int32_t> vtab;  // packed sequences: [4][B] q off, q len, kv off, kv len
+  // packed sequences: [5][B] q offset, used q length, kv offset, used kv
+  // length (the shorter of the span and seqused), q span
+  std::vector<int32_t> vtab;
+  bool truncated_q = false, truncated_kv = false;
   if (cu_q != nullptr) {
-    vtab.resize(4 * B);
+    vtab.resize(5 * B);
     for (int64_t b = 0; b < B; ++b) {
+      const int64_t span_q = cu_q[b + 1] - cu_q[b];
+      const int64_t span_kv = cu_kv[b + 1] - cu_kv[b];
+      const int64_t uq = used_q ? std::min(span_q, used_q[b]) : span_q;
+      const int64_t ukv = used_kv ? std::min(span_kv, used_kv[b]) : span_kv;
+      truncated_q = truncated_q || uq < span_q;
+      truncated_kv = truncated_kv || ukv < span_kv;
       vtab[b] = static_cast<int32_t>(cu_q[b]);
-      vtab[B + b] = static_cast<int32_t>(cu_q[b + 1] - cu_q[b]);
+      vtab[B + b] = static_cast<int32_t>(uq);
       vtab[2 * B + b] = static_cast<int32_t>(cu_kv[b]);
-      vtab[3 * B + b] = static_cast<int32_t>(cu_kv[b + 1] - cu_kv[b]);
+      vtab[3 * B + b] = static_cast<int32_t>(ukv);
+      vtab[4 * B + b] = static_cast<int32_t>(span_q);
     }
     // depends on the lengths: built for every call
     build_prefill_schedule(B, num_heads, Hkv, S_q, S_kv, win_left, win_right, grid, IR, BN,
@@ -468,14 +483,32 @@ fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok
   if (cudaMemcpyAsync(wsb, blob.data(), blob.size() * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return FA_ERR_RUNTIME;
   const uint32_t* bits = nullptr;
-  if ((key_mask != nullptr || lens != nullptr) && S_kv > 0) {
+  const int32_t* vtab_dev =
+      cu_q != nullptr ? reinterpret_cast<const int32_t*>(wsb + ws.varlen) : nullptr;
+  // the validity table also zeroes the V rows of excluded keys: needed for a
+  // key mask, for lengths, and for packed keys cut by seqused_kv (the rows
+  // past a used length may hold anything)
+  if ((key_mask != nullptr || lens != nullptr || truncated_kv) && S_kv > 0) {
     uint32_t* bits_dev = reinterpret_cast<uint32_t*>(wsb + ws.bits);
     const int* lens_dev = lens ? reinterpret_cast<const int*>(wsb + ws.lens) : nullptr;
-    if (launch_tile_bits(key_mask, lens_dev, static_cast<int>(B), static_cast<int>(S_kv),
-                         bits_dev, s) != cudaSuccess)
+    // packed: the keys of sequence b start at its kv offset and end at its
+    // used kv length (both in the table)
+    if (launch_tile_bits(key_mask, lens_dev, vtab_dev, static_cast<int>(B),
+                         static_cast<int>(S_kv), bits_dev, s) != cudaSuccess)
       return FA_ERR_RUNTIME;
     count_launches(1);
     bits = bits_dev;
+  }
+  if (truncated_q) {
+    // query rows past a sequence's used length: out 0, lse +inf (the prefill
+    // kernel writes only the used rows)
+    int64_t most = 0;
+    for (int64_t b = 0; b < B; ++b) most = std::max<int64_t>(most, vtab[4 * B + b] - vtab[B + b]);
+    if (launch_truncated_rows(vtab_dev, static_cast<int>(B), static_cast<int>(most),
+                              static_cast<int>(num_heads), static_cast<int>(D), out, lse,
+                              s) != cudaSuccess)
+      return FA_ERR_RUNTIME;
+    count_launches(1);
   }
   PrefillLaunch x;
   x.q = q;
@@ -494,7 +527,7 @@ fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok
   x.tile_bits = bits;
   x.sched = reinterpret_cast<const int32_t*>(wsb + ws.sched);
   x.grid = grid;
-  x.varlen = cu_q != nullptr ? reinterpret_cast<const int32_t*>(wsb + ws.varlen) : nullptr;
+  x.varlen = vtab_dev;
   x.T_q = cu_q != nullptr ? cu_q[B] : 0;
   x.T_kv = cu_kv != nullptr ? cu_kv[B] : 0;
   x.out = out;
@@ -533,10 +566,11 @@ namespace {
 // the window (-1, -1) no mask, (-1, 0) causal
 fa_status forward_varlen_impl(const void* q, const void* k, const void* v,
                               const int64_t* cu_seqlens_q, const int64_t* cu_seqlens_kv,
-                              bool mask_ok, int64_t win_left, int64_t win_right, int64_t B,
-                              int64_t num_heads, int64_t num_kv_heads, int64_t D, float scale,
-                              void* out, float* lse, void* workspace, size_t workspace_bytes,
-                              void* stream) {
+                              const int64_t* seqused_q, const int64_t* seqused_kv,
+                              const uint8_t* key_mask, bool mask_ok, int64_t win_left,
+                              int64_t win_right, int64_t B, int64_t num_heads,
+                              int64_t num_kv_heads, int64_t D, float scale, void* out, float* lse,
+                              void* workspace, size_t workspace_bytes, void* stream) {
   if (cu_seqlens_q == nullptr || cu_seqlens_kv == nullptr) return FA_ERR_NULLPTR;
   if (B < 0) return FA_ERR_PARAM_INVALID;
   if (cu_seqlens_q[0] != 0 || cu_seqlens_kv[0] != 0) return FA_ERR_PARAM_INVALID;
@@ -545,14 +579,17 @@ fa_status forward_varlen_impl(const void* q, const void* k, const void* v,
     const int64_t lq = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
     const int64_t lkv = cu_seqlens_kv[b + 1] - cu_seqlens_kv[b];
     if (lq < 0 || lkv < 0) return FA_ERR_PARAM_INVALID;
+    if ((seqused_q != nullptr && seqused_q[b] < 0) || (seqused_kv != nullptr && seqused_kv[b] < 0))
+      return FA_ERR_PARAM_INVALID;
     max_q = std::max(max_q, lq);
     max_kv = std::max(max_kv, lkv);
   }
   if (cu_seqlens_q[B] > kMaxDim || cu_seqlens_kv[B] > kMaxDim) return FA_ERR_PARAM_INVALID;
   // packed tensors [T, H, D] are BSND with one batch
-  return forward_impl(q, k, v, mask_ok, win_left, win_right, nullptr, nullptr, B, max_q, max_kv,
+  return forward_impl(q, k, v, mask_ok, win_left, win_right, key_mask, nullptr, B, max_q, max_kv,
                       num_heads, num_kv_heads, D, scale, FA_LAYOUT_BSND, out, lse, workspace,
-                      workspace_bytes, stream, cu_seqlens_q, cu_seqlens_kv);
+                      workspace_bytes, stream, cu_seqlens_q, cu_seqlens_kv, seqused_q,
+                      seqused_kv);
 }
 }  // namespace
 
@@ -563,9 +600,9 @@ fa_status fa_forward_varlen(const void* q, const void* k, const void* v,
                             size_t workspace_bytes, void* stream) {
   const bool mask_ok = mask_mode == FA_MASK_NONE || mask_mode == FA_MASK_CAUSAL;
   const bool causal = mask_mode == FA_MASK_CAUSAL;
-  return forward_varlen_impl(q, k, v, cu_seqlens_q, cu_seqlens_kv, mask_ok, -1, causal ? 0 : -1,
-                             B, num_heads, num_kv_heads, D, scale, out, lse, workspace,
-                             workspace_bytes, stream);
+  return forward_varlen_impl(q, k, v, cu_seqlens_q, cu_seqlens_kv, nullptr, nullptr, nullptr,
+                             mask_ok, -1, causal ? 0 : -1, B, num_heads, num_kv_heads, D, scale,
+                             out, lse, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_forward_varlen_window(const void* q, const void* k, const void* v,
@@ -574,9 +611,21 @@ fa_status fa_forward_varlen_window(const void* q, const void* k, const void* v,
                                    int64_t num_heads, int64_t num_kv_heads, int64_t D, float scale,
                                    void* out, float* lse, void* workspace,
                                    size_t workspace_bytes, void* stream) {
-  return forward_varlen_impl(q, k, v, cu_seqlens_q, cu_seqlens_kv, true, win_left, win_right, B,
-                             num_heads, num_kv_heads, D, scale, out, lse, workspace,
-                             workspace_bytes, stream);
+  return forward_varlen_impl(q, k, v, cu_seqlens_q, cu_seqlens_kv, nullptr, nullptr, nullptr,
+                             true, win_left, win_right, B, num_heads, num_kv_heads, D, scale,
+                             out, lse, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_forward_varlen_ex(const void* q, const void* k, const void* v,
+                               const int64_t* cu_seqlens_q, const int64_t* cu_seqlens_kv,
+                               const int64_t* seqused_q, const int64_t* seqused_kv,
+                               const uint8_t* key_mask, int64_t win_left, int64_t win_right,
+                               int64_t B, int64_t num_heads, int64_t num_kv_heads, int64_t D,
+                               float scale, void* out, float* lse, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  return forward_varlen_impl(q, k, v, cu_seqlens_q, cu_seqlens_kv, seqused_q, seqused_kv,
+                             key_mask, true, win_left, win_right, B, num_heads, num_kv_heads, D,
+                             scale, out, lse, workspace, workspace_bytes, stream);
 }
 
 fa_status fa_forward_window(const void* q, const void* k, const void* v, int64_t win_left,
@@ -597,13 +646,20 @@ struct PagedKv {
   int64_t max_blocks, num_blocks, block_size;
 };
 
+// scratch: when given, the workspace is not the caller's but the one this
+// function returns (the library-owned array of fa_decode_noalloc, looked up
+// only after every argument check); it need only hold what this call's plan
+// uses. Otherwise the workspace must hold the size query's bound, as the
+// contract of fa_decode states.
 fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv* pg,
                       const uint8_t* key_mask, const int64_t* lens, int64_t B, int64_t S_kv_max,
                       int64_t num_heads, int64_t num_kv_heads, int64_t D, float scale, int layout,
                       int num_splits, void* out, float* lse, void* workspace,
-                      size_t workspace_bytes, void* stream) {
-  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || workspace == nullptr ||
-      lens == nullptr)
+                      size_t workspace_bytes, void* stream,
+                      fa_status (*scratch)(void**) = nullptr) {
+  const bool exact_ws = scratch != nullptr;
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr ||
+      (workspace == nullptr && !exact_ws) || lens == nullptr)
     return FA_ERR_NULLPTR;
   int64_t Hkv = num_kv_heads;
   fa_status st = check_common(B, 1, S_kv_max, num_heads, Hkv, D, scale, layout);
@@ -614,7 +670,9 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
     return FA_ERR_PARAM_INVALID;
   for (int64_t b = 0; b < B; ++b)
     if (lens[b] < 0 || lens[b] > S_kv_max) return FA_ERR_PARAM_INVALID;
-  if (workspace_bytes < fa_decode_workspace_size(B, S_kv_max, num_heads, Hkv, D, num_splits))
+  if (exact_ws && B > kDecodeParamBatches) return FA_ERR_PARAM_INVALID;
+  if (!exact_ws &&
+      workspace_bytes < fa_decode_workspace_size(B, S_kv_max, num_heads, Hkv, D, num_splits))
     return FA_ERR_WORKSPACE_TOO_SMALL;
   if (B == 0) return FA_OK;
 
@@ -635,8 +693,13 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
   if (st != FA_OK) return st;
   const int64_t slots = std::max<int64_t>(max_slots, 1);
   if (slots > max_slots_bound(S_kv_max, num_splits)) return FA_ERR_RUNTIME;  // cannot happen
-  const DecodeWs ws = decode_ws(B, num_heads, D, slots);
+  // partial buffers only when some sequence is cut into several pieces
+  const DecodeWs ws = decode_ws(B, num_heads, D, max_slots > 1 ? slots : 0);
   if (workspace_bytes < ws.total) return FA_ERR_WORKSPACE_TOO_SMALL;
+  if (exact_ws) {
+    st = scratch(&workspace);
+    if (st != FA_OK) return st;
+  }
 
   // length prefix sums: on the stack for batches that travel in the launch
   // parameters, on the heap only for larger ones
@@ -786,3 +849,15 @@ void fa_set_main_kernel_events(void* before, void* after) {
 uint64_t fa_kernel_launch_count(void) { return g_launches.load(); }
 
 }  // extern "C"
+
+namespace fa {
+fa_status decode_on_scratch(const void* q, const void* k, const void* v,
+                            const uint8_t* key_mask, const int64_t* lens, int64_t B,
+                            int64_t S_kv_max, int64_t num_heads, int64_t num_kv_heads, int64_t D,
+                            float scale, int layout, int num_splits, void* out, float* lse,
+                            fa_status (*scratch)(void**), size_t scratch_bytes, void* stream) {
+  return decode_impl(q, k, v, nullptr, key_mask, lens, B, S_kv_max, num_heads, num_kv_heads, D,
+                     scale, layout, num_splits, out, lse, nullptr, scratch_bytes, stream,
+                     scratch);
+}
+}  // namespace fa

@@ -125,9 +125,9 @@ struct PrefillLaunch {
   float scale;
   const uint32_t* tile_bits;  // [B][ceil(S_kv/128)][4] or null
   const int32_t* sched;       // per-CTA work-item lists (offsets[grid + 1], then the lists)
-  // packed sequences: [4][B] q offset, q length, kv offset, kv length (device),
-  // or null; then q/k/v/out are [T, H, D] (BSND with B = 1 in the tile maps),
-  // S_q / S_kv the longest sequence and lse [T_q, Hq]
+  // packed sequences: [5][B] q offset, used q length, kv offset, used kv
+  // length, q span (device), or null; then q/k/v/out are [T, H, D] (BSND with
+  // B = 1 in the tile maps), S_q / S_kv the longest span and lse [T_q, Hq]
   const int32_t* varlen;
   long long T_q, T_kv;        // packed rows of q and k/v (packed sequences only)
   int grid;                   // persistent CTAs
@@ -139,11 +139,29 @@ struct PrefillLaunch {
 cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t stream);
 
 // Build the per-(batch, 128-key tile) validity bit table from an optional
-// key mask and optional device lengths.
-cudaError_t launch_tile_bits(const uint8_t* key_mask, const int* lens_dev, int B, int S_kv,
-                             uint32_t* bits, cudaStream_t stream);
+// key mask and optional device lengths; for packed sequences (varlen = the
+// device [5][B] table) the mask is one flag per packed key and each
+// sequence's keys end at its used kv length.
+cudaError_t launch_tile_bits(const uint8_t* key_mask, const int* lens_dev, const int32_t* varlen,
+                             int B, int S_kv, uint32_t* bits, cudaStream_t stream);
+
+// Packed sequences: out = 0, lse = +inf for the query rows between each
+// sequence's used length and its span (varlen = the device [5][B] table;
+// most_rows = the largest such gap).
+cudaError_t launch_truncated_rows(const int32_t* varlen, int B, int most_rows, int Hq, int D,
+                                  void* out, float* lse, cudaStream_t stream);
 
 cudaError_t launch_wait_probe(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+
+// fa_decode on a library-owned scratch array of scratch_bytes whose device
+// address `scratch` returns: every argument is checked (host only) before it
+// is called, and the array need only hold this call's plan (not the size
+// query's bound); used by fa_decode_noalloc. Same checks and errors otherwise.
+fa_status decode_on_scratch(const void* q, const void* k, const void* v,
+                            const uint8_t* key_mask, const int64_t* lens, int64_t B,
+                            int64_t S_kv_max, int64_t num_heads, int64_t num_kv_heads, int64_t D,
+                            float scale, int layout, int num_splits, void* out, float* lse,
+                            fa_status (*scratch)(void**), size_t scratch_bytes, void* stream);
 
 // Diagnostics: events recorded around the main kernel (thread-local, may be
 // null) and a process-wide count of kernel launches.

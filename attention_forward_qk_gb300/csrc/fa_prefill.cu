@@ -875,17 +875,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// One 128-bit validity word set per (batch, 128-key tile). Padded layouts:
+// key j of batch b is valid iff j < S_kv, j < lens[b] and key_mask[b][j] == 0.
+// Packed sequences (varlen = the [5][B] table): key j of sequence b is valid
+// iff j < its used kv length and the flag of its packed row (kv offset + j)
+// is 0.
 __global__ void tile_bits_kernel(const uint8_t* __restrict__ key_mask, const int* __restrict__ lens,
-                                 int S_kv, int n_tiles, uint32_t* __restrict__ bits) {
+                                 const int32_t* __restrict__ varlen, int B, int S_kv, int n_tiles,
+                                 uint32_t* __restrict__ bits) {
   const int tile = blockIdx.x;
   const int b = blockIdx.y;
   const int key = tile * kBitsTile + threadIdx.x;
   bool valid = key < S_kv;
+  size_t mask_at = static_cast<size_t>(b) * S_kv + key;
+  if (varlen != nullptr) {
+    valid = key < __ldg(varlen + 3 * B + b);
+    mask_at = static_cast<size_t>(__ldg(varlen + 2 * B + b)) + key;
+  }
   if (valid && lens != nullptr) valid = key < lens[b];
-  if (valid && key_mask != nullptr) valid = key_mask[static_cast<size_t>(b) * S_kv + key] == 0;
+  if (valid && key_mask != nullptr) valid = key_mask[mask_at] == 0;
   const uint32_t word = __ballot_sync(0xffffffffu, valid);
   if ((threadIdx.x & 31) == 0)
     bits[(static_cast<size_t>(b) * n_tiles + tile) * 4 + (threadIdx.x >> 5)] = word;
+}
+
+// Packed sequences cut by seqused_q: the query rows between a sequence's used
+// length and its span get out = 0 and lse = +inf (rows with no valid key,
+// FlashAttn guide §1.7). One thread per 16-byte chunk of such a row and head;
+// blockIdx.y is the sequence.
+template <int D>
+__global__ void truncated_rows_kernel(const int32_t* __restrict__ varlen, int B, int Hq,
+                                      __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+  constexpr int kChunks = D / 8;  // 16-byte chunks of a row of one head
+  const int b = blockIdx.y;
+  const int q_off = __ldg(varlen + b);
+  const int used = __ldg(varlen + B + b);
+  const int span = __ldg(varlen + 4 * B + b);
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<long long>(span - used) * Hq * kChunks) return;
+  const int r = static_cast<int>(idx / (Hq * kChunks));
+  const int h = static_cast<int>((idx / kChunks) % Hq);
+  const int c = static_cast<int>(idx % kChunks);
+  const long long row = static_cast<long long>(q_off) + used + r;  // packed row
+  reinterpret_cast<uint4*>(out + (row * Hq + h) * D)[c] = make_uint4(0u, 0u, 0u, 0u);
+  if (c == 0 && lse != nullptr) lse[row * Hq + h] = INFINITY;
 }
 
 __global__ void wait_probe_kernel(uint32_t* status, uint64_t timeout_ns) {
@@ -967,11 +1000,23 @@ cudaError_t launch_prefill(const PrefillLaunch& x, cudaStream_t stream) {
                       : launch_prefill_d<64>(x, stream);
 }
 
-cudaError_t launch_tile_bits(const uint8_t* key_mask, const int* lens_dev, int B, int S_kv,
-                             uint32_t* bits, cudaStream_t stream) {
+cudaError_t launch_tile_bits(const uint8_t* key_mask, const int* lens_dev, const int32_t* varlen,
+                             int B, int S_kv, uint32_t* bits, cudaStream_t stream) {
   const int n_tiles = (S_kv + kBitsTile - 1) / kBitsTile;
-  tile_bits_kernel<<<dim3(n_tiles, B), kBitsTile, 0, stream>>>(key_mask, lens_dev, S_kv, n_tiles,
-                                                               bits);
+  tile_bits_kernel<<<dim3(n_tiles, B), kBitsTile, 0, stream>>>(key_mask, lens_dev, varlen, B,
+                                                               S_kv, n_tiles, bits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_truncated_rows(const int32_t* varlen, int B, int most_rows, int Hq, int D,
+                                  void* out, float* lse, cudaStream_t stream) {
+  if (B == 0 || most_rows == 0) return cudaSuccess;
+  const long long work = static_cast<long long>(most_rows) * Hq * (D / 8);
+  const dim3 grid(static_cast<unsigned>((work + 255) / 256), B);
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+  if (D == 256) truncated_rows_kernel<256><<<grid, 256, 0, stream>>>(varlen, B, Hq, o, lse);
+  else if (D == 128) truncated_rows_kernel<128><<<grid, 256, 0, stream>>>(varlen, B, Hq, o, lse);
+  else truncated_rows_kernel<64><<<grid, 256, 0, stream>>>(varlen, B, Hq, o, lse);
   return cudaGetLastError();
 }
 

@@ -162,8 +162,21 @@ def fa_forward_varlen_window(q, k, v, cu_seqlens_q, cu_seqlens_kv, win_left, win
                    scale, num_heads, out, lse, return_lse, workspace, stream)
 
 
+def fa_forward_varlen_ex(q, k, v, cu_seqlens_q, cu_seqlens_kv, *, seqused_q=None,
+                         seqused_kv=None, key_mask=None, win_left=-1, win_right=-1, scale=1.0,
+                         num_heads=None, num_kv_heads=None, out=None, lse=None, return_lse=True,
+                         workspace=None, stream=None):
+    """Packed sequences with the used lengths (seqused_q / seqused_kv, host
+    sequences of B entries: the shorter of the span and the used length
+    holds; truncated query rows read out 0, lse +inf), a per-packed-key mask
+    (device uint8 [T_kv], nonzero = excluded) and a window ((-1, 0) causal)."""
+    return _varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, (int(win_left), int(win_right)), None,
+                   scale, num_heads, out, lse, return_lse, workspace, stream,
+                   ex=(seqused_q, seqused_kv, key_mask))
+
+
 def _varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, window, mask_mode, scale, num_heads, out, lse,
-            return_lse, workspace, stream):
+            return_lse, workspace, stream, ex=None):
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check_tensor(t, n)
     if q.dim() != 3 or k.dim() != 3 or tuple(v.shape) != tuple(k.shape):
@@ -196,7 +209,21 @@ def _varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, window, mask_mode, scale, num_
     tail = (B, Hq, Hkv, D, float(scale), out.data_ptr(),
             lse.data_ptr() if lse is not None else None, workspace.data_ptr(),
             workspace.numel() * workspace.element_size(), _stream_ptr(stream))
-    if window is None:
+    if ex is not None:
+        used_q, used_kv, km = ex
+        uq = (ctypes.c_int64 * B)(*[int(x) for x in used_q]) if used_q is not None else None
+        ukv = (ctypes.c_int64 * B)(*[int(x) for x in used_kv]) if used_kv is not None else None
+        if (used_q is not None and len(used_q) != B) or (used_kv is not None and len(used_kv) != B):
+            raise ValueError("seqused_q / seqused_kv need B entries")
+        if km is not None:
+            _check_tensor(km, "key_mask", torch.uint8)
+            if km.numel() != T_kv:
+                raise ValueError("key_mask needs one flag per packed key row")
+        st = _lib.load().fa_forward_varlen_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), aq, akv,
+                                              uq, ukv, km.data_ptr() if km is not None else None,
+                                              window[0], window[1], *tail)
+        check(st, "fa_forward_varlen_ex")
+    elif window is None:
         st = _lib.load().fa_forward_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), aq, akv,
                                            MASK_MODES.get(mask_mode, mask_mode), *tail)
         check(st, "fa_forward_varlen")
@@ -339,6 +366,12 @@ def fa_decode_noalloc(q, k, v, actual_seq_lengths, *, key_mask=None, scale=1.0, 
         lse.data_ptr() if lse is not None else None, _stream_ptr(stream))
     check(st, "fa_decode_noalloc")
     return out, lse
+
+
+def fa_decode_noalloc_status(stream=None) -> int:
+    """Synchronise the stream and read/clear the status word of the scratch
+    array fa_decode_noalloc uses on the current device."""
+    return int(_lib.load().fa_decode_noalloc_status(_stream_ptr(stream)))
 
 
 def fa_workspace_status(workspace, stream=None) -> int:

@@ -6,9 +6,10 @@
 One step is one call of the library's public entry point over one batch of
 the workload (default: the GQA decode workload, B=8, Hq=32, Hkv=8, D=128,
 KV cache padded to 8192 rows with per-batch lengths ~U[1024, 8192]). The
-line also carries the other headline workloads measured in the same run
-(long-context decode, causal prefill, GQA prefill with key padding, tiny
-prefill) under "workloads".
+line also carries, in short form, the workloads beyond the five
+configurations ("next_rows"), the decode split-count and warm-L2 sweeps
+("decode_sweeps") and, last, all five configurations ("configs": step rate,
+step and kernel times, the kernel's roofline fraction and DRAM traffic).
 
 Timing: W untimed warm-up steps, then exactly K steps, each bracketed by
 CUDA events on the launching stream; L2 is flushed (512 MB write) between
@@ -44,6 +45,12 @@ METRIC = "prefill attn TFLOP/s & decode KV-read GB/s on 1 GB300, as % of rooflin
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 512 * 1024 * 1024  # written, then half as much read: both above L2 (126 MB)
 MAIN_KERNEL = {"decode": "decode_kernel", "prefill": "prefill_kernel"}
+# the five configurations of the problem statement, by their workload names
+CONFIGS = {"C1": "tiny_prefill", "C2": "gqa_decode", "C3": "long_decode",
+           "C4": "causal_prefill", "C5": "gqa_masked_prefill"}
+OTHER_WORKLOADS = ("long_decode", "causal_prefill", "gqa_masked_prefill", "tiny_prefill",
+                   "window_prefill", "varlen_prefill", "d256_prefill", "paged_decode",
+                   "d256_decode", "batch_decode", "gqa_decode")
 KERNEL_SOURCE = {"decode": "attention_forward_qk_gb300/csrc/fa_decode.cu",
                  "prefill": "attention_forward_qk_gb300/csrc/fa_prefill.cu"}
 
@@ -323,6 +330,24 @@ class L2Flush:
         torch.sum(self.r, dim=0, keepdim=True, out=self.sink)
 
 
+def sig(x, n=4):
+    """x rounded to n significant digits (None stays None)."""
+    return None if x is None else float(f"{x:.{n}g}")
+
+
+def summary(r, full=False):
+    """Short form of one workload's measurement for the JSON line: step rate,
+    step and main-kernel times, the kernel's roofline fraction (and, for the
+    five configurations, its achieved rate, bound and DRAM traffic)."""
+    rf = r["roofline"]
+    d = {"value": sig(r["value"]), "unit": r["unit"], "ms": sig(r["ms_per_step"]),
+         "kernel_ms": sig(r["kernel_ms"]), "frac": sig(rf["frac"], 3)}
+    if full:
+        d.update({"kernel": rf["kernel"], "bound": rf["bound"], "achieved": sig(rf["achieved"]),
+                  "traffic": rf["traffic"]})
+    return d
+
+
 def median(xs):
     s = sorted(xs)
     n = len(s)
@@ -482,7 +507,7 @@ def decode_sweeps(args, dev, flush, peaks, peak_kind):
     equal share per SM, and the GQA decode workload with L2 left warm between
     steps (its valid K/V rows, about 120 MB, then partly hit in the 126 MB L2)."""
     import torch
-    out = {"long_decode_num_splits": {}, "gqa_decode_warm_l2": None}
+    out = {"C3_num_splits": {}, "C2_warm_l2": None}
     wl = workloads.WORKLOADS["long_decode"]
     r = Runner(wl, dev)
     for n in (0, 128, 256, 512, 1024):
@@ -494,8 +519,9 @@ def decode_sweeps(args, dev, flush, peaks, peak_kind):
         o_ms, o_k = sum(s_ms) / len(s_ms), sum(m_ms) / len(m_ms)
         v, u = value_of("decode", r.units["step"], o_ms)
         rf = roofline("decode", r.units["main"], o_k, peaks, peak_kind, "long_decode")
-        out["long_decode_num_splits"][str(n) if n else "0 (one share per SM)"] = {
-            "value": v, "unit": u, "ms_per_step": o_ms, "kernel_frac": rf["frac"]}
+        # key "0": one equal share per SM (the default plan)
+        out["C3_num_splits"][str(n)] = {"value": sig(v), "unit": u, "ms": sig(o_ms),
+                                        "frac": sig(rf["frac"], 3)}
     del r
     torch.cuda.empty_cache()
     wg = workloads.WORKLOADS["gqa_decode"]
@@ -505,9 +531,8 @@ def decode_sweeps(args, dev, flush, peaks, peak_kind):
     o_ms, o_k = sum(s_ms) / len(s_ms), sum(m_ms) / len(m_ms)
     v, u = value_of("decode", r.units["step"], o_ms)
     rf = roofline("decode", r.units["main"], o_k, peaks, peak_kind, "gqa_decode")
-    out["gqa_decode_warm_l2"] = {"value": v, "unit": u, "ms_per_step": o_ms,
-                                 "kernel_frac": rf["frac"],
-                                 "l2": "not flushed between steps"}
+    out["C2_warm_l2"] = {"value": sig(v), "unit": u, "ms": sig(o_ms),
+                         "frac": sig(rf["frac"], 3), "l2": "not flushed between steps"}
     del r
     torch.cuda.empty_cache()
     return out
@@ -569,9 +594,7 @@ def run_gpu(args):
 
     others, sweeps = {}, None
     if not args.only:
-        for name in ("long_decode", "causal_prefill", "gqa_masked_prefill", "tiny_prefill",
-                     "window_prefill", "varlen_prefill", "d256_prefill", "paged_decode",
-                     "d256_decode", "batch_decode", "gqa_decode"):
+        for name in OTHER_WORKLOADS:
             if name == args.workload:
                 continue
             wo = workloads.WORKLOADS[name]
@@ -582,8 +605,7 @@ def run_gpu(args):
             o_k = sum(m_ms) / len(m_ms)
             v, u = value_of(wo.kind, r.units["step"], o_ms)
             others[name] = {"value": v, "unit": u, "ms_per_step": o_ms,
-                            "ms_per_step_median": median(s_ms),
-                            "config": wo.note,
+                            "ms_per_step_median": median(s_ms), "kernel_ms": o_k,
                             "roofline": roofline(wo.kind, r.units["main"], o_k, peaks, peak_kind,
                                                  name)}
             del r
@@ -591,6 +613,9 @@ def run_gpu(args):
         sweeps = decode_sweeps(args, dev, flush, peaks, peak_kind)
 
     if rank == 0:
+        main_rf = roofline(w.kind, main.units["main"], kms, peaks, peak_kind, w.name)
+        others[w.name] = {"value": value, "unit": unit, "ms_per_step": ms, "kernel_ms": kms,
+                          "roofline": main_rf}
         line = {
             "metric": METRIC,
             "value": value,
@@ -608,16 +633,23 @@ def run_gpu(args):
             "config": {"workload": w.name, "shape": w.note, "l2": "flushed between steps "
                        "(512 MB write then 256 MB read, outside the timed events)",
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
-            "roofline": roofline(w.kind, main.units["main"], kms, peaks, peak_kind, w.name),
+            "roofline": main_rf,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": unit, "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": main.h2d_bytes(),
                     "d2h_bytes_per_step": main.d2h_bytes()},
             "gpu_launches": int(launches),
             "clocks": clocks,
-            "workloads": others,
-            "decode_sweeps": sweeps,
         }
+        if not args.only:
+            # the workloads beyond the five configurations, then the sweeps, then
+            # the five configurations last and compact (a reader that keeps only
+            # the end of the line still sees all five)
+            line["next_rows"] = {n: summary(others[n]) for n in OTHER_WORKLOADS
+                                 if n in others and n not in CONFIGS.values()}
+            line["decode_sweeps"] = sweeps
+            line["configs"] = {f"{c} {n}": summary(others[n], full=True)
+                               for c, n in CONFIGS.items() if n in others}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

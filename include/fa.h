@@ -160,6 +160,32 @@ fa_status fa_forward_varlen_window(const void* q, const void* k, const void* v,
                                    void* out, float* lse, void* workspace,
                                    size_t workspace_bytes, void* stream);
 
+/* The packed-sequence forward with every option of FlashAttn guide §1.3-§1.5
+ * at once: the used lengths of §1.4 and a key mask, with causal or a window.
+ *   seqused_q, seqused_kv  NULL or HOST int64 [B], each >= 0: sequence b uses
+ *            the first min(cu_q[b+1] - cu_q[b], seqused_q[b]) query rows and
+ *            the first min(cu_kv[b+1] - cu_kv[b], seqused_kv[b]) keys of its
+ *            span (when both are given the shorter length holds, §1.4). Keys
+ *            past the used kv length are ignored whatever they hold; query
+ *            rows past the used q length are truncated rows: out 0, lse +inf
+ *            (§1.7 counts seqused truncation among the causes of a row with
+ *            no valid key)
+ *   key_mask NULL or device uint8 [T_kv], one flag per packed key row
+ *            (nonzero = excluded), shared by all heads and query rows
+ *   win_left, win_right  the window of fa_forward_varlen_window: (-1, -1) no
+ *            mask, (-1, 0) causal; causal and windows need equal q and kv
+ *            spans per sequence (cu_seqlens), top-left aligned within it
+ * The other arguments, the workspace (fa_forward_varlen_workspace_size with
+ * the longest spans) and the errors are those of fa_forward_varlen; a
+ * negative seqused entry is FA_ERR_PARAM_INVALID. */
+fa_status fa_forward_varlen_ex(const void* q, const void* k, const void* v,
+                               const int64_t* cu_seqlens_q, const int64_t* cu_seqlens_kv,
+                               const int64_t* seqused_q, const int64_t* seqused_kv,
+                               const uint8_t* key_mask, int64_t win_left, int64_t win_right,
+                               int64_t B, int64_t num_heads, int64_t num_kv_heads, int64_t D,
+                               float scale, void* out, float* lse, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
 /* Fused attention forward with a sliding window (FlashAttn guide §1.5,
  * mask_mode 4: a band of win_left tokens before and win_right tokens after
  * each query). Query row i keeps key j iff
@@ -270,22 +296,38 @@ fa_status fa_decode_plan(int64_t B, int64_t S_kv_max, int64_t num_heads, int64_t
  * global memory that the library owns: every GPU that loads the library
  * holds that array until the process exits. This entry point has no
  * counterpart on the pages; it is a packaging variant of fa_decode.
- *   - Limits: the scratch fa_decode_workspace_size(...) reports must fit in
- *     FA_NOALLOC_SCRATCH_BYTES, else FA_ERR_WORKSPACE_TOO_SMALL; B must be
- *     at most 1024, else FA_ERR_PARAM_INVALID. Nothing is enqueued then.
- *   - The first call on a device looks up the array's device address (with
- *     that device current); make that first call before any stream capture.
+ *   - Limits: the part of the array this call's split plan uses (the plan
+ *     fa_decode would make for these lengths on this device; its partial
+ *     results take 4 * B * num_heads * (D + 1) bytes per piece slot, none
+ *     when no sequence is cut) must fit in FA_NOALLOC_SCRATCH_BYTES, else
+ *     FA_ERR_WORKSPACE_TOO_SMALL; B must be at most 1024, else
+ *     FA_ERR_PARAM_INVALID. Nothing is enqueued then. (The long-context
+ *     shape B = 1, 32 heads, D = 128, 131072 keys needs well under 1 MiB.)
+ *   - Every argument is checked before any CUDA call. Each call then looks
+ *     up the array's device address on the current device; the first call
+ *     on a device may load the library's device code there (which creates
+ *     the array), so make that first call before any stream capture.
  *   - All calls on a device share the one array: calls whose GPU work
  *     overlaps (other streams, other threads) race and must be serialised by
  *     the caller. Each call clears the part of the array it needs cleared.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call,
- *     and no host heap allocation. */
+ *     and the library's own code makes no host heap allocation on this path
+ *     (the CUDA runtime and driver may allocate internally on first use).
+ *   - A device-side timeout (FA_ERR_DEVICE_TIMEOUT) is recorded in the
+ *     array's status word: read it with fa_decode_noalloc_status. */
 #define FA_NOALLOC_SCRATCH_BYTES (8u << 20)
 
 fa_status fa_decode_noalloc(const void* q, const void* k, const void* v, const uint8_t* key_mask,
                             const int64_t* actual_seq_lengths, int64_t B, int64_t S_kv_max,
                             int64_t num_heads, int64_t num_kv_heads, int64_t D, float scale,
                             int layout, int num_splits, void* out, float* lse, void* stream);
+
+/* Status of the fa_decode_noalloc calls on the current device, as
+ * fa_workspace_status gives it for a workspace: synchronises `stream`, then
+ * reads and clears the status word of the library-owned array. Returns FA_OK,
+ * FA_ERR_DEVICE_TIMEOUT (a bounded wait in a kernel expired) or
+ * FA_ERR_RUNTIME. No counterpart on the pages (see fa_decode_noalloc). */
+fa_status fa_decode_noalloc_status(void* stream);
 
 /* ------------------------------------------------------------ diagnostics
  * Synchronises `stream`, then reads and clears the device status word at

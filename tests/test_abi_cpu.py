@@ -452,3 +452,30 @@ def test_python_binding_has_every_declared_function():
     assert all(hasattr(pkg, n) for n in names), sorted(n for n in names if not hasattr(pkg, n))
     assert F.fa_forward_varlen_workspace_size(3, 100, 200, 8, 2, 128) == int(
         _lib.load().fa_forward_varlen_workspace_size(3, 100, 200, 8, 2, 128))
+
+
+def _fwd_varlen_ex(lib, cq, ckv, uq, ukv, wl=-1, wr=0, ws_bytes=1 << 22, km=None):
+    B = len(cq) - 1
+    aq = (ctypes.c_int64 * len(cq))(*cq)
+    akv = (ctypes.c_int64 * len(ckv))(*ckv)
+    auq = (ctypes.c_int64 * B)(*uq) if uq is not None else None
+    aukv = (ctypes.c_int64 * B)(*ukv) if ukv is not None else None
+    return lib.fa_forward_varlen_ex(P, P, P, aq, akv, auq, aukv, km, wl, wr, B, 4, 2, 128, 0.1, P,
+                                    None, WS, ws_bytes, None)
+
+
+@pytest.mark.parametrize("cq,ckv,uq,ukv,wl,wr,expect", [
+    ([0, 10, 30], [0, 10, 30], [5, -1], None, -1, 0, _lib.FA_ERR_PARAM_INVALID),
+    ([0, 10, 30], [0, 10, 30], None, [-3, 20], -1, 0, _lib.FA_ERR_PARAM_INVALID),
+    ([0, 10, 30], [0, 12, 30], [5, 5], [5, 5], -1, 0, _lib.FA_ERR_PARAM_INVALID),  # causal spans
+    ([0, 10, 30], [0, 10, 30], [5, 5], [5, 5], -2, 0, _lib.FA_ERR_PARAM_INVALID),
+    ([1, 10], [0, 10], None, None, -1, -1, _lib.FA_ERR_PARAM_INVALID),
+])
+def test_forward_varlen_ex_rejects_before_any_cuda_call(lib, cq, ckv, uq, ukv, wl, wr, expect):
+    assert _fwd_varlen_ex(lib, cq, ckv, uq, ukv, wl, wr) == expect
+
+
+def test_forward_varlen_ex_workspace_and_empty_batch(lib):
+    assert _fwd_varlen_ex(lib, [0, 10], [0, 10], [3], [3], ws_bytes=16) == \
+        _lib.FA_ERR_WORKSPACE_TOO_SMALL
+    assert _fwd_varlen_ex(lib, [0], [0], [], []) == _lib.FA_OK  # B = 0: nothing to do

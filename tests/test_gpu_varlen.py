@@ -133,3 +133,66 @@ def test_varlen_workload_sampled_rows(cuda_device):
         err = np.abs(got_o - ro[0])
         assert err.max() <= OUT_MAX and err.mean() <= OUT_MEAN
         assert np.abs(got_l - rl[0].T).max() <= LSE_MAX
+
+
+def _garbage_past_used(q, k, v, cq, ckv, uq, ukv, seed):
+    """Random bf16 bit patterns (NaN and Inf included) in the truncated query
+    rows and in the keys / values past each used kv length."""
+    import workloads
+    g = torch.Generator().manual_seed(seed)
+    q, k, v = q.clone(), k.clone(), v.clone()
+    for b in range(len(uq)):
+        for t, c, u in ((q, cq, uq), (k, ckv, ukv), (v, ckv, ukv)):
+            lo, hi = int(c[b]) + min(int(u[b]), int(c[b + 1] - c[b])), int(c[b + 1])
+            if hi > lo:
+                t[lo:hi] = workloads.random_bf16_bits(t[lo:hi].numel(), g).view(t[lo:hi].shape)
+    return q, k, v
+
+
+EX_CASES = [
+    # lq, lkv, seqused_q, seqused_kv, masked, window, Hq, Hkv, D
+    ([300, 500, 129], [300, 500, 129], [200, 500, 0], [300, 131, 129], False, (-1, 0), 4, 2, 128),
+    ([640, 257], [640, 257], [640, 257], [500, 100], True, (-1, 0), 8, 2, 128),
+    ([100, 700, 33], [250, 40, 900], [90, 800, 33], [250, 39, 777], True, (-1, -1), 4, 1, 128),
+    ([513, 1000], [513, 1000], [400, 999], [513, 1000], True, (100, 17), 4, 4, 64),
+    ([300, 520], [300, 520], [290, 520], [255, 400], True, (-1, 0), 2, 2, 256),
+    ([0, 128, 1], [0, 128, 1], [5, 128, 1], [0, 0, 1], False, (-1, 0), 2, 1, 128),
+]
+
+
+@pytest.mark.parametrize("lq,lkv,uq,ukv,masked,window,Hq,Hkv,D", EX_CASES)
+def test_varlen_seqused_and_key_mask_match_oracle(cuda_device, lq, lkv, uq, ukv, masked, window,
+                                                   Hq, Hkv, D):
+    """seqused_q / seqused_kv (the shorter of them and the span holds),
+    truncated query rows (out 0, lse +inf), garbage past the used lengths and
+    a per-packed-key mask, with causal, a window or no mask (FlashAttn guide
+    §1.3-§1.5, §1.7)."""
+    q, k, v, cq, ckv = _packed(lq, lkv, Hq, Hkv, D, seed=sum(lq) + 3 * D)
+    q, k, v = _garbage_past_used(q, k, v, cq, ckv, uq, ukv, seed=sum(lkv))
+    km = None
+    if masked:
+        g = torch.Generator().manual_seed(sum(uq) + 1)
+        km = (torch.rand(int(ckv[-1]), generator=g) < 0.2).to(torch.uint8)
+    scale = 1.0 / math.sqrt(D)
+    out = torch.full_like(q.cuda(), float("nan"))
+    lse = torch.full((int(cq[-1]), Hq), float("nan"), dtype=torch.float32, device="cuda")
+    F.fa_forward_varlen_ex(q.cuda(), k.cuda(), v.cuda(), cq.tolist(), ckv.tolist(), seqused_q=uq,
+                           seqused_kv=ukv, key_mask=km.cuda() if km is not None else None,
+                           win_left=window[0], win_right=window[1], scale=scale, out=out, lse=lse)
+    torch.cuda.synchronize()
+    ro, rl = oracle.attention_varlen(q, k, v, cq, ckv, scale=scale, window=window, seqused_q=uq,
+                                     seqused_kv=ukv, key_mask=km)
+    _compare(out, lse, ro, rl)
+
+
+def test_varlen_ex_without_options_equals_varlen(cuda_device):
+    """No seqused and no mask: bit-identical to fa_forward_varlen (same kernel,
+    same schedule)."""
+    q, k, v, cq, ckv = _packed([300, 257, 700], [300, 257, 700], 4, 2, 128, seed=5)
+    q, k, v = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = F.fa_forward_varlen(q, k, v, cq.tolist(), ckv.tolist(), mask_mode="causal",
+                                 scale=0.088)
+    o2, l2 = F.fa_forward_varlen_ex(q, k, v, cq.tolist(), ckv.tolist(), win_left=-1, win_right=0,
+                                    scale=0.088)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
