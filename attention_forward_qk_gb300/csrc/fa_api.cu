@@ -25,6 +25,11 @@ namespace {
 constexpr size_t kAlign = 256;
 constexpr int kChunkQuant = 64;  // forced-split chunk sizes are multiples of this
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+// K/V bytes of one prefill schedule section (see build_prefill_schedule): a
+// quarter of the 126 MB L2, so that the K/V of two sections (the one ending
+// and the one starting on other CTAs) and the Q tiles and outputs streaming
+// through fit together
+constexpr int64_t kPrefillL2Budget = int64_t(32) << 20;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -95,21 +100,25 @@ PrefillWs prefill_ws(int64_t B, int64_t S_q, int64_t S_kv, int64_t num_heads, in
 }
 
 
-// Static schedule of the persistent prefill CTAs. Items are numbered as the
+// Static schedule of the persistent prefill CTAs, in L2-sized sections (the
+// FlashAttn guide §4, SectionStreamK: batch x head units are gathered into a
+// section until their K/V reach an L2 budget, so that a section's K/V is not
+// pushed out of L2 while its items run; each section is spread over all
+// cores, and the sections follow one another). Items are numbered as the
 // kernel decodes them: (batch, KV head) units one after another, inside a
-// unit its query pairs heaviest (last) first, query heads innermost. Units
-// are taken in groups of 8; inside a group the items go, longest first, to
-// the CTA with the least work so far (a greedy longest-processing-time
-// schedule), and the groups follow one another, so the items in flight at any
-// time read the K/V of a few units out of L2. The cost of an item is its KV
-// tiles under the causal or window limits plus a constant for its start-up.
+// unit its query pairs heaviest (last) first, query heads innermost. A
+// section is a run of consecutive units whose K/V bytes together stay within
+// l2_budget (at least one unit); inside a section the items go, longest
+// first, to the CTA with the least work so far (a greedy longest-processing-
+// time schedule). The cost of an item is its KV tiles under the causal or
+// window limits plus a constant for its start-up.
 // Layout: offsets[grid + 1] into the lists, then the item lists (int32).
 // lq, lkv: per-sequence lengths of packed sequences (else null); items past a
 // sequence's query rows do not exist and are not scheduled. IR: query rows
 // per item, BN: keys per KV tile (prefill_item_rows, prefill_kv_tile).
 void build_prefill_schedule(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int64_t S_kv,
-                            int64_t win_left, int64_t win_right, int grid, int64_t IR,
-                            int64_t BN, std::vector<int32_t>& sched,
+                            int64_t D, int64_t win_left, int64_t win_right, int grid, int64_t IR,
+                            int64_t BN, int64_t l2_budget, std::vector<int32_t>& sched,
                             const int32_t* lq = nullptr, const int32_t* lkv = nullptr) {
   const int64_t g = Hq / Hkv;
   const int64_t nq = ceil_div(S_q, IR);
@@ -145,10 +154,19 @@ void build_prefill_schedule(int64_t B, int64_t Hq, int64_t Hkv, int64_t S_q, int
   auto cmp = [](const std::pair<int64_t, int>& x, const std::pair<int64_t, int>& y) {
     return x > y;
   };
+  // K and V bytes of a (batch, KV head) unit
+  auto unit_bytes = [&](int64_t u) -> int64_t {
+    const int64_t L = lkv ? static_cast<int64_t>(lkv[u / Hkv]) : S_kv;
+    return 2 * 2 * D * L;
+  };
   std::vector<std::pair<int64_t, int64_t>> grp;
-  for (int64_t u0 = 0; u0 < units; u0 += 8) {
+  for (int64_t u0 = 0, u1 = 0; u0 < units; u0 = u1) {
+    // the section: units u0 .. u1-1, as many as the budget holds (at least one)
+    int64_t bytes = unit_bytes(u0);
+    for (u1 = u0 + 1; u1 < units && bytes + unit_bytes(u1) <= l2_budget; ++u1)
+      bytes += unit_bytes(u1);
     const int64_t w0 = u0 * per_unit;
-    const int64_t w1 = std::min(units, u0 + 8) * per_unit;
+    const int64_t w1 = u1 * per_unit;
     grp.clear();
     for (int64_t w = w0; w < w1; ++w) {
       const int64_t c = cost(w);
@@ -465,12 +483,12 @@ fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok
       vtab[4 * B + b] = static_cast<int32_t>(span_q);
     }
     // depends on the lengths: built for every call
-    build_prefill_schedule(B, num_heads, Hkv, S_q, S_kv, win_left, win_right, grid, IR, BN,
-                           sched, vtab.data() + B, vtab.data() + 3 * B);
+    build_prefill_schedule(B, num_heads, Hkv, S_q, S_kv, D, win_left, win_right, grid, IR, BN,
+                           kPrefillL2Budget, sched, vtab.data() + B, vtab.data() + 3 * B);
     sched_key = SchedKey{-1, 0, 0, 0, 0, 0, 0, 0, 0};
   } else if (!(key == sched_key)) {
-    build_prefill_schedule(B, num_heads, Hkv, S_q, S_kv, win_left, win_right, grid, IR, BN,
-                           sched);
+    build_prefill_schedule(B, num_heads, Hkv, S_q, S_kv, D, win_left, win_right, grid, IR, BN,
+                           kPrefillL2Budget, sched);
     sched_key = key;
   }
   // header: zeroed status word, the schedule, the packed-sequence table, then
