@@ -22,6 +22,7 @@ from .fa import (  # noqa: F401
     fa_kernel_launch_count,
     fa_selftest_wait_timeout,
     fa_set_main_kernel_events,
+    fa_set_wait_timeout_ns,
     fa_status_string,
     fa_workspace_status,
 )

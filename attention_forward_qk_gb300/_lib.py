@@ -67,6 +67,7 @@ SIGNATURES = {
                                          ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp, _vp,
                                          _vp]),
     "fa_decode_noalloc_status": (ctypes.c_int, [_vp]),
+    "fa_set_wait_timeout_ns": (ctypes.c_int, [ctypes.c_uint64]),
     "fa_set_main_kernel_events": (None, [_vp, _vp]),
     "fa_kernel_launch_count": (ctypes.c_uint64, []),
 }

@@ -46,16 +46,17 @@ struct DecodeWs {
   size_t prefix, real_lens, counters, part_lse, part_o, total;
 };
 
-// [status | pad][length prefix sums, large batches only][partial lse][partial o]
+// [status word, piece counters | pad][length prefix sums, large batches
+// only][real lengths, paged][partial lse][partial o]: the counters follow the
+// status word so that one clear before the launch covers both
 DecodeWs decode_ws(int64_t B, int64_t Hq, int64_t D, int64_t max_slots) {
   DecodeWs w;
-  size_t off = kAlign;  // status word
+  w.counters = sizeof(uint32_t);  // per (batch, KV head, head group): pieces finished
+  size_t off = align_up(sizeof(uint32_t) * (1 + B * Hq));
   w.prefix = off;
   off += align_up(sizeof(int64_t) * (B + 1));
   w.real_lens = off;  // paged cache only
   off += align_up(sizeof(int32_t) * B);
-  w.counters = off;  // per (batch, KV head, head group): pieces finished
-  off += align_up(sizeof(uint32_t) * B * Hq);
   w.part_lse = off;
   off += align_up(sizeof(float) * B * Hq * max_slots);
   w.part_o = off;
@@ -247,8 +248,11 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int layout, int64_t B, 
 namespace {
 thread_local cudaEvent_t tl_before = nullptr;
 thread_local cudaEvent_t tl_after = nullptr;
+thread_local uint64_t tl_timeout_ns = 0;  // 0: kDefaultTimeoutNs
 std::atomic<uint64_t> g_launches{0};
 }  // namespace
+
+uint64_t wait_timeout_ns() { return tl_timeout_ns != 0 ? tl_timeout_ns : kDefaultTimeoutNs; }
 
 void main_kernel_begin(cudaStream_t stream) {
   if (tl_before != nullptr && tl_after != nullptr) cudaEventRecord(tl_before, stream);
@@ -551,7 +555,7 @@ fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok
   x.out = out;
   x.lse = lse;
   x.status = reinterpret_cast<uint32_t*>(wsb);
-  x.timeout_ns = kDefaultTimeoutNs;
+  x.timeout_ns = wait_timeout_ns();
   main_kernel_begin(s);
   const cudaError_t e = launch_prefill(x, s);
   main_kernel_end(s);
@@ -752,13 +756,12 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
                         s) != cudaSuccess)
       return FA_ERR_RUNTIME;
   }
-  // the main kernel clears the status word when it starts; without one, clear it here
-  if (total == 0 && cudaMemsetAsync(wsb, 0, sizeof(uint32_t), s) != cudaSuccess)
-    return FA_ERR_RUNTIME;
-  // the piece counters of the units cut into several pieces start at zero
-  if (total > 0 && max_slots > 1 &&
-      cudaMemsetAsync(wsb + ws.counters, 0, sizeof(uint32_t) * B * KH, s) != cudaSuccess)
-    return FA_ERR_RUNTIME;
+  // the status word, and the piece counters of the units cut into several
+  // pieces, start at zero: one clear on the stream before the launch (a
+  // kernel-side clear could erase a timeout another CTA recorded first)
+  const size_t clear_bytes =
+      sizeof(uint32_t) * (1 + ((total > 0 && max_slots > 1) ? B * KH : 0));
+  if (cudaMemsetAsync(wsb, 0, clear_bytes, s) != cudaSuccess) return FA_ERR_RUNTIME;
 
   DecodeLaunch x;
   x.q = q;
@@ -798,7 +801,7 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
   x.out = out;
   x.lse = lse;
   x.status = reinterpret_cast<uint32_t*>(wsb);
-  x.timeout_ns = kDefaultTimeoutNs;
+  x.timeout_ns = wait_timeout_ns();
   return launch_decode(x, s) == cudaSuccess ? FA_OK : FA_ERR_RUNTIME;
 }
 
@@ -856,6 +859,12 @@ fa_status fa_selftest_wait_timeout(void* workspace, uint64_t timeout_ns, void* s
   if (launch_wait_probe(static_cast<uint32_t*>(workspace), timeout_ns, s) != cudaSuccess)
     return FA_ERR_RUNTIME;
   count_launches(1);
+  return FA_OK;
+}
+
+fa_status fa_set_wait_timeout_ns(uint64_t timeout_ns) {
+  if (timeout_ns > 10000000000ull) return FA_ERR_PARAM_INVALID;
+  tl_timeout_ns = timeout_ns;
   return FA_OK;
 }
 

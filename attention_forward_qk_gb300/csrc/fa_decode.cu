@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         for (int s = 0; s < h.nstage; ++s, ++st) {
           const int slot = st % NST;
           const int use = st / NST;
-          if (use > 0 && !mbar_wait(empty0 + 8 * slot, (use - 1) & 1, a.timeout_ns, a.status,
+          if (use > 0 && !mbar_wait_polled(empty0 + 8 * slot, (use - 1) & 1, a.timeout_ns, a.status,
                                     kDevTimeoutDecodeEmpty, abort_flag)) {
             ok = false;
             break;
@@ -445,15 +445,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
       if (*abort_flag) {
         // let every copy this CTA started land before shared memory is released
+        const uint64_t drain_ns = a.timeout_ns > kDrainFloorNs ? a.timeout_ns : kDrainFloorNs;
         for (int s = max(0, st - NST); s < st; ++s)
-          mbar_wait(full0 + 8 * (s % NST), (s / NST) & 1, a.timeout_ns, a.status,
+          mbar_wait_polled(full0 + 8 * (s % NST), (s / NST) & 1, drain_ns, a.status,
                     kDevTimeoutDrain, nullptr);
       }
     }
   } else {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    // a timeout needs timeout_ns to fire, long after this clear
-    if (tid == 0 && blockIdx.x == 0) *a.status = 0;
+    // (the status word was cleared on the stream before this kernel)
     // work queued after this kernel may be scheduled as soon as SMs free up
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (a.has_empty) {
@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
     for (int st = 0;; ++st) {
       const int slot = st % NST;
-      bool got = mbar_wait(full0 + 8 * slot, (st / NST) & 1, a.timeout_ns, a.status,
+      bool got = mbar_wait_polled(full0 + 8 * slot, (st / NST) & 1, a.timeout_ns, a.status,
                            kDevTimeoutDecodeFull, abort_flag);
       got = __all_sync(0xffffffffu, got);
       if (!got) break;
@@ -678,7 +678,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const int use = piece_seq / C::NSB;
       const uint32_t use_parity = use & 1;
       if (use >= 1) {
-        bool fr = mbar_wait(sfree0 + 8 * buf, use_parity ^ 1, a.timeout_ns, a.status,
+        bool fr = mbar_wait_polled(sfree0 + 8 * buf, use_parity ^ 1, a.timeout_ns, a.status,
                             kDevTimeoutDecodeFull, abort_flag);
         fr = __all_sync(0xffffffffu, fr);
         if (!fr) break;
@@ -715,7 +715,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       if (lane == 0) mbar_arrive(parked0 + 8 * buf);
       // 3) every consumer warp combines a slice of the G x D results once all
       //    of them have parked
-      bool pk = mbar_wait(parked0 + 8 * buf, use_parity, a.timeout_ns, a.status,
+      bool pk = mbar_wait_polled(parked0 + 8 * buf, use_parity, a.timeout_ns, a.status,
                           kDevTimeoutDecodeFull, abort_flag);
       pk = __all_sync(0xffffffffu, pk);
       if (!pk) break;

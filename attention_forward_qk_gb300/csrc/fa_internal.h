@@ -171,5 +171,13 @@ void count_launches(int n);
 
 // Default bounded-wait limit of the kernels (nanoseconds).
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+// Lower bound of the limit of a drain wait (a kernel that gave up waits for
+// its own copies and MMAs in flight before it releases shared memory and
+// TMEM): those always complete, so the drain keeps a long limit even when the
+// bounded-wait limit is set short.
+constexpr uint64_t kDrainFloorNs = 100000000ull;
+// The bounded-wait limit of the calls made from this thread
+// (fa_set_wait_timeout_ns; kDefaultTimeoutNs unless set).
+uint64_t wait_timeout_ns();
 
 }  // namespace fa

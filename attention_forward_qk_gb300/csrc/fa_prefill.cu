@@ -277,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int item = 0;  // ring items issued so far (K_j and V_j are one item each)
     int fixes = 0;
+    int q_loads = 0;  // work items whose Q tiles were requested
     bool ok = true;
     for (int r = 0; ok; ++r) {
       const int w = item_of(r);
@@ -291,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
       }
+      ++q_loads;
       if (lane == 0) {
         const int nq = wi.has_t1 ? 2 : 1;
         mbar_expect_tx(bar(kBarQ), nq * C::kQTileBytes);
@@ -364,14 +366,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
       }
     }
+    const uint64_t drain_ns = a.timeout_ns > kDrainFloorNs ? a.timeout_ns : kDrainFloorNs;
     if (!ok && lane == 0) {
       // let the copies this CTA started land before its shared memory is released
       for (int it = max(0, item - kRing); it < item; ++it)
-        mbar_wait(bar(kBarKvFull + it % kRing), (it / kRing) & 1, a.timeout_ns, a.status,
+        mbar_wait(bar(kBarKvFull + it % kRing), (it / kRing) & 1, drain_ns, a.status,
                   kDevTimeoutDrain, nullptr);
-      if (fixes > 0) mbar_wait(bar(kBarFix), (fixes - 1) & 1, a.timeout_ns, a.status,
+      if (fixes > 0) mbar_wait(bar(kBarFix), (fixes - 1) & 1, drain_ns, a.status,
                                kDevTimeoutDrain, nullptr);
     }
+    // the last Q tiles requested have landed (at once unless an MMA warp gave
+    // up before it waited for them)
+    if (q_loads > 0 && lane == 0)
+      mbar_wait(bar(kBarQ), (q_loads - 1) & 1, drain_ns, a.status, kDevTimeoutDrain, nullptr);
     __syncwarp();
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ================================================================ MMA
@@ -867,7 +874,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // in-flight MMAs of this stream retire in order: one commit covers them
       const int t = warp - kMmaWarp;
       umma_commit(bar(kBarDrain + t));
-      mbar_wait(bar(kBarDrain + t), 0, a.timeout_ns, a.status, kDevTimeoutDrain, nullptr);
+      const uint64_t drain_ns = a.timeout_ns > kDrainFloorNs ? a.timeout_ns : kDrainFloorNs;
+      mbar_wait(bar(kBarDrain + t), 0, drain_ns, a.status, kDevTimeoutDrain, nullptr);
     }
     __syncwarp();
     asm volatile("bar.sync 1, 64;" ::: "memory");  // both streams drained

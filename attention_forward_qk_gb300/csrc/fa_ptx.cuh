@@ -61,18 +61,69 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking test of phase `parity` (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// try_wait that suspends the thread for at most `hint_ns` (or until the
+// phase completes): without the hint a thread may sleep for a system-defined
+// time, so that a wait limit shorter than that would never be checked.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 // Wait for phase `parity` of `bar` to complete. Gives up after limit_ns
 // (recording `code`) or as soon as *abort becomes nonzero (another role of
-// the same CTA gave up). Returns true when the phase completed.
+// the same CTA gave up). Returns true when the phase completed. After a first
+// try, the thread sleeps at most min(limit_ns, 1 ms) between two checks of
+// the clock (the hardware may wake it later than that: a limit far below the
+// waits' own durations is not guaranteed to expire; mbar_wait_polled is).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                           uint32_t* status, uint32_t code,
                                           volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint32_t hint = static_cast<uint32_t>(limit_ns < 1000000ull ? limit_ns : 1000000ull);
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 16; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_hint(bar, parity, hint)) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      record_error(status, code);
+      if (abort_flag != nullptr) *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// mbar_wait whose limit always expires on time: a limit under a microsecond
+// (a test of the failure path) polls the barrier without sleeping.
+__device__ __forceinline__ bool mbar_wait_polled(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                 uint32_t* status, uint32_t code,
+                                                 volatile int* abort_flag) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  const bool poll = limit_ns < 1000ull;
+  const uint32_t hint = static_cast<uint32_t>(limit_ns < 1000000ull ? limit_ns : 1000000ull);
+  while (true) {
+    if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait_hint(bar, parity, hint)) return true;
     if (abort_flag != nullptr && *abort_flag) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       record_error(status, code);

@@ -384,6 +384,12 @@ def fa_selftest_wait_timeout(workspace, timeout_ns: int, stream=None) -> int:
                                                     _stream_ptr(stream)))
 
 
+def fa_set_wait_timeout_ns(timeout_ns: int) -> None:
+    """Bounded-wait limit of the kernels of later calls from this thread (0 =
+    the default, 2 s). A diagnostic for failure-detection tests."""
+    check(int(_lib.load().fa_set_wait_timeout_ns(int(timeout_ns))), "fa_set_wait_timeout_ns")
+
+
 def fa_set_main_kernel_events(before, after) -> None:
     """Record torch.cuda.Event `before`/`after` around the main kernel of every
     later call from this thread (None, None turns it off). Each event must

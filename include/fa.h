@@ -224,10 +224,10 @@ size_t fa_decode_workspace_size(int64_t B, int64_t S_kv_max, int64_t num_heads,
  *   workspace           device, >= fa_decode_workspace_size(..., num_splits)
  *                       bytes, 256-byte aligned
  * The lengths are read on the host during the call. On `stream` the call
- * clears the per-sequence piece counters in the workspace, copies the
- * lengths' prefix sums there when B > 1024 (else they travel in the launch
- * parameters), and launches one kernel: the CTA that finishes the last piece
- * of a sequence cut into several merges them. */
+ * clears the status word and the per-sequence piece counters at the start of
+ * the workspace, copies the lengths' prefix sums there when B > 1024 (else
+ * they travel in the launch parameters), and launches one kernel: the CTA
+ * that finishes the last piece of a sequence cut into several merges them. */
 fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* key_mask,
                     const int64_t* actual_seq_lengths, int64_t B, int64_t S_kv_max,
                     int64_t num_heads, int64_t num_kv_heads, int64_t D, float scale, int layout,
@@ -335,6 +335,18 @@ fa_status fa_decode_noalloc_status(void* stream);
  * FA_ERR_DEVICE_TIMEOUT (a bounded wait in a kernel expired) or
  * FA_ERR_RUNTIME. */
 fa_status fa_workspace_status(void* workspace, void* stream);
+
+/* The bounded-wait limit (nanoseconds) of every later fa_forward* / fa_decode*
+ * call made from this host thread; 0 restores the default of 2 s. Every wait
+ * of the kernels on a barrier, a turn or a peer gives up after this limit:
+ * the kernel records FA_ERR_DEVICE_TIMEOUT in the workspace status word (see
+ * fa_workspace_status and fa_decode_noalloc_status), lets its own copies and
+ * tensor-core operations in flight finish (those waits keep a limit of at
+ * least 100 ms), frees what it holds and returns; its outputs are then
+ * undefined. A diagnostic for failure-detection tests: a limit of a few
+ * microseconds makes the first waits of a real call run out. Limits above
+ * 10 s are FA_ERR_PARAM_INVALID. No counterpart on the pages. */
+fa_status fa_set_wait_timeout_ns(uint64_t timeout_ns);
 
 /* Self-test of the bounded-wait path: launches one CTA that waits on an
  * mbarrier nothing ever arrives on, with a limit of timeout_ns. The kernel

@@ -116,3 +116,27 @@ def test_noalloc_rejects_a_plan_that_does_not_fit(cuda_device):
                                _lib.FA_LAYOUT_BNSD, splits, p, None, None)
     assert st == _lib.FA_ERR_WORKSPACE_TOO_SMALL
     assert lib.fa_kernel_launch_count() == n0
+
+
+def test_noalloc_status_reports_a_device_timeout(cuda_device):
+    """A device-side timeout of a noalloc call lands in the library-owned
+    array's status word, which fa_decode_noalloc_status reads and clears; the
+    next call with the default limit matches the oracle again."""
+    B, Hq, Hkv, S, D = 2, 8, 2, 3000, 128
+    x = workloads.make_decode(B, Hq, Hkv, S, D, "BNSD", seed=79, len_lo=800, len_hi=S)
+    q, k, v = x["q"].cuda(), x["k"].cuda(), x["v"].cuda()
+    lib = _lib.load()
+    scale = 1.0 / math.sqrt(D)
+    assert lib.fa_set_wait_timeout_ns(100) == _lib.FA_OK
+    try:
+        _noalloc(lib, q, k, v, None, x["lengths"], B, S, Hq, Hkv, D, scale, 0,
+                 _lib.FA_LAYOUT_BNSD)
+        assert lib.fa_decode_noalloc_status(None) == _lib.FA_ERR_DEVICE_TIMEOUT
+        assert lib.fa_decode_noalloc_status(None) == _lib.FA_OK  # read clears it
+    finally:
+        lib.fa_set_wait_timeout_ns(0)
+    out, lse = _noalloc(lib, q, k, v, None, x["lengths"], B, S, Hq, Hkv, D, scale, 0,
+                        _lib.FA_LAYOUT_BNSD)
+    assert lib.fa_decode_noalloc_status(None) == _lib.FA_OK
+    ro, rl = oracle.decode(x["q"], x["k"], x["v"], x["lengths"], scale=scale)
+    _check(out, lse, ro, rl)
