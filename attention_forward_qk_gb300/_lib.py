@@ -10,6 +10,8 @@ import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
+# the same library with device-side index checks (-DFA_DEBUG)
+DEBUG_LIB_PATH = os.path.join(_HERE, "libfa_gb300_debug.so")
 
 FA_OK = 0
 FA_ERR_NULLPTR = 1
@@ -18,6 +20,7 @@ FA_ERR_UNSUPPORTED = 3
 FA_ERR_WORKSPACE_TOO_SMALL = 4
 FA_ERR_RUNTIME = 5
 FA_ERR_DEVICE_TIMEOUT = 6
+FA_ERR_DEVICE_CHECK = 7
 
 FA_LAYOUT_BNSD = 0
 FA_LAYOUT_BSND = 1
@@ -74,6 +77,30 @@ SIGNATURES = {
 
 _lock = threading.Lock()
 _lib = None
+_debug_lib = None
+
+
+def _open(path: str) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+def load_debug() -> ctypes.CDLL:
+    """The debug build (device-side index checks reported as
+    FA_ERR_DEVICE_CHECK); same functions as load()'s. Raises if missing."""
+    global _debug_lib
+    with _lock:
+        if _debug_lib is None:
+            _debug_lib = _open(DEBUG_LIB_PATH)
+        return _debug_lib
 
 
 def load() -> ctypes.CDLL:
@@ -81,16 +108,7 @@ def load() -> ctypes.CDLL:
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIB_PATH):
-                raise RuntimeError(
-                    f"{LIB_PATH} is missing: build the CUDA library first "
-                    "(python -c 'import __graft_entry__ as g; g.build()')")
-            lib = ctypes.CDLL(LIB_PATH)
-            for name, (res, args) in SIGNATURES.items():
-                fn = getattr(lib, name)
-                fn.restype = res
-                fn.argtypes = args
-            _lib = lib
+            _lib = _open(LIB_PATH)
         return _lib
 
 

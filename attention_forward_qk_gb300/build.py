@@ -3,7 +3,10 @@
 Each ``csrc/*.cu`` translation unit is compiled by its own nvcc process (in
 parallel), then linked into one shared library next to this file. The CUDA
 runtime is linked statically, so the library needs only the NVIDIA driver at
-run time.
+run time. The same sources are also built with ``-DFA_DEBUG`` into
+``libfa_gb300_debug.so``: device-side index checks that report
+FA_ERR_DEVICE_CHECK through the workspace status word (both libraries are
+compiled at once, in parallel).
 """
 from __future__ import annotations
 
@@ -19,6 +22,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
+DEBUG_BUILD_DIR = os.path.join(PKG_DIR, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(PKG_DIR, "libfa_gb300_debug.so")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH_FLAGS + [
@@ -45,41 +50,51 @@ def _deps():
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
-        return False
-    t = os.path.getmtime(LIB_PATH)
-    return all(os.path.getmtime(f) <= t for f in _deps())
+    for lib in (LIB_PATH, DEBUG_LIB_PATH):
+        if not os.path.exists(lib):
+            return False
+        t = os.path.getmtime(lib)
+        if any(os.path.getmtime(f) > t for f in _deps()):
+            return False
+    return True
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    """Build the library if any source is newer than it; return its path."""
+    """Build both libraries if any source is newer than them; return the
+    release library's path."""
     if not force and up_to_date():
         return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    variants = ((BUILD_DIR, LIB_PATH, []), (DEBUG_BUILD_DIR, DEBUG_LIB_PATH, ["-DFA_DEBUG"]))
+    for d, _, _ in variants:
+        os.makedirs(d, exist_ok=True)
 
-    def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [cc, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
+    def compile_one(job):
+        src, (d, _, flags) = job
+        obj = os.path.join(d, os.path.basename(src)[:-3] + ".o")
+        cmd = [cc, *NVCC_FLAGS, *flags, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed for {src}:\n{r.stderr}")
+            raise RuntimeError(f"nvcc failed for {src} {' '.join(flags)}:\n{r.stderr}")
         return obj, r.stderr
 
     srcs = _sources()
-    with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        results = list(ex.map(compile_one, srcs))
+    jobs = [(src, v) for v in variants for src in srcs]
+    with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        results = list(ex.map(compile_one, jobs))
     if verbose or ptxas_verbose:
-        for _, err in results:
+        for _, err in results[:len(srcs)]:
             if err:
                 print(err)
-    tmp = LIB_PATH + ".tmp"
-    cmd = [cc, *ARCH_FLAGS, "-shared", "-o", tmp, *[o for o, _ in results]]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
+    for i, (_, lib, _) in enumerate(variants):
+        objs = [o for o, _ in results[i * len(srcs):(i + 1) * len(srcs)]]
+        tmp = lib + ".tmp"
+        cmd = [cc, *ARCH_FLAGS, "-shared", "-o", tmp, *objs]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stderr}")
+        os.replace(tmp, lib)
     return LIB_PATH
 
 

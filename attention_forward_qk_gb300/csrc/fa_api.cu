@@ -296,6 +296,7 @@ const char* fa_status_string(int s) {
     case FA_ERR_WORKSPACE_TOO_SMALL: return "FA_ERR_WORKSPACE_TOO_SMALL";
     case FA_ERR_RUNTIME: return "FA_ERR_RUNTIME: a CUDA call failed";
     case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT: a kernel wait expired";
+    case FA_ERR_DEVICE_CHECK: return "FA_ERR_DEVICE_CHECK: a device-side index check failed (debug build)";
     default: return "unknown fa_status";
   }
 }
@@ -871,7 +872,8 @@ fa_status fa_workspace_status(void* workspace, void* stream) {
     return FA_ERR_RUNTIME;
   if (word != 0) {
     if (cudaMemset(workspace, 0, sizeof(word)) != cudaSuccess) return FA_ERR_RUNTIME;
-    // every code but the (impossible) pending-list overflow is an expired wait
+    if (word >= kDevCheckFirst && word <= kDevCheckLast) return FA_ERR_DEVICE_CHECK;
+    // every other code but the (impossible) pending-list overflow is an expired wait
     return word == kDevPendingOverflow ? FA_ERR_RUNTIME : FA_ERR_DEVICE_TIMEOUT;
   }
   return FA_OK;

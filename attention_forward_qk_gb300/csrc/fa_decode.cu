@@ -172,6 +172,9 @@ struct SlotHeader {
 template <int D>
 __device__ __forceinline__ void merge_row(const DecodeArgs& a, size_t row, int nsp, int lane) {
   constexpr int EPL = D / 32;  // output elements per lane
+  if (!FA_CHECK(nsp <= a.max_slots && row < static_cast<size_t>(a.B) * a.Hq, a.status,
+                kDevCheckDecodeMerge))
+    return;
   const float* pl = a.part_lse + row * a.max_slots;
   const float* po = a.part_o + row * a.max_slots * D + lane * EPL;
   float M = -INFINITY, W = 0.f, acc[EPL];
@@ -362,6 +365,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       kvh = h.kh / a.head_groups;
       hg = h.kh % a.head_groups;
       r += rows;
+      if (!FA_CHECK(b >= 0 && b < a.B && kh >= 0 && kh < KH && h.row0 >= 0 && rows > 0 &&
+                        h.row0 + rows <= L && h.slot >= 0 && h.slot < h.nsp,
+                    a.status, kDevCheckDecodePiece))
+        h.piece = -1;  // stop: nothing of this piece is loaded
     };
     SlotHeader h{};
     int kvh = 0, hg = 0;
@@ -743,6 +750,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           }
           const float inv = empty ? 0.f : 1.f / Ls;
           acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+          if (!FA_CHECK(bh0 + h < static_cast<size_t>(a.B) * a.Hq, a.status, kDevCheckDecodeRow) ||
+              !FA_CHECK(hd.nsp == 1 || hd.slot < a.max_slots, a.status, kDevCheckDecodeSlot))
+            continue;
           if (hd.nsp == 1) {
             __nv_bfloat16* dst = a.out + (bh0 + h) * D + d;
             *reinterpret_cast<uint2*>(dst) =

@@ -76,6 +76,16 @@ enum DeviceError : uint32_t {
   kDevTimeoutDecodeEmpty = 0x202,
   kDevPendingOverflow = 0x203,  // decode: more split pieces than a CTA can record
   kDevTimeoutProbe = 0x301,
+  // debug builds (FA_DEBUG): device-side index checks that failed
+  kDevCheckFirst = 0x401,
+  kDevCheckDecodePiece = 0x401,    // a planned piece outside its unit or batch
+  kDevCheckDecodeSlot = 0x402,     // a partial result slot past max_slots
+  kDevCheckDecodeRow = 0x403,      // an output row past B x Hq
+  kDevCheckDecodeMerge = 0x404,    // a merge over more pieces than slots
+  kDevCheckPrefillItem = 0x411,    // a work item or Q tile outside the problem
+  kDevCheckPrefillKv = 0x412,      // a KV tile outside the sequence
+  kDevCheckPrefillOut = 0x413,     // an output row outside the tensor
+  kDevCheckLast = 0x4ff,
 };
 
 // Largest persistent prefill grid the workspace's schedule has room for.

@@ -97,6 +97,9 @@ struct PrefillArgs {
   int n_qpairs, n_kv_tiles, n_items;  // work items per (batch, head), KV tiles, all items
   long long out_row_stride, out_head_stride, out_batch_stride;  // elements
   float scale_log2;
+#ifdef FA_DEBUG
+  long long T_q;  // packed query rows (index checks only)
+#endif
 };
 
 // Barrier slots (8 bytes each) after the tiles.
@@ -285,6 +288,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const WorkItem<D> wi = work_item<D>(a, w);
       const int kvh = wi.kvh;
       const auto& seq = wi.seq;
+      if (!FA_CHECK(w >= 0 && wi.b < a.B && wi.h < a.Hq && wi.q_row0 < wi.S_q &&
+                        wi.q_base + wi.S_q <= (a.varlen != nullptr ? a.T_q : a.S_q) &&
+                        seq.end <= wi.n_kv,
+                    a.status, kDevCheckPrefillItem)) {
+        ok = false;
+        break;
+      }
       if (r > 0) {
         // the Q region is free once both streams' S products of the last item are done
         ok = mbar_wait(bar(kBarQFree), (r - 1) & 1, a.timeout_ns, a.status, kDevTimeoutQ,
@@ -303,6 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       for (int j = seq.next(0); ok && j < seq.end; j = seq.next(j + 1)) {
+      if (!FA_CHECK(j >= 0 && j * kBN < wi.S_kv, a.status, kDevCheckPrefillKv)) {
+        ok = false;
+        break;
+      }
       const bool fix_v = !seq.full(j);
       for (int kv = 0; kv < 2; ++kv) {
         const int slot = item % kRing;
@@ -822,7 +836,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(bar(kBarODrained + t));
       }
-      const bool row_ok = row < wi.S_q;
+      const bool row_ok = row < wi.S_q &&
+                          FA_CHECK(wi.q_base + row < (a.varlen != nullptr ? a.T_q : a.S_q),
+                                   a.status, kDevCheckPrefillOut);
       const bool invalid = (l_run == 0.f);
       const float inv_l = invalid ? 0.f : 1.f / l_run;
       __nv_bfloat16* dst = a.out + static_cast<long long>(wi.tma_b) * a.out_batch_stride +
@@ -994,6 +1010,9 @@ cudaError_t launch_prefill_d(const PrefillLaunch& x, cudaStream_t stream) {
     pa.out_batch_stride = static_cast<long long>(x.S_q) * x.Hq * D;
   }
   pa.scale_log2 = x.scale * 1.4426950408889634f;
+#ifdef FA_DEBUG
+  pa.T_q = x.T_q;
+#endif
   // persistent: one CTA per SM (each CTA holds all 512 TMEM columns)
   const int grid = x.grid;  // the schedule in the workspace was built for this grid
   prefill_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, pa);

@@ -30,6 +30,21 @@ __device__ __forceinline__ void record_error(uint32_t* status, uint32_t code) {
   if (status != nullptr) atomicCAS(status, 0u, code);
 }
 
+// Device-side index checks of debug builds (compiled with -DFA_DEBUG; the
+// library is then libfa_gb300_debug.so). A failed check records its code in
+// the status word (fa_workspace_status reports FA_ERR_DEVICE_CHECK) and the
+// guarded access is skipped; nothing traps. In release builds the checks
+// compile to nothing.
+#ifdef FA_DEBUG
+__device__ __forceinline__ bool fa_check(bool ok, uint32_t* status, uint32_t code) {
+  if (!ok) record_error(status, code);
+  return ok;
+}
+#define FA_CHECK(cond, status, code) ::fa::fa_check((cond), (status), (code))
+#else
+#define FA_CHECK(cond, status, code) true
+#endif
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

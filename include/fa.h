@@ -71,7 +71,9 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 3,         /* allowed by the pages but not built here (D not 64/128/256) */
   FA_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes below the size query's answer */
   FA_ERR_RUNTIME = 5,             /* a CUDA call failed (launch, copy, device query) */
-  FA_ERR_DEVICE_TIMEOUT = 6       /* a kernel's bounded wait expired; outputs are undefined */
+  FA_ERR_DEVICE_TIMEOUT = 6,      /* a kernel's bounded wait expired; outputs are undefined */
+  FA_ERR_DEVICE_CHECK = 7         /* debug builds only (libfa_gb300_debug.so, FA_DEBUG): a
+                                     device-side index check failed and the access was skipped */
 } fa_status;
 
 typedef enum {
@@ -332,7 +334,8 @@ fa_status fa_decode_noalloc_status(void* stream);
 /* ------------------------------------------------------------ diagnostics
  * Synchronises `stream`, then reads and clears the device status word at
  * the start of a workspace used by fa_forward / fa_decode. Returns FA_OK,
- * FA_ERR_DEVICE_TIMEOUT (a bounded wait in a kernel expired) or
+ * FA_ERR_DEVICE_TIMEOUT (a bounded wait in a kernel expired),
+ * FA_ERR_DEVICE_CHECK (debug builds: an index check failed) or
  * FA_ERR_RUNTIME. */
 fa_status fa_workspace_status(void* workspace, void* stream);
 

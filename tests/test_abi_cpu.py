@@ -42,7 +42,7 @@ def test_exports_every_declared_function(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.fa_abi_version() == 1
-    for s in range(7):
+    for s in range(8):
         assert lib.fa_status_string(s)
     assert b"unknown" in lib.fa_status_string(99)
 
@@ -479,3 +479,12 @@ def test_forward_varlen_ex_workspace_and_empty_batch(lib):
     assert _fwd_varlen_ex(lib, [0, 10], [0, 10], [3], [3], ws_bytes=16) == \
         _lib.FA_ERR_WORKSPACE_TOO_SMALL
     assert _fwd_varlen_ex(lib, [0], [0], [], []) == _lib.FA_OK  # B = 0: nothing to do
+
+
+def test_debug_library_exports_every_declared_function():
+    """The FA_DEBUG build (device-side index checks) carries the same C ABI."""
+    dbg = _lib.load_debug()
+    for n in header_functions():
+        assert hasattr(dbg, n), n
+    assert dbg.fa_abi_version() == 1
+    assert b"FA_ERR_DEVICE_CHECK" in dbg.fa_status_string(_lib.FA_ERR_DEVICE_CHECK)
