@@ -125,7 +125,9 @@ def attention(q, k, v, *, scale: float = 1.0, layout: str = "BNSD", causal: bool
     """out (fp64, same layout as q) and lse (fp64, [B, Hq, S_q]).
 
     q: [B,Hq,S_q,D] (BNSD) or [B,S_q,Hq,D] (BSND); k, v likewise with Hkv heads.
-    key_mask: optional [B, S_kv], nonzero = masked. actual_seq_lengths:
+    key_mask: optional [B, S_kv], nonzero = masked, or one mask per query head
+    ([IFA] §四 attenMask shapes (B, N, 1, S) and (1, N, 1, S)): [B, Hq, S_kv] or
+    [1, Hq, S_kv] (the singleton batch is shared by every batch). actual_seq_lengths:
     optional per-batch valid KV length (default S_kv). rows: optional list of
     query indices; then only those rows are evaluated and the S_q axis of the
     results has len(rows) entries, in that order. window: optional
@@ -146,16 +148,22 @@ def attention(q, k, v, *, scale: float = 1.0, layout: str = "BNSD", causal: bool
     lens = [S_kv] * B if actual_seq_lengths is None else [int(x) for x in actual_seq_lengths]
     out = np.zeros((B, Hq, R, D))
     lse = np.full((B, Hq, R), np.inf)
+    per_head = km is not None and km.ndim == 3
     for b in range(B):
         L = max(0, min(lens[b], S_kv))
-        ok = valid_key_matrix(rows, S_kv, L, None if km is None else km[b], causal, window)
-        # keys that no row can see (past L or masked) are dropped outright, so
-        # whatever they hold (NaN included) never enters a product
-        cols = np.nonzero(ok.any(axis=0))[0]
-        okc = ok[:, cols]
-        has_key = okc.any(axis=1)
         for h in range(Hq):
             kvh = h // g
+            if per_head:
+                mrow = km[b if km.shape[0] > 1 else 0, h]
+            else:
+                mrow = None if km is None else km[b]
+            ok = valid_key_matrix(rows, S_kv, L, mrow, causal, window)
+            # keys that no row of this head can see (past L or masked) are
+            # dropped outright, so whatever they hold (NaN included) never
+            # enters a product
+            cols = np.nonzero(ok.any(axis=0))[0]
+            okc = ok[:, cols]
+            has_key = okc.any(axis=1)
             kk = kn[b, kvh][cols]
             vv = vn[b, kvh][cols]
             s = scale * (qn[b, h] @ kk.T)
@@ -202,7 +210,9 @@ def attention_bruteforce(q, k, v, *, scale: float = 1.0, layout: str = "BNSD",
             for i in range(S_q):
                 keys = []
                 for j in range(min(L, S_kv)):
-                    if km is not None and km[b, j]:
+                    if km is not None and km.ndim == 3 and km[b if km.shape[0] > 1 else 0, h, j]:
+                        continue  # one mask per query head
+                    if km is not None and km.ndim == 2 and km[b, j]:
                         continue
                     if causal and j > i:
                         continue

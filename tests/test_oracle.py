@@ -509,3 +509,58 @@ def test_varlen_truncated_rows_and_keys_have_no_effect():
                                      seqused_kv=skv, key_mask=km)
     np.testing.assert_array_equal(o1, o2)
     np.testing.assert_array_equal(l1, l2)
+
+
+def _per_head_case(seed, B=2, Hq=4, Hkv=2, S=9, D=6):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, Hq, 1, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, Hkv, S, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, Hkv, S, D, generator=g).to(torch.bfloat16)
+    return q, k, v
+
+
+@pytest.mark.parametrize("mb", [2, 1])
+def test_per_head_mask_equals_bruteforce(mb):
+    """attenMask of [IFA] §四 with one mask per query head, (B, N, 1, S) and the
+    batch-shared (1, N, 1, S): each head against the scalar-loop definition."""
+    q, k, v = _per_head_case(17)
+    g = torch.Generator().manual_seed(18)
+    km = (torch.rand(mb, 4, 9, generator=g) < 0.4).to(torch.uint8)
+    km[0, 1, :] = 1  # head 1 of batch 0 (and, shared, of every batch when mb = 1) sees nothing
+    lens = [9, 6]
+    o1, l1 = oracle.decode(q, k, v, lens, scale=0.3, key_mask=km)
+    o2, l2 = oracle.attention_bruteforce(q, k, v, scale=0.3, key_mask=km, actual_seq_lengths=lens)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(np.isfinite(l1), np.isfinite(l2))
+    fin = np.isfinite(l2)
+    np.testing.assert_allclose(l1[fin], l2[fin], rtol=0, atol=1e-12)
+    assert np.all(l1[0, 1] == np.inf) and np.all(o1[0, 1] == 0)
+
+
+def test_per_head_mask_with_equal_rows_is_the_shared_mask():
+    """A per-head mask whose heads all carry the same row is exactly the
+    (B, 1, 1, S) key mask."""
+    q, k, v = _per_head_case(19)
+    g = torch.Generator().manual_seed(20)
+    km2 = (torch.rand(2, 9, generator=g) < 0.3).to(torch.uint8)
+    km3 = km2[:, None, :].expand(2, 4, 9).contiguous()
+    o1, l1 = oracle.decode(q, k, v, [9, 8], scale=0.5, key_mask=km2)
+    o2, l2 = oracle.decode(q, k, v, [9, 8], scale=0.5, key_mask=km3)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_per_head_mask_keys_masked_for_a_head_have_no_effect_on_it():
+    """Whatever a key holds (NaN included), a head that masks it is not
+    changed by it; a head that sees it is (the mask is per head)."""
+    q, k, v = _per_head_case(21, B=1)
+    km = torch.zeros(1, 4, 9, dtype=torch.uint8)
+    km[0, 0, 3] = 1  # head 0 masks key 3; head 1 (same KV head) sees it
+    o1, l1 = oracle.decode(q, k, v, [9], scale=0.4, key_mask=km)
+    k2, v2 = k.clone(), v.clone()
+    k2[0, 0, 3] += 1.0
+    v2[0, 0, 3] = float("nan")
+    o2, l2 = oracle.decode(q, k2, v2, [9], scale=0.4, key_mask=km)
+    np.testing.assert_array_equal(o1[0, 0], o2[0, 0])
+    np.testing.assert_array_equal(l1[0, 0], l2[0, 0])
+    assert not np.all(np.isfinite(o2[0, 1]))  # head 1 reads the changed key
