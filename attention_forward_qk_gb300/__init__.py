@@ -7,6 +7,7 @@ from .fa import (  # noqa: F401
     FaError,
     fa_abi_version,
     fa_decode,
+    fa_decode_masked,
     fa_decode_noalloc,
     fa_decode_noalloc_status,
     fa_decode_paged,

@@ -29,6 +29,9 @@ FA_MASK_CAUSAL = 3
 FA_MASK_WINDOW = 4
 FA_LAYOUT_PA_BBND = 2
 FA_LAYOUT_PA_BNBD = 3
+FA_KEY_MASK_B11S = 0
+FA_KEY_MASK_BN1S = 1
+FA_KEY_MASK_1N1S = 2
 
 _i64 = ctypes.c_int64
 _vp = ctypes.c_void_p
@@ -61,6 +64,9 @@ SIGNATURES = {
     "fa_decode": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                                  ctypes.c_float, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _sz,
                                  _vp]),
+    "fa_decode_masked": (ctypes.c_int, [_vp, _vp, _vp, _vp, ctypes.c_int, _vp, _i64, _i64, _i64,
+                                        _i64, _i64, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                        _vp, _vp, _vp, _sz, _vp]),
     "fa_decode_plan": (ctypes.c_int, [_i64, _i64, _i64, _i64, _i64, _vp, ctypes.c_int, ctypes.c_int,
                                       ctypes.POINTER(_i64), ctypes.POINTER(_i64),
                                       ctypes.POINTER(_i64)]),

@@ -700,12 +700,15 @@ struct PagedKv {
 // only after every argument check); it need only hold what this call's plan
 // uses. Otherwise the workspace must hold the size query's bound, as the
 // contract of fa_decode states.
+// mask_layout: FA_KEY_MASK_B11S (one flag per key, shared by the heads),
+// FA_KEY_MASK_BN1S or FA_KEY_MASK_1N1S (one row of flags per query head).
 fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv* pg,
                       const uint8_t* key_mask, const int64_t* lens, int64_t B, int64_t S_kv_max,
                       int64_t num_heads, int64_t num_kv_heads, int64_t D, float scale, int layout,
                       int num_splits, void* out, float* lse, void* workspace,
                       size_t workspace_bytes, void* stream,
-                      fa_status (*scratch)(void**) = nullptr) {
+                      fa_status (*scratch)(void**) = nullptr,
+                      int mask_layout = FA_KEY_MASK_B11S) {
   const bool exact_ws = scratch != nullptr;
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr ||
       (workspace == nullptr && !exact_ws) || lens == nullptr)
@@ -714,6 +717,9 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
   fa_status st = check_common(B, 1, S_kv_max, num_heads, Hkv, D, scale, layout);
   if (st != FA_OK) return st;
   if (num_splits < 0) return FA_ERR_PARAM_INVALID;
+  if (mask_layout != FA_KEY_MASK_B11S && mask_layout != FA_KEY_MASK_BN1S &&
+      mask_layout != FA_KEY_MASK_1N1S)
+    return FA_ERR_PARAM_INVALID;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
     return FA_ERR_PARAM_INVALID;
@@ -795,6 +801,11 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
   x.k = k;
   x.v = v;
   x.key_mask = key_mask;
+  const long long S_mask = std::max<int64_t>(S_kv_max, 1);
+  x.mask_bstride = mask_layout == FA_KEY_MASK_B11S   ? S_mask
+                   : mask_layout == FA_KEY_MASK_BN1S ? S_mask * num_heads
+                                                     : 0;
+  x.mask_hstride = mask_layout == FA_KEY_MASK_B11S ? 0 : S_mask;
   x.B = static_cast<int>(B);
   x.Hq = static_cast<int>(num_heads);
   x.Hkv = static_cast<int>(Hkv);
@@ -841,6 +852,16 @@ fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* 
                     void* stream) {
   return decode_impl(q, k, v, nullptr, key_mask, lens, B, S_kv_max, num_heads, num_kv_heads, D,
                      scale, layout, num_splits, out, lse, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_decode_masked(const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                           int key_mask_layout, const int64_t* lens, int64_t B, int64_t S_kv_max,
+                           int64_t num_heads, int64_t num_kv_heads, int64_t D, float scale,
+                           int layout, int num_splits, void* out, float* lse, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  return decode_impl(q, k, v, nullptr, key_mask, lens, B, S_kv_max, num_heads, num_kv_heads, D,
+                     scale, layout, num_splits, out, lse, workspace, workspace_bytes, stream,
+                     nullptr, key_mask_layout);
 }
 
 fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cache,

@@ -126,6 +126,10 @@ struct DecodeArgs {
   // rounded up (the real length is the work-space length minus this)
   unsigned char pad16[kDecodeParamBatches];
   Prefix prefix;           // prefix[b] = sum of lengths of batches < b (work space)
+  // key mask element (b, query head h, key j) at key_mask[b * mask_bstride +
+  // h * mask_hstride + j]: (B, 1, 1, S) has mask_hstride 0, (1, N, 1, S)
+  // mask_bstride 0
+  long long mask_bstride, mask_hstride;
 };
 
 // Largest b with KH * (prefix[b] + pc * b) <= r: with pc = 0 the batch whose
@@ -508,7 +512,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         ++piece_seq;
         row_begin = hd.row0;
         row_end = hd.row0 + hd.vend;  // rows past a paged length hold no key
-        mask_row = a.key_mask ? a.key_mask + static_cast<size_t>(hd.b) * a.S_kv : nullptr;
+        // the mask row of this lane's head x (the same row for every head of a
+        // (B, 1, 1, S) mask)
+        mask_row = nullptr;
+        if (a.key_mask != nullptr) {
+          const long long h0 = static_cast<long long>(hd.kh / a.head_groups) * g_total +
+                               static_cast<long long>(hd.kh % a.head_groups) * G + x;
+          mask_row = a.key_mask + hd.b * a.mask_bstride + h0 * a.mask_hstride;
+        }
         const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(qbuf + slot * C::QB);
         m = -INFINITY;
         l = 0.f;
@@ -535,7 +546,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       // every row of the stage holds a key: no per-row checks
       const bool dense = mask_row == nullptr && stage_row0 + C::R <= row_end;
       float s[C::STEPS];
-      bool valid[C::STEPS];
+      bool valid[C::STEPS];  // some head of the row group sees the key
 #pragma unroll
       for (int i = 0; i < C::STEPS; ++i) {
         const int r = warp * C::RPWS + i * C::RPW + rg;
@@ -543,9 +554,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         bool ok = true;
         if (!dense) {
           ok = gr < row_end;
-          if (ok && mask_row != nullptr) ok = mask_row[gr] == 0;
+          if (ok && mask_row != nullptr) ok = mask_row[gr] == 0;  // head x
+          // the V row is zeroed only when no head of the row group sees it
+          const uint32_t seen = __ballot_sync(0xffffffffu, ok) >> (rg * C::LPR);
+          valid[i] = (seen & ((1u << C::LPR) - 1u)) != 0u;
+        } else {
+          valid[i] = true;
         }
-        valid[i] = ok;
         uint64_t kp[NP];
 #pragma unroll
         for (int ch = 0; ch < C::NCH; ++ch) {
@@ -938,6 +953,8 @@ cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
                                                x.lens_host[b]);
   da.counters = x.counters;
   da.has_empty = x.has_empty ? 1 : 0;
+  da.mask_bstride = x.mask_bstride;
+  da.mask_hstride = x.mask_hstride;
 
   if (x.total > 0) {
     // K, V with stage-high boxes (112 rows, 56 for D = 256); K, V with the

@@ -96,6 +96,7 @@ struct DecodeLaunch {
   const void* k;
   const void* v;
   const uint8_t* key_mask;
+  long long mask_bstride, mask_hstride;  // key mask strides (elements) of batch and query head
   int B, Hq, Hkv, S_kv, D, layout;
   float scale;
   long long total;            // rows of the work space (KV heads x head groups x sum L_b)

@@ -291,6 +291,44 @@ def fa_decode(q, k, v, actual_seq_lengths, *, key_mask=None, scale=1.0, layout="
     return out, lse
 
 
+KEY_MASK_LAYOUTS = {"B11S": 0, "BN1S": 1, "1N1S": 2}
+
+
+def fa_decode_masked(q, k, v, actual_seq_lengths, key_mask, key_mask_layout, *, scale=1.0,
+                     layout="BNSD", num_splits=0, out=None, lse=None, return_lse=True,
+                     workspace=None, stream=None):
+    """fa_decode with the key mask in a given layout: "B11S" [B, S_kv] (shared
+    by the heads), "BN1S" [B, Hq, S_kv] or "1N1S" [Hq, S_kv] (one row per
+    query head). Returns (out, lse)."""
+    lid = _layout_id(layout)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n)
+    _check_tensor(key_mask, "key_mask", torch.uint8)
+    B, Hq, S_q, D = _dims(q, lid)
+    if S_q != 1:
+        raise ValueError("decode takes one query row per batch (S_q = 1)")
+    _, Hkv, S_kv, _ = _dims(k, lid)
+    ml = KEY_MASK_LAYOUTS[key_mask_layout] if isinstance(key_mask_layout, str) else key_mask_layout
+    want = {0: B * S_kv, 1: B * Hq * S_kv, 2: Hq * S_kv}.get(ml)
+    if want is not None and key_mask.numel() != want:
+        raise ValueError("key_mask size does not match its layout")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(fa_decode_workspace_size(B, S_kv, Hq, Hkv, D, num_splits),
+                                dtype=torch.uint8, device=q.device)
+    lens_arr, _ = _lens_array(actual_seq_lengths, B)
+    st = _lib.load().fa_decode_masked(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), key_mask.data_ptr(), int(ml), lens_arr, B, S_kv,
+        Hq, Hkv, D, float(scale), lid, int(num_splits), out.data_ptr(),
+        lse.data_ptr() if lse is not None else None, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    check(st, "fa_decode_masked")
+    return out, lse
+
+
 def fa_decode_paged(q, k_cache, v_cache, block_table, block_size, actual_seq_lengths, *,
                     kv_layout="PA_BBND", key_mask=None, scale=1.0, num_splits=0, num_heads=None,
                     num_kv_heads=None, out=None, lse=None, return_lse=True, workspace=None,

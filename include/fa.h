@@ -236,6 +236,30 @@ fa_status fa_decode(const void* q, const void* k, const void* v, const uint8_t* 
                     int num_splits, void* out, float* lse, void* workspace,
                     size_t workspace_bytes, void* stream);
 
+/* Layouts of the decode key mask (aclnnIncreFlashAttention guide §四,
+ * attenMask): one flag per key shared by every query head, (B, 1, 1, S) =
+ * [B, S_kv_max]; or one row of flags per query head, (B, N, 1, S) =
+ * [B, num_heads, S_kv_max], or the same rows for every batch, (1, N, 1, S) =
+ * [num_heads, S_kv_max]. */
+typedef enum {
+  FA_KEY_MASK_B11S = 0,
+  FA_KEY_MASK_BN1S = 1,
+  FA_KEY_MASK_1N1S = 2
+} fa_key_mask_layout;
+
+/* fa_decode with the key mask in any of the layouts above (fa_decode's
+ * key_mask is FA_KEY_MASK_B11S). With a per-head mask, query head h keeps
+ * key j iff j < actual_seq_lengths[b] and its own flag is 0; a key that some
+ * head of its KV group still sees must hold finite K and V values (keys past
+ * a length, or masked for every head of the group, may hold anything).
+ * key_mask_layout outside the enum -> FA_ERR_PARAM_INVALID; the other
+ * arguments, the workspace and the errors are those of fa_decode. */
+fa_status fa_decode_masked(const void* q, const void* k, const void* v, const uint8_t* key_mask,
+                           int key_mask_layout, const int64_t* actual_seq_lengths, int64_t B,
+                           int64_t S_kv_max, int64_t num_heads, int64_t num_kv_heads, int64_t D,
+                           float scale, int layout, int num_splits, void* out, float* lse,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
 /* Split-KV decode against a paged K/V cache (FlashAttn guide §1.2,
  * PagedAttention: the cache is stored in blocks of block_size tokens and a
  * block table maps each sequence's logical blocks to physical ones).

@@ -488,3 +488,10 @@ def test_debug_library_exports_every_declared_function():
         assert hasattr(dbg, n), n
     assert dbg.fa_abi_version() == 1
     assert b"FA_ERR_DEVICE_CHECK" in dbg.fa_status_string(_lib.FA_ERR_DEVICE_CHECK)
+
+
+def test_decode_masked_rejects_an_unknown_mask_layout(lib):
+    lens = (ctypes.c_int64 * 1)(10)
+    st = lib.fa_decode_masked(P, P, P, P, 3, lens, 1, 16, 4, 4, 128, 0.1, 0, 0, P, None, WS,
+                              1 << 22, None)
+    assert st == _lib.FA_ERR_PARAM_INVALID
