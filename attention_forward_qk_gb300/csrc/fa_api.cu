@@ -43,16 +43,21 @@ int64_t chunk_for_splits(int64_t S_kv_max, int num_splits) {
 }
 
 struct DecodeWs {
-  size_t prefix, real_lens, counters, part_lse, part_o, total;
+  size_t prefix, real_lens, counters, grp_counters, part_lse, part_o, grp_lse, grp_o, total;
+  size_t clear;  // bytes from the start that are cleared before the launch
 };
 
-// [status word, piece counters | pad][length prefix sums, large batches
-// only][real lengths, paged][partial lse][partial o]: the counters follow the
-// status word so that one clear before the launch covers both
-DecodeWs decode_ws(int64_t B, int64_t Hq, int64_t D, int64_t max_slots) {
+// [status word, unit counters, group counters | pad][length prefix sums,
+// large batches only][real lengths, paged][partial lse][partial o][group lse]
+// [group o]: the counters follow the status word so that one clear before the
+// launch covers them all. groups: merge groups per unit (forced split counts,
+// else 0).
+DecodeWs decode_ws(int64_t B, int64_t Hq, int64_t D, int64_t max_slots, int64_t groups = 0) {
   DecodeWs w;
-  w.counters = sizeof(uint32_t);  // per (batch, KV head, head group): pieces finished
-  size_t off = align_up(sizeof(uint32_t) * (1 + B * Hq));
+  w.counters = sizeof(uint32_t);  // per (batch, KV head, head group): pieces (or groups) finished
+  w.grp_counters = w.counters + sizeof(uint32_t) * B * Hq;  // [units][groups]: pieces finished
+  w.clear = w.grp_counters + sizeof(uint32_t) * B * Hq * groups;
+  size_t off = align_up(w.clear);
   w.prefix = off;
   off += align_up(sizeof(int64_t) * (B + 1));
   w.real_lens = off;  // paged cache only
@@ -61,8 +66,17 @@ DecodeWs decode_ws(int64_t B, int64_t Hq, int64_t D, int64_t max_slots) {
   off += align_up(sizeof(float) * B * Hq * max_slots);
   w.part_o = off;
   off += align_up(sizeof(float) * B * Hq * max_slots * D);
+  w.grp_lse = off;
+  off += align_up(sizeof(float) * B * Hq * groups);
+  w.grp_o = off;
+  off += align_up(sizeof(float) * B * Hq * groups * D);
   w.total = off;
   return w;
+}
+
+// Merge groups of a unit cut into `slots` pieces by a forced split count.
+int64_t merge_groups(int64_t slots, int num_splits) {
+  return num_splits > 0 && slots > 1 ? ceil_div(slots, kDecodeMergeGroup) : 0;
 }
 
 // Upper bound of the pieces one sequence is cut into, for the size query.
@@ -392,7 +406,8 @@ size_t fa_decode_workspace_size(int64_t B, int64_t S_kv_max, int64_t num_heads,
   if (num_kv_heads == 0) num_kv_heads = num_heads;
   if (B < 0 || S_kv_max < 0 || num_heads < 0 || num_kv_heads < 0 || D < 0 || num_splits < 0)
     return 0;
-  return decode_ws(B, num_heads, D, max_slots_bound(S_kv_max, num_splits)).total;
+  const int64_t slots = max_slots_bound(S_kv_max, num_splits);
+  return decode_ws(B, num_heads, D, slots, merge_groups(slots, num_splits)).total;
 }
 
 // Head dims: 64, 128 and 256.
@@ -749,7 +764,8 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
   const int64_t slots = std::max<int64_t>(max_slots, 1);
   if (slots > max_slots_bound(S_kv_max, num_splits)) return FA_ERR_RUNTIME;  // cannot happen
   // partial buffers only when some sequence is cut into several pieces
-  const DecodeWs ws = decode_ws(B, num_heads, D, max_slots > 1 ? slots : 0);
+  const int64_t groups = max_slots > 1 ? merge_groups(slots, num_splits) : 0;
+  const DecodeWs ws = decode_ws(B, num_heads, D, max_slots > 1 ? slots : 0, groups);
   if (workspace_bytes < ws.total) return FA_ERR_WORKSPACE_TOO_SMALL;
   if (exact_ws) {
     st = scratch(&workspace);
@@ -792,8 +808,7 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
   // the status word, and the piece counters of the units cut into several
   // pieces, start at zero: one clear on the stream before the launch (a
   // kernel-side clear could erase a timeout another CTA recorded first)
-  const size_t clear_bytes =
-      sizeof(uint32_t) * (1 + ((total > 0 && max_slots > 1) ? B * KH : 0));
+  const size_t clear_bytes = (total > 0 && max_slots > 1) ? ws.clear : sizeof(uint32_t);
   if (cudaMemsetAsync(wsb, 0, clear_bytes, s) != cudaSuccess) return FA_ERR_RUNTIME;
 
   DecodeLaunch x;
@@ -816,18 +831,20 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
   x.total = total;
   x.rows_per_cta = rc;
   x.piece_cost = pc;
-  // a forced split count cuts fixed-size shares: one CTA per SM takes them in
-  // turn (no CTA more than half as many as it can record split pieces of)
+  // a forced split count cuts fixed-size chunks: one CTA per SM takes them in
+  // turn and hands them to its consumer warps (split_kernel)
   x.loop_shares = num_splits > 0;
-  x.n_ctas = x.loop_shares ? std::max<int64_t>(std::min<int64_t>(n_ctas, sms),
-                                                ceil_div(n_ctas, kDecodeLoopSharesPerCta))
-                           : n_ctas;
+  x.n_ctas = x.loop_shares ? std::min<int64_t>(n_ctas, sms) : n_ctas;
   x.max_slots = static_cast<int>(slots);
   x.prefix_host = prefix;
   x.prefix_dev = in_params ? nullptr : reinterpret_cast<const long long*>(wsb + ws.prefix);
   x.part_o = reinterpret_cast<float*>(wsb + ws.part_o);
   x.part_lse = reinterpret_cast<float*>(wsb + ws.part_lse);
   x.counters = reinterpret_cast<unsigned int*>(wsb + ws.counters);
+  x.grp_counters = reinterpret_cast<unsigned int*>(wsb + ws.grp_counters);
+  x.grp_lse = reinterpret_cast<float*>(wsb + ws.grp_lse);
+  x.grp_o = reinterpret_cast<float*>(wsb + ws.grp_o);
+  x.max_groups = static_cast<int>(std::max<int64_t>(groups, 1));
   x.has_empty = has_empty;
   x.block_table = pg != nullptr ? pg->block_table : nullptr;
   x.max_blocks = pg != nullptr ? static_cast<int>(pg->max_blocks) : 0;

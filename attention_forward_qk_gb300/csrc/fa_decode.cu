@@ -130,6 +130,15 @@ struct DecodeArgs {
   // h * mask_hstride + j]: (B, 1, 1, S) has mask_hstride 0, (1, N, 1, S)
   // mask_bstride 0
   long long mask_bstride, mask_hstride;
+  // forced split counts (split_kernel): the pieces of a unit are merged in
+  // groups of kMergeGroup slots, then the groups; group partials
+  // [B][Hq][max_groups][D] (normalised) and [B][Hq][max_groups] (log2 lse),
+  // piece counters per group [units][max_groups] (group counters per unit in
+  // `counters`)
+  float* grp_o;
+  float* grp_lse;
+  unsigned int* grp_counters;
+  int max_groups;
 };
 
 // Largest b with KH * (prefix[b] + pc * b) <= r: with pc = 0 the batch whose
@@ -240,17 +249,11 @@ struct Pending {
 };
 
 // How the work space is cut into shares, one instantiation each so that the
-// code of the common case carries nothing of the others:
+// code of the common case carries nothing of the other:
 //   kSharesRows  one share per CTA, equal in rows
 //   kSharesCost  one share per CTA, equal in cost (piece_cost > 0)
-//   kSharesLoop  fixed-size shares (a forced split count), more than CTAs:
-//                each CTA takes shares blockIdx.x, blockIdx.x + gridDim.x, ...
-//                and counts the split pieces of all of them at its end
-constexpr int kSharesRows = 0, kSharesCost = 1, kSharesLoop = 2;
-// split pieces a CTA can record in the loop mode (two per share at most; the
-// host gives no CTA more than half as many shares)
-constexpr int kMaxLoopPending = 512;
-constexpr int kLoopSmemExtra = 1024 + kMaxLoopPending * 16;
+// (a forced split count runs split_kernel instead)
+constexpr int kSharesRows = 0, kSharesCost = 1;
 
 template <int D, int G, int kShares>
 __global__ void __launch_bounds__(kDecThreads, 1)
@@ -261,7 +264,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   using C = DecCfg<D, G>;
   constexpr int NP = C::NP;
   constexpr int NST = C::NST;
-  static_assert(kShares != kSharesLoop || C::SMEM + kLoopSmemExtra <= 232448, "shared memory");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -271,13 +273,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   // bars: full[kMaxStages], empty[kMaxStages], scratch free[2], scratch parked[2]
   SlotHeader* hdr = reinterpret_cast<SlotHeader*>(bars + 2 * kMaxStages + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(hdr + kMaxStages);
-  // split pieces of this CTA (at most its first and its last; in the loop
-  // mode those of all its shares, after the barrier block): counted at the end
+  // split pieces of this CTA (at most its first and its last): counted at the end
   int* n_pending = const_cast<int*>(abort_flag) + 1;
-  Pending* pending = kShares == kSharesLoop
-                         ? reinterpret_cast<Pending*>(qbuf + kMaxStages * C::QB + 1024)
-                         : reinterpret_cast<Pending*>(n_pending + 3);  // [2]
-  constexpr int kPendingCap = kShares == kSharesLoop ? kMaxLoopPending : 2;
+  Pending* pending = reinterpret_cast<Pending*>(n_pending + 3);  // [2]
+  constexpr int kPendingCap = 2;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -335,14 +334,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     // the next piece of this CTA's range [r, r1): its unit, rows and stages
     auto plan = [&](int piece, SlotHeader& h, int& kvh, int& hg) {
       h = SlotHeader{-1, 0, 1, 0, 0, 0, 0, 0, 0, 0};
-      if constexpr (kShares == kSharesLoop) {
-        while (r >= r1) {  // this share is done: the CTA's next one
-          v += gridDim.x;
-          if (v * Rc >= a.total) return;
-          r = v * Rc;
-          r1 = min(r + Rc, a.total);
-        }
-      }
       if (r >= r1) return;
       const int b = find_batch(a.prefix, a.B, KH, 0, r);
       const long long base = KH * a.prefix[b];
@@ -797,32 +788,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   __syncthreads();
   // ---- count this CTA's split pieces; the CTA that finishes a unit's last
   // piece merges the unit (every partial of it is visible by then)
-  if constexpr (kShares == kSharesLoop) {
-    // many pieces: every thread counts some; a unit to merge is marked by a
-    // negative nsp, then its G rows are merged one warp per row
-    const int np = min(*n_pending, kPendingCap);
-    if (np == 0 || *abort_flag) return;
-    if (tid < np) __threadfence();  // the partials of this CTA, written before the barrier
-    bool merges = false;
-    for (int e = tid; e < np; e += kDecThreads) {
-      const unsigned c = atomicAdd(a.counters + pending[e].unit, 1u);
-      if (c == static_cast<unsigned>(pending[e].nsp - 1)) {
-        pending[e].nsp = -pending[e].nsp;
-        merges = true;
-      }
-    }
-    if (merges) __threadfence();  // the other CTAs' partials of those units, before reading them
-    __syncthreads();
-    for (int t = warp; t < np * G; t += kDecWarps + 1) {
-      const Pending p = pending[t / G];
-      if (p.nsp >= 0) continue;
-      const int kvh = p.kh / a.head_groups;
-      const int hg = p.kh % a.head_groups;
-      const size_t bh0 = static_cast<size_t>(p.b) * a.Hq + kvh * g_total + hg * G;
-      merge_row<D>(a, bh0 + t % G, -p.nsp, lane);
-    }
-    return;
-  }
   const int np = min(*n_pending, 2);
   if (np == 0 || *abort_flag) return;
   volatile int* merge_mask = n_pending + 1;
@@ -848,6 +813,608 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const size_t bh0 = static_cast<size_t>(p.b) * a.Hq + kvh * g_total + hg * G;
     merge_row<D>(a, bh0 + h, p.nsp, lane);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Forced split counts (num_splits > 0: the FlashDecoding tutorial's fixed
+// number of KV chunks per sequence, §三 3.2). The work space is cut into
+// chunks of Rc rows (the last one shorter); CTA c takes the chunks c, c + G,
+// c + 2G, ... (G = gridDim.x) and hands them to its consumer warps in turn:
+// warp w takes its CTA's chunks w, w + 7, w + 14, ... Every stage carries one
+// slice (one tail box of RPWS rows) per warp, from that warp's current chunk,
+// so that each warp walks its own chunks slice by slice. A piece is a chunk's
+// rows within one unit; the warp ends each of its pieces by itself: it sums
+// its row groups, writes the piece's normalised partial o and log-sum-exp (or
+// the output, when the piece is the whole unit) and counts the piece in the
+// unit's counter; the warp that completes a unit's count merges the unit.
+// No piece end waits for the other warps, so pieces of a few stages stay
+// cheap.
+// A group of the pieces of one unit, complete and to be merged.
+struct GroupTask {
+  int unit, nsp, b, kh, g;
+};
+// pieces of a unit merged together before the groups are
+constexpr int kMergeGroup = kDecodeMergeGroup;
+
+struct WarpSlice {
+  int b, kh;   // batch and unit (KV head x head group) of the slice
+  int row;     // first key row of the slice within the unit
+  int rows;    // rows of the slice in the piece (0: the warp has nothing in this stage)
+  int vend;    // rows of the slice that hold keys (fewer only past a paged length)
+  int slot;    // the piece's partial slot within the unit
+  int nsp;     // pieces of the unit
+  int flags;   // kSliceFirst | kSliceLast
+};
+constexpr int kSliceFirst = 1, kSliceLast = 2;
+
+template <int D, int G>
+struct SplitCfg {
+  using C = DecCfg<D, G>;
+  static constexpr int SLICE = C::RPWS;  // rows of a warp's slice
+  static_assert(SLICE == C::TAIL, "a slice is one tail box");
+  // ring | q of each (slot, warp) | slices [slot][warp] | barriers, flags
+  static constexpr int QW_OFF = kRingBytes;
+  static constexpr int SL_OFF = QW_OFF + C::NST * kDecWarps * C::QB;
+  static constexpr int BAR_OFF = SL_OFF + C::NST * kDecWarps * static_cast<int>(sizeof(WarpSlice));
+  // groups of pieces whose count this CTA completed, merged after its stream
+  static constexpr int DEF_OFF = BAR_OFF + 256;
+  static constexpr int MAX_DEFERRED = 512;
+  static constexpr int SMEM = DEF_OFF + MAX_DEFERRED * static_cast<int>(sizeof(GroupTask)) + 1024;
+  static_assert(SMEM <= 232448, "shared memory");
+};
+
+// Merge partials [k0, k1) of one (batch, query head) row (normalised o of D
+// floats each at o_row, log2 lse at lse_row) into a running state (M, W,
+// acc), as merge_row does: all lse and o loads of up to 8 partials in flight
+// before any is used, the largest lse factored out.
+template <int D>
+__device__ __forceinline__ void merge_range(const float* lse_row, const float* o_row, int k0,
+                                            int k1, int lane, float& M, float& W,
+                                            float (&acc)[D / 32]) {
+  constexpr int EPL = D / 32;
+  const float* pl = lse_row;
+  const float* po = o_row + lane * EPL;
+  for (int kb = k0; kb < k1; kb += 8) {
+    float lk[8], v[8][EPL];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const bool in = kb + u < k1;
+      lk[u] = in ? __ldcg(pl + kb + u) : -INFINITY;
+#pragma unroll
+      for (int e = 0; e < EPL; e += 2) {
+        const float2 t = in ? __ldcg(reinterpret_cast<const float2*>(po + static_cast<size_t>(kb + u) * D + e))
+                            : make_float2(0.f, 0.f);
+        v[u][e] = t.x;
+        v[u][e + 1] = t.y;
+      }
+    }
+    float mb = M;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) mb = fmaxf(mb, lk[u]);
+    if (mb == -INFINITY) continue;  // only empty pieces so far
+    const float sc = ex2(M - mb);
+    W *= sc;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] *= sc;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float wk = ex2(lk[u] - mb);
+      W += wk;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wk, v[u][e], acc[e]);
+    }
+    M = mb;
+  }
+}
+
+// Write a merged row: out = acc / W (bf16), lse = M + log2 W (natural log);
+// no valid key at all: out 0, lse +inf.
+template <int D>
+__device__ __forceinline__ void write_merged(const DecodeArgs& a, size_t row, int lane, float M,
+                                             float W, const float (&acc)[D / 32]) {
+  constexpr int EPL = D / 32;
+  const bool invalid = (M == -INFINITY);
+  const float inv = invalid ? 0.f : 1.f / W;
+  __nv_bfloat16* dst = a.out + row * D + lane * EPL;
+#pragma unroll
+  for (int e = 0; e < EPL; e += 2)
+    *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+  if (lane == 0 && a.lse != nullptr) a.lse[row] = invalid ? INFINITY : (M + log2f(W)) * kLn2;
+}
+
+// One warp finishes a complete group of pieces: for each of the G rows it
+// merges the group's pieces in slot order into the group partial (or, when
+// the unit has one group, into the output); then it counts the group, and
+// the warp that completes the unit's groups merges them, in order, into the
+// output. Nothing waits for another warp or CTA.
+template <int D, int G>
+__device__ __forceinline__ void finish_group(const DecodeArgs& a, const GroupTask& t, int lane) {
+  constexpr int EPL = D / 32;
+  const int g_total = a.Hq / a.Hkv;
+  const size_t bh0 = static_cast<size_t>(t.b) * a.Hq + (t.kh / a.head_groups) * g_total +
+                     (t.kh % a.head_groups) * G;
+  const int ng = (t.nsp + kMergeGroup - 1) / kMergeGroup;
+  const int k0 = t.g * kMergeGroup, k1 = min(k0 + kMergeGroup, t.nsp);
+#pragma unroll 1
+  for (int h = 0; h < G; ++h) {
+    const size_t row = bh0 + h;
+    float M = -INFINITY, W = 0.f, acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    merge_range<D>(a.part_lse + row * a.max_slots, a.part_o + row * a.max_slots * D, k0, k1,
+                   lane, M, W, acc);
+    if (ng == 1) {
+      write_merged<D>(a, row, lane, M, W, acc);
+    } else {
+      const bool empty = (M == -INFINITY);
+      const float inv = empty ? 0.f : 1.f / W;
+      float* dst = a.grp_o + (row * a.max_groups + t.g) * D + lane * EPL;
+#pragma unroll
+      for (int e = 0; e < EPL; e += 2)
+        *reinterpret_cast<float2*>(dst + e) = make_float2(acc[e] * inv, acc[e + 1] * inv);
+      if (lane == 0) a.grp_lse[row * a.max_groups + t.g] = empty ? -INFINITY : M + log2f(W);
+    }
+  }
+  if (ng == 1) return;
+  __threadfence();  // this lane's group partials, before the count
+  __syncwarp();
+  unsigned c = 0;
+  if (lane == 0) c = atomicAdd(a.counters + t.unit, 1u);
+  c = __shfl_sync(0xffffffffu, c, 0);
+  if (c != static_cast<unsigned>(ng - 1)) return;
+  __threadfence();  // the other groups' partials, before they are read
+#pragma unroll 1
+  for (int h = 0; h < G; ++h) {
+    const size_t row = bh0 + h;
+    float M = -INFINITY, W = 0.f, acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    merge_range<D>(a.grp_lse + row * a.max_groups, a.grp_o + row * a.max_groups * D, 0, ng, lane,
+                   M, W, acc);
+    write_merged<D>(a, row, lane, M, W, acc);
+  }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kDecThreads, 1)
+    split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                 const __grid_constant__ CUtensorMap tm_k16,
+                 const __grid_constant__ CUtensorMap tm_v16,
+                 const __grid_constant__ DecodeArgs a) {
+  using C = DecCfg<D, G>;
+  using SC = SplitCfg<D, G>;
+  constexpr int NP = C::NP;
+  constexpr int NST = C::NST;
+  constexpr int SLICE = SC::SLICE;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* qw = smem + SC::QW_OFF;  // [NST][warps][QB]
+  WarpSlice* slices = reinterpret_cast<WarpSlice*>(smem + SC::SL_OFF);  // [NST][warps]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SC::BAR_OFF);     // full[NST], empty[NST]
+  volatile int* done = reinterpret_cast<volatile int*>(bars + 2 * kMaxStages);  // [NST]: no more work
+  volatile int* abort_flag = done + kMaxStages;
+  int* n_deferred = const_cast<int*>(abort_flag) + 1;
+  GroupTask* deferred = reinterpret_cast<GroupTask*>(smem + SC::DEF_OFF);  // [MAX_DEFERRED]
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const long long KH = static_cast<long long>(a.Hkv) * a.head_groups;
+  const int g_total = a.Hq / a.Hkv;
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = smem_u32(bars + kMaxStages);
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kDecWarps);
+    }
+    *abort_flag = 0;
+    *n_deferred = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kDecWarps) {
+    // ================================================================ producer
+    // lane w < 7 plans the slices of consumer warp w; lane 0 completes the
+    // stage's barrier bookkeeping
+    const long long Rc = a.rows_per_cta;  // chunk rows
+    const long long n_chunks = (a.total + Rc - 1) / Rc;
+    long long v = static_cast<long long>(blockIdx.x) + static_cast<long long>(lane) * gridDim.x;
+    bool have = lane < kDecWarps && v < n_chunks;
+    long long r = have ? v * Rc : 0;
+    long long r_end = have ? min(r + Rc, a.total) : 0;
+    long long u0 = 0, u1 = 0;  // the unit holding row r (rows of the work space)
+    int ub = 0, ukh = 0;
+    if (lane == 0) {
+      tma_prefetch_map(&tm_k16);
+      tma_prefetch_map(&tm_v16);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    int st = 0;
+    bool ok = true;
+    for (;; ++st) {
+      const int slot = st % NST;
+      const int use = st / NST;
+      if (use > 0) {
+        ok = mbar_wait_polled(empty0 + 8 * slot, (use - 1) & 1, a.timeout_ns, a.status,
+                              kDevTimeoutDecodeEmpty, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      // this warp's next slice
+      if (have && r >= r_end) {
+        v += static_cast<long long>(kDecWarps) * gridDim.x;  // the warp's next chunk
+        have = v < n_chunks;
+        if (have) {
+          r = v * Rc;
+          r_end = min(r + Rc, a.total);
+        }
+      }
+      WarpSlice ws{0, 0, 0, 0, 0, 0, 0, 0};
+      uint32_t bytes = 0;
+      if (have) {
+        if (r < u0 || r >= u1) {
+          const int b = find_batch(a.prefix, a.B, KH, 0, r);
+          const long long base = KH * a.prefix[b];
+          const long long L = a.prefix[b + 1] - a.prefix[b];
+          const long long kh = div_nn(r - base, L);
+          u0 = base + kh * L;
+          u1 = u0 + L;
+          ub = b;
+          ukh = static_cast<int>(kh);
+        }
+        const long long p0 = max(u0, v * Rc), p1 = min(u1, r_end);  // this piece
+        const int rows = static_cast<int>(min(static_cast<long long>(SLICE), p1 - r));
+        ws.b = ub;
+        ws.kh = ukh;
+        ws.row = static_cast<int>(r - u0);
+        ws.rows = rows;
+        ws.vend = rows;
+        if (a.block_table != nullptr) {
+          const long long real =
+              a.real_len != nullptr ? __ldg(a.real_len + ub) : (u1 - u0) - a.pad16[ub];
+          ws.vend = static_cast<int>(max(0ll, min(static_cast<long long>(rows), real - ws.row)));
+        }
+        ws.slot = static_cast<int>(v - div_nn(u0, Rc));
+        ws.nsp = static_cast<int>(div_nn(u1 - 1, Rc) - div_nn(u0, Rc) + 1);
+        ws.flags = (r == p0 ? kSliceFirst : 0) | (r + rows == p1 ? kSliceLast : 0);
+        bytes = 2u * SLICE * D * 2 + ((ws.flags & kSliceFirst) ? G * D * 2 : 0);
+        r += rows;
+      }
+      uint32_t total_bytes = bytes;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        total_bytes += __shfl_xor_sync(0xffffffffu, total_bytes, off);
+      const bool any = __any_sync(0xffffffffu, have);
+      if (lane < kDecWarps) slices[slot * kDecWarps + lane] = ws;
+      __syncwarp();  // every lane's slice is written before lane 0 publishes the stage
+      if (!any) {
+        if (lane == 0) {
+          done[slot] = 1;
+          mbar_arrive(full0 + 8 * slot);  // end marker: no data
+        }
+        ++st;
+        break;
+      }
+      if (lane == 0) {
+        done[slot] = 0;
+        mbar_expect_tx(full0 + 8 * slot, total_bytes);
+      }
+      __syncwarp();
+      if (have) {
+        const uint32_t dst = smem_u32(smem + slot * C::STAGE_BYTES) + lane * SLICE * D * 2;
+        const int kvh = ws.kh / a.head_groups;
+        const int hg = ws.kh % a.head_groups;
+        if (a.block_table != nullptr) {
+          // a slice never straddles a block: blocks are multiples of 16 rows and
+          // slices start at multiples of SLICE rows of the (16-row rounded) unit
+          const int32_t* bt = a.block_table + static_cast<size_t>(ws.b) * a.max_blocks;
+          const int blk = __ldg(bt + ws.row / a.block_size);
+          const int in_blk = ws.row % a.block_size;
+          tma_load_4d(dst, &tm_k16, full0 + 8 * slot, 0, in_blk, kvh, blk);
+          tma_load_4d(dst + C::TILE_BYTES, &tm_v16, full0 + 8 * slot, 0, in_blk, kvh, blk);
+        } else {
+          tma_load_4d(dst, &tm_k16, full0 + 8 * slot, 0, ws.row, kvh, ws.b);
+          tma_load_4d(dst + C::TILE_BYTES, &tm_v16, full0 + 8 * slot, 0, ws.row, kvh, ws.b);
+        }
+        if (ws.flags & kSliceFirst) {
+          const __nv_bfloat16* qsrc =
+              a.q + (static_cast<size_t>(ws.b) * a.Hq + kvh * g_total + hg * G) * D;
+          bulk_load(smem_u32(qw + (slot * kDecWarps + lane) * C::QB), qsrc, G * D * 2,
+                    full0 + 8 * slot);
+        }
+      }
+    }
+    if (*abort_flag && lane == 0) {
+      // let every copy this CTA started land before shared memory is released
+      const uint64_t drain_ns = a.timeout_ns > kDrainFloorNs ? a.timeout_ns : kDrainFloorNs;
+      for (int s = max(0, st - NST); s < st; ++s)
+        mbar_wait_polled(full0 + 8 * (s % NST), (s / NST) & 1, drain_ns, a.status,
+                         kDevTimeoutDrain, nullptr);
+    }
+    return;
+  }
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (a.has_empty) {
+    // sequences of length 0: out = 0, lse = +inf; one thread per row
+    for (int row = static_cast<int>(blockIdx.x) * kDecWarps * 32 + tid; row < a.B * a.Hq;
+         row += static_cast<int>(gridDim.x) * kDecWarps * 32) {
+      const int b = row / a.Hq;
+      if (a.prefix[b + 1] != a.prefix[b]) continue;
+      uint4* dst = reinterpret_cast<uint4*>(a.out + static_cast<size_t>(row) * D);
+#pragma unroll
+      for (int i = 0; i < D * 2 / 16; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (a.lse != nullptr) a.lse[row] = INFINITY;
+    }
+  }
+  // ================================================================ consumers
+  // The lane layout of decode_kernel: LPR lanes share a K/V row, each lane
+  // holds q and o of all G heads in the order j -> head j ^ x (x = sub >>
+  // SHIFT) and ends the butterfly with the score of head x.
+  const int sub = lane % C::LPR;
+  const int rg = lane / C::LPR;
+  const int x = sub >> C::SHIFT;
+  float m = -INFINITY, l = 0.f;  // head x of this row group
+  uint64_t o[G][NP];
+  uint64_t qp[G][NP];
+  const uint8_t* mask_row = nullptr;
+  size_t bh0 = 0;  // the piece's first (batch, query head) row
+#pragma unroll
+  for (int j = 0; j < G; ++j)
+#pragma unroll
+    for (int k = 0; k < NP; ++k) o[j][k] = 0ull;
+
+  for (int st = 0;; ++st) {
+    const int slot = st % NST;
+    bool got = mbar_wait_polled(full0 + 8 * slot, (st / NST) & 1, a.timeout_ns, a.status,
+                                kDevTimeoutDecodeFull, abort_flag);
+    got = __all_sync(0xffffffffu, got);
+    if (!got || done[slot]) break;
+    const WarpSlice ws = slices[slot * kDecWarps + warp];
+    if (ws.rows > 0) {
+      if (ws.flags & kSliceFirst) {
+        // ---- a new piece of this warp: q landed with this stage; fresh state
+        const int kvh = ws.kh / a.head_groups;
+        const int hg = ws.kh % a.head_groups;
+        bh0 = static_cast<size_t>(ws.b) * a.Hq + kvh * g_total + hg * G;
+        mask_row = nullptr;
+        if (a.key_mask != nullptr)
+          mask_row = a.key_mask + ws.b * a.mask_bstride +
+                     (static_cast<long long>(kvh) * g_total + hg * G + x) * a.mask_hstride;
+        const __nv_bfloat16* qs =
+            reinterpret_cast<const __nv_bfloat16*>(qw + (slot * kDecWarps + warp) * C::QB);
+        m = -INFINITY;
+        l = 0.f;
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+#pragma unroll
+          for (int k = 0; k < NP; ++k) o[j][k] = 0ull;
+#pragma unroll
+          for (int ch = 0; ch < C::NCH; ++ch) {
+            const uint4 u =
+                *reinterpret_cast<const uint4*>(qs + (j ^ x) * D + (sub + C::LPR * ch) * 8);
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              qp[j][ch * 4 + k] = pair_f32(bf16lo_to_f32(w4[k]) * a.scale_log2,
+                                           bf16hi_to_f32(w4[k]) * a.scale_log2);
+          }
+        }
+      }
+      // ---- this warp's slice: SLICE rows of K and V at rows
+      // [warp * SLICE, (warp + 1) * SLICE) of the stage
+      const __nv_bfloat16* Ks = reinterpret_cast<const __nv_bfloat16*>(smem + slot * C::STAGE_BYTES);
+      const __nv_bfloat16* Vs = Ks + C::R * D;
+      const int stage_row0 = ws.row - warp * SLICE;  // key row of stage row 0
+      const int row_end = ws.row + ws.vend;
+      const bool dense = mask_row == nullptr && ws.vend == SLICE;
+      float s[C::STEPS];
+      bool valid[C::STEPS];  // some head of the row group sees the key
+#pragma unroll
+      for (int i = 0; i < C::STEPS; ++i) {
+        const int rr = warp * SLICE + i * C::RPW + rg;
+        const int gr = stage_row0 + rr;
+        bool ok = true;
+        if (!dense) {
+          ok = gr < row_end;
+          if (ok && mask_row != nullptr) ok = mask_row[gr] == 0;
+          const uint32_t seen = __ballot_sync(0xffffffffu, ok) >> (rg * C::LPR);
+          valid[i] = (seen & ((1u << C::LPR) - 1u)) != 0u;
+        } else {
+          valid[i] = true;
+        }
+        uint64_t kp[NP];
+#pragma unroll
+        for (int ch = 0; ch < C::NCH; ++ch) {
+          const uint4 u = *reinterpret_cast<const uint4*>(Ks + rr * D + (sub + C::LPR * ch) * 8);
+          kp[ch * 4 + 0] = bf16x2_pair(u.x);
+          kp[ch * 4 + 1] = bf16x2_pair(u.y);
+          kp[ch * 4 + 2] = bf16x2_pair(u.z);
+          kp[ch * 4 + 3] = bf16x2_pair(u.w);
+        }
+        float part[G];
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          uint64_t ac = ffma2(qp[j][0], kp[0], 0ull);
+          if constexpr (G <= 2) {
+            uint64_t ac2 = ffma2(qp[j][1], kp[1], 0ull);
+#pragma unroll
+            for (int k = 2; k < NP; k += 2) {
+              ac = ffma2(qp[j][k], kp[k], ac);
+              ac2 = ffma2(qp[j][k + 1], kp[k + 1], ac2);
+            }
+            ac = fadd2(ac, ac2);
+          } else {
+#pragma unroll
+            for (int k = 1; k < NP; ++k) ac = ffma2(qp[j][k], kp[k], ac);
+          }
+          const float2 a2 = unpair(ac);
+          part[j] = a2.x + a2.y;
+        }
+#pragma unroll
+        for (int lv = 0; lv < C::LG; ++lv) {
+          const int half = G >> (lv + 1);
+#pragma unroll
+          for (int j = 0; j < half; ++j)
+            part[j] += __shfl_xor_sync(0xffffffffu, part[j + half], (C::LPR / 2) >> lv);
+        }
+#pragma unroll
+        for (int lv = C::LG; lv < C::LOG_LPR; ++lv)
+          part[0] += __shfl_xor_sync(0xffffffffu, part[0], (C::LPR / 2) >> lv);
+        s[i] = ok ? part[0] : -INFINITY;
+      }
+      // online softmax of head x over this slice (running max shared by the row groups)
+      float mx = s[0];
+#pragma unroll
+      for (int i = 1; i < C::STEPS; ++i) mx = fmaxf(mx, s[i]);
+#pragma unroll
+      for (int off = C::LPR; off < 32; off <<= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mn = fmaxf(m, mx);
+      const float m_use = (mn == -INFINITY) ? 0.f : mn;
+      const float alpha = ex2(m - m_use);  // 0 when m was -inf
+      m = mn;
+      float ps = 0.f;
+#pragma unroll
+      for (int i = 0; i < C::STEPS; ++i) {
+        s[i] = ex2(s[i] - m_use);  // -inf -> 0
+        ps += s[i];
+      }
+      l = fmaf(l, alpha, ps);
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          const float aj = j == 0 ? alpha : __shfl_xor_sync(0xffffffffu, alpha, j << C::SHIFT);
+          const uint64_t a2 = pair_f32(aj, aj);
+#pragma unroll
+          for (int k = 0; k < NP; ++k) o[j][k] = fmul2(o[j][k], a2);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < C::STEPS; ++i) {
+        const int rr = warp * SLICE + i * C::RPW + rg;
+        uint64_t vp[NP];
+#pragma unroll
+        for (int ch = 0; ch < C::NCH; ++ch) {
+          uint4 u = *reinterpret_cast<const uint4*>(Vs + rr * D + (sub + C::LPR * ch) * 8);
+          if (!dense && !valid[i]) u = make_uint4(0u, 0u, 0u, 0u);  // never a stale row
+          vp[ch * 4 + 0] = bf16x2_pair(u.x);
+          vp[ch * 4 + 1] = bf16x2_pair(u.y);
+          vp[ch * 4 + 2] = bf16x2_pair(u.z);
+          vp[ch * 4 + 3] = bf16x2_pair(u.w);
+        }
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          const float pj = j == 0 ? s[i] : __shfl_xor_sync(0xffffffffu, s[i], j << C::SHIFT);
+          const uint64_t p2 = pair_f32(pj, pj);
+#pragma unroll
+          for (int k = 0; k < NP; ++k) o[j][k] = ffma2(p2, vp[k], o[j][k]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+    if (ws.rows == 0 || !(ws.flags & kSliceLast)) continue;
+
+    // ================================================= end of this warp's piece
+    // l of head x over the row groups (m is shared); the accumulators halved
+    // across the row groups so that a lane keeps 1/RPW of them, summed
+#pragma unroll
+    for (int off = C::LPR; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    constexpr int F = G * NP;
+    constexpr int FQ = F / C::RPW;
+    const bool b0 = (rg & 1) != 0, b1 = (rg & 2) != 0;
+    uint64_t h1[F / 2];
+#pragma unroll
+    for (int f = 0; f < F / 2; ++f) {
+      const uint64_t lo = o[f / NP][f % NP], hi = o[(f + F / 2) / NP][(f + F / 2) % NP];
+      const uint64_t keep = b0 ? hi : lo, send = b0 ? lo : hi;
+      const float2 sp = unpair(send);
+      const float rx = __shfl_xor_sync(0xffffffffu, sp.x, C::LPR);
+      const float ry = __shfl_xor_sync(0xffffffffu, sp.y, C::LPR);
+      h1[f] = fadd2(keep, pair_f32(rx, ry));
+    }
+    uint64_t hq[FQ];
+    if constexpr (C::RPW == 4) {
+#pragma unroll
+      for (int f = 0; f < F / 4; ++f) {
+        const uint64_t keep = b1 ? h1[f + F / 4] : h1[f], send = b1 ? h1[f] : h1[f + F / 4];
+        const float2 sp = unpair(send);
+        const float rx = __shfl_xor_sync(0xffffffffu, sp.x, 2 * C::LPR);
+        const float ry = __shfl_xor_sync(0xffffffffu, sp.y, 2 * C::LPR);
+        hq[f] = fadd2(keep, pair_f32(rx, ry));
+      }
+    } else {
+#pragma unroll
+      for (int f = 0; f < FQ; ++f) hq[f] = h1[f];
+    }
+    // write the piece: o / l of every head (l of head h from a lane whose
+    // head x is h) and one lse per head
+    const int base = (b0 ? F / 2 : 0) + (b1 ? F / 4 : 0);
+#pragma unroll
+    for (int f = 0; f < FQ; ++f) {
+      const int fl = base + f;
+      const int j = fl / NP, k = fl % NP;
+      const int h = j ^ x;
+      const float lh = __shfl_sync(0xffffffffu, l, h << C::SHIFT);
+      const float inv = lh > 0.f ? 1.f / lh : 0.f;
+      const int d = (sub + C::LPR * (k / 4)) * 8 + 2 * (k % 4);
+      const float2 v2 = unpair(hq[f]);
+      if (FA_CHECK(bh0 + h < static_cast<size_t>(a.B) * a.Hq, a.status, kDevCheckDecodeRow) &&
+          FA_CHECK(ws.nsp == 1 || ws.slot < a.max_slots, a.status, kDevCheckDecodeSlot)) {
+        if (ws.nsp == 1)
+          *reinterpret_cast<uint32_t*>(a.out + (bh0 + h) * D + d) = pack_bf16x2(v2.x * inv, v2.y * inv);
+        else
+          *reinterpret_cast<float2*>(a.part_o + ((bh0 + h) * a.max_slots + ws.slot) * D + d) =
+              make_float2(v2.x * inv, v2.y * inv);
+      }
+    }
+    if (rg == 0 && (sub & ((1 << C::SHIFT) - 1)) == 0) {  // one lane per head x
+      const bool empty = !(l > 0.f);
+      if (ws.nsp == 1) {
+        if (a.lse != nullptr) a.lse[bh0 + x] = empty ? INFINITY : (m + log2f(l)) * kLn2;
+      } else {
+        a.part_lse[(bh0 + x) * a.max_slots + ws.slot] = empty ? -INFINITY : m + log2f(l);
+      }
+    }
+    if (ws.nsp > 1) {
+      // count the piece in its group; the CTA that completes a group merges
+      // it after its stream (at once when its list is full)
+      __threadfence();  // this lane's partial, before the count
+      __syncwarp();
+      const int unit = static_cast<int>(ws.b * KH + ws.kh);
+      const int g = ws.slot / kMergeGroup;
+      const int gsize = min(kMergeGroup, ws.nsp - g * kMergeGroup);
+      int slot_def = -2;  // -2: the group is not complete
+      if (lane == 0) {
+        const unsigned c =
+            atomicAdd(a.grp_counters + static_cast<size_t>(unit) * a.max_groups + g, 1u);
+        if (c == static_cast<unsigned>(gsize - 1)) {
+          __threadfence();  // the other pieces' partials, before they are read
+          slot_def = atomicAdd(n_deferred, 1);
+          if (slot_def < SC::MAX_DEFERRED)
+            deferred[slot_def] = GroupTask{unit, ws.nsp, ws.b, ws.kh, g};
+          else
+            slot_def = -1;
+        }
+      }
+      slot_def = __shfl_sync(0xffffffffu, slot_def, 0);
+      if (slot_def == -1)
+        finish_group<D, G>(a, GroupTask{unit, ws.nsp, ws.b, ws.kh, g}, lane);
+    }
+  }
+
+  // ---- the groups this CTA completed, one warp each
+  asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
+  if (*abort_flag) return;
+  const int nd = min(*n_deferred, SC::MAX_DEFERRED);
+#pragma unroll 1
+  for (int t = warp; t < nd; t += kDecWarps) finish_group<D, G>(a, deferred[t], lane);
 }
 
 // When no sequence has a key stage 1 is not launched: every row gets out = 0
@@ -877,9 +1444,8 @@ cudaError_t launch_decode_dg(int grid, bool loop, const CUtensorMap* m, const De
       e = cudaFuncSetAttribute(decode_kernel<D, G, kSharesCost>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, DecCfg<D, G>::SMEM);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_kernel<D, G, kSharesLoop>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               DecCfg<D, G>::SMEM + kLoopSmemExtra);
+      e = cudaFuncSetAttribute(split_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SplitCfg<D, G>::SMEM);
     if (e != cudaSuccess) return e;
     setup_done(configured);
   }
@@ -894,8 +1460,8 @@ cudaError_t launch_decode_dg(int grid, bool loop, const CUtensorMap* m, const De
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (loop) {
-    cfg.dynamicSmemBytes = DecCfg<D, G>::SMEM + kLoopSmemExtra;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<D, G, kSharesLoop>, m[0], m[1], m[2], m[3], da);
+    cfg.dynamicSmemBytes = SplitCfg<D, G>::SMEM;
+    return cudaLaunchKernelEx(&cfg, split_kernel<D, G>, m[0], m[1], m[2], m[3], da);
   }
   if (da.piece_cost != 0)
     return cudaLaunchKernelEx(&cfg, decode_kernel<D, G, kSharesCost>, m[0], m[1], m[2], m[3], da);
@@ -955,6 +1521,10 @@ cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
   da.has_empty = x.has_empty ? 1 : 0;
   da.mask_bstride = x.mask_bstride;
   da.mask_hstride = x.mask_hstride;
+  da.grp_o = x.grp_o;
+  da.grp_lse = x.grp_lse;
+  da.grp_counters = x.grp_counters;
+  da.max_groups = x.max_groups;
 
   if (x.total > 0) {
     // K, V with stage-high boxes (112 rows, 56 for D = 256); K, V with the

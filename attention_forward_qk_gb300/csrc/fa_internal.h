@@ -50,6 +50,9 @@ inline int prefill_kv_tile(int64_t D) { return D == 256 ? 64 : 128; }
 // prefix sums travel as launch parameters (larger batches use the workspace).
 constexpr int kDecodeStageRows = 112;
 constexpr int kDecodeParamBatches = 1024;
+// Forced split counts merge the pieces of a unit in groups of this many
+// slots, then the groups.
+constexpr int kDecodeMergeGroup = 32;
 // Smallest share of the work space one decode CTA is given.
 constexpr int kDecodeMinRowsPerCta = 224;
 // Cost of a piece end (park, combine, partial write) in K/V rows of D = 128
@@ -57,9 +60,6 @@ constexpr int kDecodeMinRowsPerCta = 224;
 // rows: only when there are more units than SMs, so that a share holds
 // several unit starts.
 constexpr int kDecodePieceCostRows128 = 96;
-// Forced split counts: most fixed-size shares one CTA takes in turn (each
-// leaves at most two split pieces to count at the CTA's end).
-constexpr int kDecodeLoopSharesPerCta = 256;
 
 // Error codes written to the device status word (first one wins).
 enum DeviceError : uint32_t {
@@ -103,13 +103,19 @@ struct DecodeLaunch {
   long long rows_per_cta;     // cost of each CTA's contiguous share (a row costs 1)
   long long piece_cost;       // cost of a unit start after the first (0: shares of rows)
   long long n_ctas;           // CTAs to launch
-  bool loop_shares;           // fixed-size shares, more than CTAs (a forced split count)
+  bool loop_shares;           // fixed-size chunks, more than CTAs (a forced split count: split_kernel)
   int max_slots;              // piece slots per (batch, head) in the partial buffers
   const long long* prefix_host;  // [B + 1] prefix sums of the lengths
   const long long* prefix_dev;   // the same in the workspace, or null (then in params)
   float* part_o;            // [B, Hq, max_slots, D]
   float* part_lse;          // [B, Hq, max_slots] (log2 domain)
-  unsigned int* counters;   // [B * units per batch] pieces finished, zeroed before the launch
+  unsigned int* counters;   // [B * units per batch] pieces (forced splits: groups) finished, zeroed before the launch
+  // forced split counts: group partials [B, Hq, max_groups, D] and
+  // [B, Hq, max_groups], pieces finished per group [units][max_groups] (zeroed)
+  float* grp_o;
+  float* grp_lse;
+  unsigned int* grp_counters;
+  int max_groups;
   bool has_empty;           // some sequence has length 0
   // paged K/V (block_table != null): k, v are block pools of num_blocks blocks
   // of block_size rows in `layout` (BSND: PA_BBND, BNSD: PA_BNBD), logical
