@@ -907,6 +907,69 @@ __device__ __forceinline__ void merge_range(const float* lse_row, const float* o
   }
 }
 
+// merge_range for at most 32 partials, in one or two rounds of loads: lane k
+// loads partial k's lse while every lane loads its part of a whole batch of
+// o rows; the largest lse and the weights then come by shuffles, and the
+// batch is summed without a rescale chain. Same result as merge_range up to
+// the order of the additions within the batch (fixed, so still deterministic).
+template <int D>
+__device__ __forceinline__ void merge_few(const float* lse_row, const float* o_row, int k0, int k1,
+                                          int lane, float& M, float& W, float (&acc)[D / 32]) {
+  constexpr int EPL = D / 32;
+  constexpr int BK = 128 / EPL < 32 ? 128 / EPL : 32;  // pieces per batch of loads
+  const int n = k1 - k0;  // <= 32
+  const float* po = o_row + static_cast<size_t>(k0) * D + lane * EPL;
+  const float lk = lane < n ? __ldcg(lse_row + k0 + lane) : -INFINITY;
+  float v[BK][EPL];
+#pragma unroll
+  for (int u = 0; u < BK; ++u)
+#pragma unroll
+    for (int e = 0; e < EPL; e += 2) {
+      const float2 t = u < n ? __ldcg(reinterpret_cast<const float2*>(po + static_cast<size_t>(u) * D + e))
+                             : make_float2(0.f, 0.f);
+      v[u][e] = t.x;
+      v[u][e + 1] = t.y;
+    }
+  float mx = lk;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  M = mx;
+  W = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+  if (mx == -INFINITY) return;  // only empty pieces
+  const float wk = ex2(lk - mx);  // 0 for an empty or absent piece
+  float ws = wk;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, off);
+  W = ws;
+#pragma unroll
+  for (int u = 0; u < BK; ++u) {
+    const float w = __shfl_sync(0xffffffffu, wk, u);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
+  }
+#pragma unroll 1
+  for (int kb = BK; kb < n; kb += BK) {  // D = 256: a second batch
+#pragma unroll
+    for (int u = 0; u < BK; ++u)
+#pragma unroll
+      for (int e = 0; e < EPL; e += 2) {
+        const float2 t = kb + u < n
+                             ? __ldcg(reinterpret_cast<const float2*>(po + static_cast<size_t>(kb + u) * D + e))
+                             : make_float2(0.f, 0.f);
+        v[u][e] = t.x;
+        v[u][e + 1] = t.y;
+      }
+#pragma unroll
+    for (int u = 0; u < BK; ++u) {
+      const float w = __shfl_sync(0xffffffffu, wk, (kb + u) & 31);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
+    }
+  }
+}
+
 // Write a merged row: out = acc / W (bf16), lse = M + log2 W (natural log);
 // no valid key at all: out 0, lse +inf.
 template <int D>
@@ -927,7 +990,10 @@ __device__ __forceinline__ void write_merged(const DecodeArgs& a, size_t row, in
 // the unit has one group, into the output); then it counts the group, and
 // the warp that completes the unit's groups merges them, in order, into the
 // output. Nothing waits for another warp or CTA.
-template <int D, int G>
+// kBatched: merge with merge_few (after the stream, when nothing else is
+// live); the rare call from inside the streaming loop (a full list) uses
+// merge_range, whose few registers keep the loop free of spills.
+template <int D, int G, bool kBatched>
 __device__ __forceinline__ void finish_group(const DecodeArgs& a, const GroupTask& t, int lane) {
   constexpr int EPL = D / 32;
   const int g_total = a.Hq / a.Hkv;
@@ -941,8 +1007,12 @@ __device__ __forceinline__ void finish_group(const DecodeArgs& a, const GroupTas
     float M = -INFINITY, W = 0.f, acc[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-    merge_range<D>(a.part_lse + row * a.max_slots, a.part_o + row * a.max_slots * D, k0, k1,
+    if constexpr (kBatched)
+      merge_few<D>(a.part_lse + row * a.max_slots, a.part_o + row * a.max_slots * D, k0, k1,
                    lane, M, W, acc);
+    else
+      merge_range<D>(a.part_lse + row * a.max_slots, a.part_o + row * a.max_slots * D, k0, k1,
+                     lane, M, W, acc);
     if (ng == 1) {
       write_merged<D>(a, row, lane, M, W, acc);
     } else {
@@ -969,8 +1039,12 @@ __device__ __forceinline__ void finish_group(const DecodeArgs& a, const GroupTas
     float M = -INFINITY, W = 0.f, acc[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-    merge_range<D>(a.grp_lse + row * a.max_groups, a.grp_o + row * a.max_groups * D, 0, ng, lane,
+    if (kBatched && ng <= 32)
+      merge_few<D>(a.grp_lse + row * a.max_groups, a.grp_o + row * a.max_groups * D, 0, ng, lane,
                    M, W, acc);
+    else
+      merge_range<D>(a.grp_lse + row * a.max_groups, a.grp_o + row * a.max_groups * D, 0, ng,
+                     lane, M, W, acc);
     write_merged<D>(a, row, lane, M, W, acc);
   }
 }
@@ -1405,7 +1479,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
       slot_def = __shfl_sync(0xffffffffu, slot_def, 0);
       if (slot_def == -1)
-        finish_group<D, G>(a, GroupTask{unit, ws.nsp, ws.b, ws.kh, g}, lane);
+        finish_group<D, G, false>(a, GroupTask{unit, ws.nsp, ws.b, ws.kh, g}, lane);
     }
   }
 
@@ -1414,7 +1488,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   if (*abort_flag) return;
   const int nd = min(*n_deferred, SC::MAX_DEFERRED);
 #pragma unroll 1
-  for (int t = warp; t < nd; t += kDecWarps) finish_group<D, G>(a, deferred[t], lane);
+  for (int t = warp; t < nd; t += kDecWarps) finish_group<D, G, true>(a, deferred[t], lane);
 }
 
 // When no sequence has a key stage 1 is not launched: every row gets out = 0
