@@ -818,9 +818,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 // ---------------------------------------------------------------------------
 // Forced split counts (num_splits > 0: the FlashDecoding tutorial's fixed
 // number of KV chunks per sequence, §三 3.2). The work space is cut into
-// chunks of Rc rows (the last one shorter); CTA c takes the chunks c, c + G,
-// c + 2G, ... (G = gridDim.x) and hands them to its consumer warps in turn:
-// warp w takes its CTA's chunks w, w + 7, w + 14, ... Every stage carries one
+// chunks of Rc rows (the last one shorter); CTA c takes a contiguous run of
+// ceil(chunks / gridDim.x) of them and hands them to its consumer warps in
+// turn: warp w takes the run's chunks w, w + 7, w + 14, ... A run covers
+// whole groups of a unit's pieces, so the CTA that completes a group is
+// mostly the one that streamed it, and a slow SM delays few groups. Every stage carries one
 // slice (one tail box of RPWS rows) per warp, from that warp's current chunk,
 // so that each warp walks its own chunks slice by slice. A piece is a chunk's
 // rows within one unit; the warp ends each of its pieces by itself: it sums
@@ -1095,8 +1097,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     // stage's barrier bookkeeping
     const long long Rc = a.rows_per_cta;  // chunk rows
     const long long n_chunks = (a.total + Rc - 1) / Rc;
-    long long v = static_cast<long long>(blockIdx.x) + static_cast<long long>(lane) * gridDim.x;
-    bool have = lane < kDecWarps && v < n_chunks;
+    // this CTA's chunks: a contiguous run, so that the groups of pieces it
+    // completes (and merges) are mostly its own
+    const long long per_cta = (n_chunks + gridDim.x - 1) / gridDim.x;
+    const long long c_end = min(n_chunks, (static_cast<long long>(blockIdx.x) + 1) * per_cta);
+    long long v = static_cast<long long>(blockIdx.x) * per_cta + lane;
+    bool have = lane < kDecWarps && v < c_end;
     long long r = have ? v * Rc : 0;
     long long r_end = have ? min(r + Rc, a.total) : 0;
     long long u0 = 0, u1 = 0;  // the unit holding row r (rows of the work space)
@@ -1120,8 +1126,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
       // this warp's next slice
       if (have && r >= r_end) {
-        v += static_cast<long long>(kDecWarps) * gridDim.x;  // the warp's next chunk
-        have = v < n_chunks;
+        v += kDecWarps;  // the warp's next chunk
+        have = v < c_end;
         if (have) {
           r = v * Rc;
           r_end = min(r + Rc, a.total);
