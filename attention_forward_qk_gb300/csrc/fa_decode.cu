@@ -139,6 +139,10 @@ struct DecodeArgs {
   float* grp_lse;
   unsigned int* grp_counters;
   int max_groups;
+  // shares cut by cost: the first row of CTA c's share at prefix.local[share_off
+  // + c] (c = 0 .. gridDim.x, the last entry the end of the work space),
+  // computed on the host; -1: found by the kernel
+  int share_off;
 };
 
 // Largest b with KH * (prefix[b] + pc * b) <= r: with pc = 0 the batch whose
@@ -328,8 +332,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     long long r1 = min(T0 + Rc, a.total);
     long long v = blockIdx.x;  // the share being planned
     if constexpr (kWeighted) {
-      if (T0 > 0) r = row_at_cost(T0);
-      r1 = blockIdx.x + 1 == gridDim.x ? a.total : min(row_at_cost(T0 + Rc), a.total);
+      if (a.share_off >= 0) {
+        r = a.prefix.local[a.share_off + blockIdx.x];
+        r1 = a.prefix.local[a.share_off + blockIdx.x + 1];
+      } else {
+        if (T0 > 0) r = row_at_cost(T0);
+        r1 = blockIdx.x + 1 == gridDim.x ? a.total : min(row_at_cost(T0 + Rc), a.total);
+      }
     }
     // the next piece of this CTA's range [r, r1): its unit, rows and stages
     auto plan = [&](int piece, SlotHeader& h, int& kvh, int& hg) {
@@ -1599,6 +1608,35 @@ cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
                                                x.lens_host[b]);
   da.counters = x.counters;
   da.has_empty = x.has_empty ? 1 : 0;
+  // shares cut by cost: their first rows, as the kernel's search would find
+  // them (the row whose cost is the first at or above c * Rc), in the unused
+  // end of the parameters' prefix array when it has room; this spares every
+  // CTA two searches of the prefix sums before its first copy
+  da.share_off = -1;
+  const long long n_share = x.n_ctas + 1;
+  const long long off = x.prefix_dev == nullptr ? x.B + 1 : 0;
+  if (x.piece_cost != 0 && !x.loop_shares && x.total > 0 &&
+      off + n_share <= kDecodeParamBatches + 1) {
+    const long long KH = static_cast<long long>(x.Hkv) * (g_total / G);
+    const long long pc = x.piece_cost;
+    const long long* pre = x.prefix_host;
+    auto row_at_cost = [&](long long T) -> long long {
+      int b = 0;  // the last batch whose first row costs at most T
+      for (int i = 1; i < x.B; ++i)
+        if (KH * (pre[i] + pc * i) <= T) b = i;
+      const long long L = pre[b + 1] - pre[b];
+      const long long cb = KH * (pre[b] + pc * b);
+      const long long kh = std::min(KH - 1, (T - cb) / (L + pc));
+      const long long o = T - cb - kh * (L + pc);
+      const long long u0 = KH * pre[b] + kh * L;
+      return o < L ? u0 + o : u0 + L;
+    };
+    for (long long c = 0; c < n_share; ++c)
+      da.prefix.local[off + c] = c == 0             ? 0
+                                 : c == n_share - 1 ? x.total
+                                                    : std::min(row_at_cost(c * x.rows_per_cta), x.total);
+    da.share_off = static_cast<int>(off);
+  }
   da.mask_bstride = x.mask_bstride;
   da.mask_hstride = x.mask_hstride;
   da.grp_o = x.grp_o;

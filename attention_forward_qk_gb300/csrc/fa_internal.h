@@ -55,11 +55,11 @@ constexpr int kDecodeParamBatches = 1024;
 constexpr int kDecodeMergeGroup = 32;
 // Smallest share of the work space one decode CTA is given.
 constexpr int kDecodeMinRowsPerCta = 224;
-// Cost of a piece end (park, combine, partial write) in K/V rows of D = 128
-// (scaled by 128 / D), charged when the shares are cut by cost instead of by
-// rows: only when there are more units than SMs, so that a share holds
-// several unit starts.
-constexpr int kDecodePieceCostRows128 = 96;
+// Cost of a piece end (the warps' park and combine, a partial stage, the
+// partial write) in K/V rows of D = 128 (scaled by 128 / D), charged when the
+// shares are cut by cost instead of by rows: only when there are more units
+// than SMs, so that a share holds several unit starts.
+constexpr int kDecodePieceCostRows128 = 192;
 
 // Error codes written to the device status word (first one wins).
 enum DeviceError : uint32_t {

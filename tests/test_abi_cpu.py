@@ -198,11 +198,14 @@ def _units(lens, Hq, Hkv, D):
     return Hkv * (g // _heads_per_cta(g, D))
 
 
+PC128 = 192  # rows a unit start costs at D = 128 when the shares are cut by cost
+
+
 def _piece_cost(lens, Hq, Hkv, D, sms=152, splits=0):
     """The extra cost of a unit start: charged only when the non-empty units
-    outnumber the SMs (96 rows at D = 128, scaled by 128 / D)."""
+    outnumber the SMs (PC128 rows at D = 128, scaled by 128 / D)."""
     units = _units(lens, Hq, Hkv, D) * sum(1 for L in lens if L)
-    return 96 * 128 // D if splits == 0 and units > sms else 0
+    return PC128 * 128 // D if splits == 0 and units > sms else 0
 
 
 def _pieces(lens, Hq, Hkv, D, rc, pc=0):
@@ -247,6 +250,7 @@ def test_plan_one_share_per_sm():
     lens = [1024, 8192, 4000, 6000, 3000, 7777, 2048, 5000]
     rc, n, mx = _plan(lens, 8192, 32, 8)
     assert n == 152 and rc * 152 >= 8 * sum(lens) > rc * 151
+    assert mx == max(_pieces(lens, 32, 8, 128, rc)[0])
     # one long sequence, 32 heads: every SM streams an equal share
     rc, n, mx = _plan([131072], 131072, 32, 32)
     assert n == 152 and mx == max(_pieces([131072], 32, 32, 128, rc)[0])
@@ -255,11 +259,11 @@ def test_plan_one_share_per_sm():
 
 def test_plan_weights_unit_starts():
     # 64 sequences x 8 KV heads = 512 units > 152 SMs: the shares are cut by
-    # cost, a row costs 1 and each unit start after the first 96 rows more
+    # cost, a row costs 1 and each unit start after the first PC128 rows more
     lens = [(37 * b) % 2000 + 1 for b in range(64)]
     rc, n, mx = _plan(lens, 2048, 32, 8)
-    pieces, total, cost = _pieces(lens, 32, 8, 128, rc, 96)
-    assert cost == total + 96 * (64 * 8 - 1)
+    pieces, total, cost = _pieces(lens, 32, 8, 128, rc, PC128)
+    assert cost == total + PC128 * (64 * 8 - 1)
     assert rc == math.ceil(cost / 152) and n == 152 and mx == max(pieces)
     # a share that holds unit starts holds fewer rows than one that does not:
     # count the rows of every share by walking the rows with their costs
@@ -268,7 +272,7 @@ def test_plan_weights_unit_starts():
     k = 0
     for L in lens:
         for _ in range(8):
-            c0 = sum(rows) + 96 * k
+            c0 = sum(rows) + PC128 * k
             for i in range(L):
                 rows[(c0 + i) // rc] += 1
             starts[c0 // rc] += 1
@@ -277,11 +281,11 @@ def test_plan_weights_unit_starts():
     # every share but the last: its cost rc is its rows plus the piece costs
     # in it, one per unit start in it (give or take one straddling a boundary)
     for r, st in zip(rows[:-1], starts[:-1]):
-        assert rc - 96 * (st + 1) <= r <= rc - 96 * max(st - 1, 0)
-    assert max(starts) >= 3 and min(rows[:-1]) < max(rows[:-1]) - 96
-    # D = 64 (eight heads per CTA) charges 192 rows per unit start
+        assert rc - PC128 * (st + 1) <= r <= rc - PC128 * max(st - 1, 0)
+    assert max(starts) >= 3 and min(rows[:-1]) < max(rows[:-1]) - PC128
+    # D = 64 (eight heads per CTA) charges twice as many rows per unit start
     rc64, n64, _ = _plan(lens, 2048, 64, 8, D=64)
-    assert rc64 == math.ceil((8 * sum(lens) + 192 * (64 * 8 - 1)) / 152) and n64 == 152
+    assert rc64 == math.ceil((8 * sum(lens) + 2 * PC128 * (64 * 8 - 1)) / 152) and n64 == 152
     # forced splits cut rows and charge nothing
     rc2, n2, _ = _plan(lens, 2048, 32, 8, splits=4)
     assert (rc2, n2) == (512, math.ceil(8 * sum(lens) / 512))

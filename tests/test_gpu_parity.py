@@ -240,11 +240,15 @@ def test_decode_workload(cuda_device, name):
 
 @pytest.mark.parametrize("B,Hq,Hkv,S,D,layout,masked", [
     # more (batch, KV head, head group) units than SMs: the shares are cut in
-    # equal cost, each unit start costing 96 * 128 / D rows
+    # equal cost, each unit start costing 192 * 128 / D rows (their first rows
+    # computed on the host, or, when the launch parameters have no room for
+    # them, 871 to 1024 sequences, by the kernel)
     (48, 16, 4, 1500, 256, "BNSD", False),   # G = 4 at D = 256: 192 units
     (8, 32, 32, 3000, 128, "BSND", True),    # G = 1: 256 units, with a key mask
     (32, 64, 8, 1200, 64, "BNSD", False),    # G = 8 at D = 64: 256 units
     (160, 4, 1, 900, 128, "BSND", False),    # one unit per sequence, 160 units
+    (900, 8, 2, 300, 128, "BNSD", False),    # G = 4, 1800 units, shares found by the kernel
+    (1030, 8, 2, 200, 128, "BSND", True),    # prefix sums in the workspace, shares from the host
 ])
 def test_decode_shares_by_cost(cuda_device, B, Hq, Hkv, S, D, layout, masked):
     x = workloads.make_decode(B, Hq, Hkv, S, D, layout, seed=B + D, len_lo=0, len_hi=S)
