@@ -2,6 +2,7 @@
 """Benchmark of the fused attention forward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+                    [--only] [--num-splits N]
 
 One step is one call of the library's public entry point over one batch of
 the workload (default: the GQA decode workload, B=8, Hq=32, Hkv=8, D=128,
@@ -51,8 +52,11 @@ CONFIGS = {"C1": "tiny_prefill", "C2": "gqa_decode", "C3": "long_decode",
 OTHER_WORKLOADS = ("long_decode", "causal_prefill", "gqa_masked_prefill", "tiny_prefill",
                    "window_prefill", "varlen_prefill", "d256_prefill", "paged_decode",
                    "d256_decode", "batch_decode", "gqa_decode")
-KERNEL_SOURCE = {"decode": "attention_forward_qk_gb300/csrc/fa_decode.cu",
-                 "prefill": "attention_forward_qk_gb300/csrc/fa_prefill.cu"}
+# a forced split count (num_splits > 0) runs split_kernel instead of decode_kernel
+SPLIT_KERNEL = "split_kernel"
+KERNEL_SOURCE = {"decode_kernel": "attention_forward_qk_gb300/csrc/fa_decode.cu",
+                 "split_kernel": "attention_forward_qk_gb300/csrc/fa_decode.cu",
+                 "prefill_kernel": "attention_forward_qk_gb300/csrc/fa_prefill.cu"}
 
 
 # ------------------------------------------------------------------ helpers
@@ -121,10 +125,10 @@ def work_units(w, lens=None, pads=None):
     return {"step": f, "main": f}
 
 
-def traffic_from_profiles(kind, workload):
+def traffic_from_profiles(kernel, workload):
     """Per-launch DRAM bytes of the main kernel from the committed ncu summary,
     or None when there is none or the kernel source changed since."""
-    path = os.path.join(ROOT, "profiles", f"{MAIN_KERNEL[kind]}_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -132,7 +136,7 @@ def traffic_from_profiles(kind, workload):
     h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     if not m or not h:
         return None
-    src = open(os.path.join(ROOT, KERNEL_SOURCE[kind]), "rb").read()
+    src = open(os.path.join(ROOT, KERNEL_SOURCE[kernel]), "rb").read()
     if hashlib.sha256(src).hexdigest() != h.group(1):
         return None
     return float(m.group(1))
@@ -403,18 +407,21 @@ def time_steps(runner, steps, warmup, flush, fn=None, kernel=True):
     return step_ms, main_ms, launches
 
 
-def roofline(kind, units_main, main_ms, peaks, peak_kind, workload):
+def roofline(kind, units_main, main_ms, peaks, peak_kind, workload, kernel=None):
+    """`workload` names the committed profile (profiles/<kernel>_<workload>.md)
+    whose DRAM bytes are the traffic."""
+    kernel = kernel or MAIN_KERNEL[kind]
     if kind == "decode":
         achieved = units_main / (main_ms * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
-        return {"bound": "hbm", "kernel": MAIN_KERNEL[kind], "achieved": achieved, "peak": peak,
+        return {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
-                "traffic": traffic_from_profiles(kind, workload)}
+                "traffic": traffic_from_profiles(kernel, workload)}
     achieved = units_main / (main_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
-    return {"bound": "tensor", "kernel": MAIN_KERNEL[kind], "achieved": achieved, "peak": peak,
+    return {"bound": "tensor", "kernel": kernel, "achieved": achieved, "peak": peak,
             "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_kind + " (burst)",
-            "traffic": traffic_from_profiles(kind, workload)}
+            "traffic": traffic_from_profiles(kernel, workload)}
 
 
 def max_over_ranks(vals, world, device=None):
@@ -501,6 +508,11 @@ def cpu_baseline(w, budget_s=12.0):
                       f"{el:.1f} s"}
 
 
+def F_ws_size(r, w, splits):
+    """Workspace bytes of a decode call with `splits` pieces per sequence."""
+    return r.F.fa_decode_workspace_size(w.B, w.S_kv, w.Hq, w.Hkv, w.D, splits)
+
+
 def decode_sweeps(args, dev, flush, peaks, peak_kind):
     """The long decode workload with the K/V rows cut into a fixed number of
     pieces per sequence (num_splits 128 ... 1024) beside the default of one
@@ -518,10 +530,11 @@ def decode_sweeps(args, dev, flush, peaks, peak_kind):
         s_ms, m_ms, _ = time_steps(r, args.steps, args.warmup, flush)
         o_ms, o_k = sum(s_ms) / len(s_ms), sum(m_ms) / len(m_ms)
         v, u = value_of("decode", r.units["step"], o_ms)
-        rf = roofline("decode", r.units["main"], o_k, peaks, peak_kind, "long_decode")
+        rf = roofline("decode", r.units["main"], o_k, peaks, peak_kind, f"long_decode_s{n}",
+                      kernel=SPLIT_KERNEL if n else None)
         # key "0": one equal share per SM (the default plan)
         out["C3_num_splits"][str(n)] = {"value": sig(v), "unit": u, "ms": sig(o_ms),
-                                        "frac": sig(rf["frac"], 3)}
+                                        "frac": sig(rf["frac"], 3), "kernel": rf["kernel"]}
     del r
     torch.cuda.empty_cache()
     wg = workloads.WORKLOADS["gqa_decode"]
@@ -561,6 +574,10 @@ def run_gpu(args):
     B.build()
     flush = L2Flush(dev)
     main = Runner(w, dev, host_copy=True)
+    if args.num_splits:
+        # a forced split count: fixed-size pieces per sequence (split_kernel)
+        main.splits = args.num_splits
+        main.ws = torch.empty(F_ws_size(main, w, args.num_splits), dtype=torch.uint8, device=dev)
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -613,7 +630,9 @@ def run_gpu(args):
         sweeps = decode_sweeps(args, dev, flush, peaks, peak_kind)
 
     if rank == 0:
-        main_rf = roofline(w.kind, main.units["main"], kms, peaks, peak_kind, w.name)
+        main_rf = roofline(w.kind, main.units["main"], kms, peaks, peak_kind,
+                           w.name + (f"_s{args.num_splits}" if args.num_splits else ""),
+                           kernel=SPLIT_KERNEL if args.num_splits else None)
         others[w.name] = {"value": value, "unit": unit, "ms_per_step": ms, "kernel_ms": kms,
                           "roofline": main_rf}
         line = {
@@ -632,7 +651,8 @@ def run_gpu(args):
             "data": "synthetic (seeded N(0,1) bf16; stale cache rows are random bf16 bits)",
             "config": {"workload": w.name, "shape": w.note, "l2": "flushed between steps "
                        "(512 MB write then 256 MB read, outside the timed events)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+                       "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                       **({"num_splits": args.num_splits} if args.num_splits else {})},
             "roofline": main_rf,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": unit, "ms_per_step": e2e_ms,
@@ -703,11 +723,19 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ramp-s", type=float, default=0.5,
                     help="untimed steps before the timed region, in seconds (clock ramp)")
+    ap.add_argument("--num-splits", type=int, default=0,
+                    help="decode workloads: a forced number of K/V pieces per sequence "
+                         "(0: one equal share per SM)")
     ap.add_argument("--oracle-all", action="store_true",
                     help="time the fp64 oracle on the five configurations (host cores only)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.num_splits < 0 or (args.num_splits and
+                               workloads.WORKLOADS[args.workload].kind != "decode"):
+        ap.error("--num-splits takes a non-negative count and a decode workload")
+    if args.num_splits and workloads.WORKLOADS[args.workload].block_size is not None:
+        ap.error("--num-splits: the paged workload runs the default plan only")
     if args.oracle_all:
         # the oracle's own throughput on each configuration, a bounded sample
         # each (whole decode passes; sampled query rows for prefill)
