@@ -297,7 +297,7 @@ fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cach
  * is computed in pieces that are merged by their log-sum-exp.
  * With num_splits = 0 the shares are equal in cost: a row costs 1 and, when
  * the non-empty units outnumber num_sms (so that a share holds several unit
- * starts), the start of every unit after the first costs 96 * 128 / D rows
+ * starts), the start of every unit after the first costs 192 * 128 / D rows
  * more, the work of the piece end it brings; a share holding unit starts
  * then takes fewer rows. Row x of unit k costs x + that cost * k.
  *   chunk_rows  cost of a share: with num_splits = 0, the total cost divided
