@@ -18,6 +18,7 @@ from .fa import (  # noqa: F401
     fa_forward_varlen_ex,
     fa_forward_varlen_window,
     fa_forward_varlen_workspace_size,
+    fa_forward_paged,
     fa_forward_window,
     fa_forward_workspace_size,
     fa_kernel_launch_count,

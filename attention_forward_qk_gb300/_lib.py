@@ -57,6 +57,10 @@ SIGNATURES = {
     "fa_forward_window": (ctypes.c_int, [_vp, _vp, _vp, _i64, _i64, _vp, _vp, _i64, _i64, _i64,
                                          _i64, _i64, _i64, ctypes.c_float, ctypes.c_int, _vp,
                                          _vp, _vp, _sz, _vp]),
+    "fa_forward_paged": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int, _vp, _i64, _i64, _i64,
+                                        ctypes.c_int, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                        _i64, ctypes.c_float, ctypes.c_int, _vp, _vp, _vp, _sz,
+                                        _vp]),
     "fa_decode_paged": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int, _vp, _i64, _i64, _i64, _vp,
                                        _vp, _i64, _i64, _i64, _i64, ctypes.c_float, ctypes.c_int,
                                        _vp, _vp, _vp, _sz, _vp]),

@@ -454,6 +454,15 @@ PrefillHeader& prefill_header_cache() {
   return h;
 }
 
+// A paged K/V cache (fa_decode_paged, fa_forward_paged); null for a
+// contiguous one. kv_layout: FA_LAYOUT_PA_BBND or FA_LAYOUT_PA_BNBD (prefill;
+// the decode path passes the equivalent contiguous layout itself).
+struct PagedKv {
+  const int32_t* block_table;
+  int64_t max_blocks, num_blocks, block_size;
+  int kv_layout = 0;
+};
+
 // Shared by fa_forward and fa_forward_window: the window (-1, -1) is no mask,
 // (-1, 0) is causal.
 // cu_q, cu_kv: HOST prefix offsets of packed sequences (else null); then
@@ -467,7 +476,8 @@ fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok
                        int64_t num_kv_heads, int64_t D, float scale, int layout, void* out,
                        float* lse, void* workspace, size_t workspace_bytes, void* stream,
                        const int64_t* cu_q = nullptr, const int64_t* cu_kv = nullptr,
-                       const int64_t* used_q = nullptr, const int64_t* used_kv = nullptr) {
+                       const int64_t* used_q = nullptr, const int64_t* used_kv = nullptr,
+                       const PagedKv* pg = nullptr) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || workspace == nullptr)
     return FA_ERR_NULLPTR;
   int64_t Hkv = num_kv_heads;
@@ -550,9 +560,12 @@ fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok
   const int32_t* vtab_dev =
       cu_q != nullptr ? reinterpret_cast<const int32_t*>(wsb + ws.varlen) : nullptr;
   // the validity table also zeroes the V rows of excluded keys: needed for a
-  // key mask, for lengths, and for packed keys cut by seqused_kv (the rows
-  // past a used length may hold anything)
-  if ((key_mask != nullptr || lens != nullptr || truncated_kv) && S_kv > 0) {
+  // key mask, for lengths, for packed keys cut by seqused_kv (the rows past a
+  // used length may hold anything), and for a paged cache whose last KV tile
+  // runs past S_kv (its rows there are pool rows, not the zeros a load past
+  // the end of a contiguous tensor returns)
+  const bool paged_ragged = pg != nullptr && S_kv % BN != 0;
+  if ((key_mask != nullptr || lens != nullptr || truncated_kv || paged_ragged) && S_kv > 0) {
     uint32_t* bits_dev = reinterpret_cast<uint32_t*>(wsb + ws.bits);
     const int* lens_dev = lens ? reinterpret_cast<const int*>(wsb + ws.lens) : nullptr;
     // packed: the keys of sequence b start at its kv offset and end at its
@@ -594,6 +607,13 @@ fa_status forward_impl(const void* q, const void* k, const void* v, bool mask_ok
   x.varlen = vtab_dev;
   x.T_q = cu_q != nullptr ? cu_q[B] : 0;
   x.T_kv = cu_kv != nullptr ? cu_kv[B] : 0;
+  if (pg != nullptr) {
+    x.block_table = pg->block_table;
+    x.max_blocks = static_cast<int>(pg->max_blocks);
+    x.num_blocks = static_cast<int>(pg->num_blocks);
+    x.block_size = static_cast<int>(pg->block_size);
+    x.kv_layout = pg->kv_layout;
+  }
   x.out = out;
   x.lse = lse;
   x.status = reinterpret_cast<uint32_t*>(wsb);
@@ -692,6 +712,29 @@ fa_status fa_forward_varlen_ex(const void* q, const void* k, const void* v,
                              scale, out, lse, workspace, workspace_bytes, stream);
 }
 
+fa_status fa_forward_paged(const void* q, const void* k_cache, const void* v_cache, int kv_layout,
+                           const int32_t* block_table, int64_t max_blocks_per_seq,
+                           int64_t num_blocks, int64_t block_size, int mask_mode,
+                           const uint8_t* key_mask, const int64_t* lens, int64_t B, int64_t S_q,
+                           int64_t S_kv, int64_t num_heads, int64_t num_kv_heads, int64_t D,
+                           float scale, int layout, void* out, float* lse, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (block_table == nullptr && B > 0) return FA_ERR_NULLPTR;
+  if (kv_layout != FA_LAYOUT_PA_BBND && kv_layout != FA_LAYOUT_PA_BNBD) return FA_ERR_PARAM_INVALID;
+  if (block_size < 16 || block_size > 1024 || block_size % 16 != 0 || max_blocks_per_seq < 0 ||
+      num_blocks < 0 || max_blocks_per_seq > kMaxDim / 1024 || num_blocks > kMaxDim)
+    return FA_ERR_PARAM_INVALID;
+  // the table covers every key row of a sequence
+  if (S_kv > 0 && max_blocks_per_seq * block_size < S_kv) return FA_ERR_PARAM_INVALID;
+  const bool mask_ok = mask_mode == FA_MASK_NONE || mask_mode == FA_MASK_CAUSAL;
+  const bool causal = mask_mode == FA_MASK_CAUSAL;
+  const PagedKv pg{block_table, std::max<int64_t>(max_blocks_per_seq, 1),
+                   std::max<int64_t>(num_blocks, 1), block_size, kv_layout};
+  return forward_impl(q, k_cache, v_cache, mask_ok, -1, causal ? 0 : -1, key_mask, lens, B, S_q,
+                      S_kv, num_heads, num_kv_heads, D, scale, layout, out, lse, workspace,
+                      workspace_bytes, stream, nullptr, nullptr, nullptr, nullptr, &pg);
+}
+
 fa_status fa_forward_window(const void* q, const void* k, const void* v, int64_t win_left,
                             int64_t win_right, const uint8_t* key_mask, const int64_t* lens,
                             int64_t B, int64_t S_q, int64_t S_kv, int64_t num_heads,
@@ -703,12 +746,6 @@ fa_status fa_forward_window(const void* q, const void* k, const void* v, int64_t
 }
 
 namespace {
-
-// A paged K/V cache (fa_decode_paged); null for a contiguous one.
-struct PagedKv {
-  const int32_t* block_table;
-  int64_t max_blocks, num_blocks, block_size;
-};
 
 // scratch: when given, the workspace is not the caller's but the one this
 // function returns (the library-owned array of fa_decode_noalloc, looked up

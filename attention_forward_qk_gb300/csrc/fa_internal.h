@@ -147,6 +147,11 @@ struct PrefillLaunch {
   // B = 1 in the tile maps), S_q / S_kv the longest span and lse [T_q, Hq]
   const int32_t* varlen;
   long long T_q, T_kv;        // packed rows of q and k/v (packed sequences only)
+  // paged K/V (block_table != null): k, v are pools of num_blocks blocks of
+  // block_size rows in kv_layout (FA_LAYOUT_PA_BBND or FA_LAYOUT_PA_BNBD);
+  // row r of batch b lives in block block_table[b * max_blocks + r / block_size]
+  const int32_t* block_table = nullptr;
+  int max_blocks = 0, num_blocks = 0, block_size = 0, kv_layout = 0;
   int grid;                   // persistent CTAs
   void* out;
   float* lse;

@@ -37,6 +37,8 @@
 #include <math.h>
 
 #include <algorithm>
+#include <numeric>
+#include <type_traits>
 
 #include "fa_internal.h"
 #include "fa_ptx.cuh"
@@ -101,6 +103,19 @@ struct PrefillArgs {
   long long T_q;  // packed query rows (index checks only)
 #endif
 };
+
+// Paged K/V (prefill_kernel<D, Pages>): k and v are pools of blocks of
+// block_size rows; row r of batch b lives in block
+// block_table[b * max_blocks + r / block_size] at row r % block_size; a KV
+// tile is loaded as boxes of box_rows rows (a divisor of block_size), each
+// inside one block. A kernel parameter of its own (an empty one for a
+// contiguous cache), so that the contiguous instantiations' parameters and
+// code stay as they are.
+struct Pages {
+  const int32_t* block_table;
+  int max_blocks, block_size, box_rows;
+};
+struct NoPages {};
 
 // Barrier slots (8 bytes each) after the tiles.
 enum : int {
@@ -215,10 +230,11 @@ __device__ __forceinline__ WorkItem<D> work_item(const PrefillArgs& a, int w) {
   return it;
 }
 
-template <int D>
+template <int D, class PG = NoPages>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
+                   const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a, const PG pgs) {
+  constexpr bool kPaged = std::is_same_v<PG, Pages>;
   using C = PCfg<D>;
   constexpr int kBN = C::BN;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -278,6 +294,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
     }
+    // paged K/V: KV tile j of batch b, box by box (every box inside one
+    // block; the rows of a box past the table's last block, which lie past
+    // every key, come from that last block and are masked)
+    auto load_paged_tile = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar_addr, int b,
+                               int j, int kvh) {
+      if constexpr (kPaged) {
+        const int32_t* bt = pgs.block_table + static_cast<size_t>(b) * pgs.max_blocks;
+        for (int r = 0; r < kBN; r += pgs.box_rows) {
+          const int row = j * kBN + r;
+          const int blk = __ldg(bt + min(row / pgs.block_size, pgs.max_blocks - 1));
+          for (int s = 0; s < D / 64; ++s)
+            tma_load_4d(dst + s * C::kKvSub + r * 128, map, bar_addr, s * 64,
+                        row % pgs.block_size, kvh, blk);
+        }
+      }
+    };
     int item = 0;  // ring items issued so far (K_j and V_j are one item each)
     int fixes = 0;
     int q_loads = 0;  // work items whose Q tiles were requested
@@ -333,9 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // land V on the side barrier, zero the rows of excluded keys, publish
           if (lane == 0) {
             mbar_expect_tx(bar(kBarFix), C::kKvTileBytes);
-            for (int s = 0; s < D / 64; ++s)
-              tma_load_4d(dst + s * C::kKvSub, map, bar(kBarFix), s * 64,
-                          wi.kv_base + j * kBN, kvh, wi.tma_b);
+            if constexpr (kPaged) {
+              load_paged_tile(dst, map, bar(kBarFix), wi.b, j, kvh);
+            } else {
+              for (int s = 0; s < D / 64; ++s)
+                tma_load_4d(dst + s * C::kKvSub, map, bar(kBarFix), s * 64,
+                            wi.kv_base + j * kBN, kvh, wi.tma_b);
+            }
           }
           ++item;
           ok = mbar_wait(bar(kBarFix), fixes & 1, a.timeout_ns, a.status, kDevTimeoutKvFull,
@@ -361,9 +397,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           if (lane == 0) {
             mbar_expect_tx(bar(kBarKvFull + slot), C::kKvTileBytes);
-            for (int s = 0; s < D / 64; ++s)
-              tma_load_4d(dst + s * C::kKvSub, map, bar(kBarKvFull + slot), s * 64,
-                          wi.kv_base + j * kBN, kvh, wi.tma_b);
+            if constexpr (kPaged) {
+              load_paged_tile(dst, map, bar(kBarKvFull + slot), wi.b, j, kvh);
+            } else {
+              for (int s = 0; s < D / 64; ++s)
+                tma_load_4d(dst + s * C::kKvSub, map, bar(kBarKvFull + slot), s * 64,
+                            wi.kv_base + j * kBN, kvh, wi.tma_b);
+            }
           }
           ++item;
         }
@@ -961,25 +1001,38 @@ template <int D>
 cudaError_t launch_prefill_d(const PrefillLaunch& x, cudaStream_t stream) {
   using C = PCfg<D>;
   constexpr int kBN = C::BN;
-  static std::atomic<uint64_t> configured{0};  // devices with the attribute set
+  static std::atomic<uint64_t> configured{0};  // devices with the attributes set
   if (setup_needed(configured)) {
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(prefill_kernel<D, Pages>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     setup_done(configured);
   }
   CUtensorMap mq, mk, mv;
   // packed sequences: [T, H, D] tensors, one batch of T rows
   const bool packed = x.varlen != nullptr;
+  const bool paged = x.block_table != nullptr;
   const int64_t map_B = packed ? 1 : x.B;
   const int64_t S_q_map = packed ? std::max<int64_t>(x.T_q, 1) : x.S_q;
   const int64_t S_kv_map = packed ? std::max<int64_t>(x.T_kv, 1) : (x.S_kv > 0 ? x.S_kv : 1);
+  // a paged cache is a batch of num_blocks sequences of block_size rows
+  // (PA_BBND rows as BSND, PA_BNBD as BNSD), loaded in boxes of
+  // gcd(block_size, kBN) rows: each box lies inside one block
+  const int box_rows = paged ? std::gcd(x.block_size, kBN) : kBN;
+  const int kv_layout = !paged ? x.layout
+                        : x.kv_layout == FA_LAYOUT_PA_BBND ? FA_LAYOUT_BSND
+                                                           : FA_LAYOUT_BNSD;
+  const int64_t kv_B = paged ? x.num_blocks : map_B;
+  const int64_t kv_S = paged ? x.block_size : S_kv_map;
   if (!encode_bf16_map(&mq, x.q, x.layout, map_B, x.Hq, S_q_map, D, 64, kBM,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_bf16_map(&mk, x.k, x.layout, map_B, x.Hkv, S_kv_map, D, 64, kBN,
+      !encode_bf16_map(&mk, x.k, kv_layout, kv_B, x.Hkv, kv_S, D, 64, box_rows,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_bf16_map(&mv, x.v, x.layout, map_B, x.Hkv, S_kv_map, D, 64, kBN,
+      !encode_bf16_map(&mv, x.v, kv_layout, kv_B, x.Hkv, kv_S, D, 64, box_rows,
                        CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   PrefillArgs pa;
@@ -1015,7 +1068,11 @@ cudaError_t launch_prefill_d(const PrefillLaunch& x, cudaStream_t stream) {
 #endif
   // persistent: one CTA per SM (each CTA holds all 512 TMEM columns)
   const int grid = x.grid;  // the schedule in the workspace was built for this grid
-  prefill_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, pa);
+  if (paged)
+    prefill_kernel<D, Pages><<<grid, kThreads, C::kSmemBytes, stream>>>(
+        mq, mk, mv, pa, Pages{x.block_table, x.max_blocks, x.block_size, box_rows});
+  else
+    prefill_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, pa, NoPages{});
   return cudaGetLastError();
 }
 

@@ -142,6 +142,59 @@ def fa_forward(q, k, v, *, mask_mode=None, key_mask=None, actual_seq_lengths=Non
     return out, lse
 
 
+def fa_forward_paged(q, k_cache, v_cache, block_table, block_size, S_kv, *, kv_layout="PA_BBND",
+                     mask_mode=None, key_mask=None, actual_seq_lengths=None, scale=1.0,
+                     layout="BNSD", num_heads=None, num_kv_heads=None, out=None, lse=None,
+                     return_lse=True, workspace=None, stream=None):
+    """Prefill attention with K and V in a paged cache: k_cache/v_cache
+    [num_blocks, block_size, KV_N, D] (PA_BBND) or [num_blocks, KV_N,
+    block_size, D] (PA_BNBD); block_table int32 [B, max_blocks_per_seq] on the
+    device; S_kv the keys of each sequence. q and out in `layout`. Returns
+    (out, lse)."""
+    kvl = {"PA_BBND": _lib.FA_LAYOUT_PA_BBND, "PA_BNBD": _lib.FA_LAYOUT_PA_BNBD}.get(kv_layout)
+    if kvl is None:
+        raise ValueError("kv_layout must be PA_BBND or PA_BNBD")
+    lid = _layout_id(layout)
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check_tensor(t, n)
+    if block_table.dtype != torch.int32 or not block_table.is_contiguous() or block_table.dim() != 2:
+        raise ValueError("block_table must be a contiguous int32 [B, max_blocks_per_seq] tensor")
+    B, Hq, S_q, D = _dims(q, lid)
+    if kvl == _lib.FA_LAYOUT_PA_BBND:
+        nblk, bs, Hkv, Dk = k_cache.shape
+    else:
+        nblk, Hkv, bs, Dk = k_cache.shape
+    if bs != block_size or Dk != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache, v_cache, block_size or D disagree")
+    if block_table.shape[0] != B:
+        raise ValueError("block_table must have B rows")
+    if num_heads is not None and num_heads != Hq:
+        raise ValueError("num_heads does not match q")
+    if num_kv_heads not in (None, 0) and num_kv_heads != Hkv:
+        raise ValueError("num_kv_heads does not match k_cache")
+    if out is None:
+        out = torch.empty_like(q)
+    _check_tensor(out, "out")
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, S_q), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_tensor(lse, "lse", torch.float32)
+    if key_mask is not None:
+        _check_tensor(key_mask, "key_mask", torch.uint8)
+    need = fa_forward_workspace_size(B, S_q, S_kv, Hq, Hkv, D)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    lens_arr, _ = _lens_array(actual_seq_lengths, B)
+    st = _lib.load().fa_forward_paged(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), kvl, block_table.data_ptr(),
+        block_table.shape[1], nblk, block_size, MASK_MODES.get(mask_mode, mask_mode),
+        key_mask.data_ptr() if key_mask is not None else None, lens_arr, B, S_q, int(S_kv), Hq,
+        Hkv, D, float(scale), lid, out.data_ptr(), lse.data_ptr() if lse is not None else None,
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    check(st, "fa_forward_paged")
+    return out, lse
+
+
 def fa_forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_kv, *, mask_mode=None, scale=1.0,
                       num_heads=None, num_kv_heads=None, out=None, lse=None, return_lse=True,
                       workspace=None, stream=None):

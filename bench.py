@@ -50,8 +50,8 @@ MAIN_KERNEL = {"decode": "decode_kernel", "prefill": "prefill_kernel"}
 CONFIGS = {"C1": "tiny_prefill", "C2": "gqa_decode", "C3": "long_decode",
            "C4": "causal_prefill", "C5": "gqa_masked_prefill"}
 OTHER_WORKLOADS = ("long_decode", "causal_prefill", "gqa_masked_prefill", "tiny_prefill",
-                   "window_prefill", "varlen_prefill", "d256_prefill", "paged_decode",
-                   "d256_decode", "batch_decode", "gqa_decode")
+                   "window_prefill", "varlen_prefill", "d256_prefill", "paged_prefill",
+                   "paged_decode", "d256_decode", "batch_decode", "gqa_decode")
 # a forced split count (num_splits > 0) runs split_kernel instead of decode_kernel
 SPLIT_KERNEL = "split_kernel"
 KERNEL_SOURCE = {"decode_kernel": "attention_forward_qk_gb300/csrc/fa_decode.cu",
@@ -282,6 +282,11 @@ class Runner:
             F.fa_forward_varlen(self.q, self.k, self.v, self.cu, self.cu,
                                 mask_mode="causal" if w.causal else None, scale=w.scale,
                                 out=self.out, lse=self.lse, workspace=self.ws)
+        elif self.table is not None and self.kind == "prefill":
+            F.fa_forward_paged(self.q, self.k, self.v, self.table, w.block_size, w.S_kv,
+                               kv_layout="PA_BBND", mask_mode="causal" if w.causal else None,
+                               key_mask=self.km, scale=w.scale, layout=w.layout, out=self.out,
+                               lse=self.lse, workspace=self.ws)
         elif self.kind == "decode" and self.table is not None:
             F.fa_decode_paged(self.q, self.k, self.v, self.table, w.block_size, self.lens,
                               scale=w.scale, num_splits=self.splits, out=self.out, lse=self.lse,

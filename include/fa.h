@@ -79,7 +79,7 @@ typedef enum {
 typedef enum {
   FA_LAYOUT_BNSD = 0,
   FA_LAYOUT_BSND = 1,
-  /* paged K/V caches (FlashAttn guide §1.2, layout_kv), fa_decode_paged only */
+  /* paged K/V caches (FlashAttn guide §1.2, layout_kv): fa_decode_paged, fa_forward_paged */
   FA_LAYOUT_PA_BBND = 2, /* [num_blocks, block_size, KV_N, D]: rows of a block as BSND */
   FA_LAYOUT_PA_BNBD = 3  /* [num_blocks, KV_N, block_size, D]: rows of a block as BNSD */
 } fa_layout;
@@ -120,6 +120,36 @@ fa_status fa_forward(const void* q, const void* k, const void* v, int mask_mode,
                      int64_t S_q, int64_t S_kv, int64_t num_heads, int64_t num_kv_heads,
                      int64_t D, float scale, int layout, void* out, float* lse,
                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* fa_forward with K and V in a paged cache (FlashAttn guide §1.2: layout_kv
+ * PA_BBND / PA_BNBD, usable with the q layouts BSND and BNSD): blocks of
+ * block_size key rows in a pool, and a block table per sequence.
+ *   k_cache, v_cache  device bf16 pools, kv_layout FA_LAYOUT_PA_BBND
+ *                     [num_blocks, block_size, num_kv_heads, D] or
+ *                     FA_LAYOUT_PA_BNBD [num_blocks, num_kv_heads, block_size, D]
+ *   block_table       device int32 [B, max_blocks_per_seq]: key row r of
+ *                     sequence b is row r % block_size of block
+ *                     block_table[b * max_blocks_per_seq + r / block_size]
+ *   block_size        a multiple of 16 in [16, 1024]
+ *   max_blocks_per_seq  * block_size >= S_kv (the table covers every key row)
+ *   S_kv              the keys of each sequence (its logical length); the
+ *                     other arguments (q and out in `layout`, mask_mode,
+ *                     key_mask [B, S_kv], actual_seq_lengths, lse, the
+ *                     workspace of fa_forward_workspace_size) as in fa_forward
+ * Entries of a table past the blocks a sequence's keys use may hold any value:
+ * a KV tile that reaches past the last key may load rows through them (an id
+ * outside [0, num_blocks) loads zeros), and those keys are excluded before
+ * any product, with their V rows zeroed.
+ * Errors: block_table NULL with B > 0 -> FA_ERR_NULLPTR; an unknown
+ * kv_layout, a bad block_size or a table too short for S_kv ->
+ * FA_ERR_PARAM_INVALID; otherwise those of fa_forward. */
+fa_status fa_forward_paged(const void* q, const void* k_cache, const void* v_cache, int kv_layout,
+                           const int32_t* block_table, int64_t max_blocks_per_seq,
+                           int64_t num_blocks, int64_t block_size, int mask_mode,
+                           const uint8_t* key_mask, const int64_t* actual_seq_lengths, int64_t B,
+                           int64_t S_q, int64_t S_kv, int64_t num_heads, int64_t num_kv_heads,
+                           int64_t D, float scale, int layout, void* out, float* lse,
+                           void* workspace, size_t workspace_bytes, void* stream);
 
 /* Fused attention forward over packed variable-length sequences (the TND
  * layout of FlashAttn guide §1.3 and §1.4: the tokens of all sequences laid

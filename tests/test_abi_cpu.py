@@ -353,6 +353,47 @@ def test_decode_paged_zero_batch_is_noop(lib):
     assert _dec_paged(lib, B=0, lens=[], bt=None) == _lib.FA_OK
 
 
+def _fwd_paged(lib, **kw):
+    args = dict(q=P, k=P, v=P, kvl=2, bt=P, maxb=4, nblk=16, bs=64, mask=0, key_mask=None,
+                lens=None, B=2, S_q=256, S_kv=256, Hq=8, Hkv=2, D=128, scale=0.1, layout=0,
+                out=P, lse=None, ws=WS, ws_bytes=1 << 22, stream=None)
+    args.update(kw)
+    lens = args["lens"]
+    if lens is not None:
+        lens = (ctypes.c_int64 * max(len(lens), 1))(*lens)
+    return lib.fa_forward_paged(args["q"], args["k"], args["v"], args["kvl"], args["bt"],
+                                args["maxb"], args["nblk"], args["bs"], args["mask"],
+                                args["key_mask"], lens, args["B"], args["S_q"], args["S_kv"],
+                                args["Hq"], args["Hkv"], args["D"], args["scale"], args["layout"],
+                                args["out"], args["lse"], args["ws"], args["ws_bytes"],
+                                args["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(bt=None), _lib.FA_ERR_NULLPTR),
+    (dict(k=None), _lib.FA_ERR_NULLPTR),
+    (dict(kvl=0), _lib.FA_ERR_PARAM_INVALID),     # a contiguous layout is not a paged one
+    (dict(kvl=7), _lib.FA_ERR_PARAM_INVALID),
+    (dict(layout=2), _lib.FA_ERR_PARAM_INVALID),  # q itself is not paged
+    (dict(bs=8), _lib.FA_ERR_PARAM_INVALID),      # below 16
+    (dict(bs=40), _lib.FA_ERR_PARAM_INVALID),     # not a multiple of 16
+    (dict(bs=2048), _lib.FA_ERR_PARAM_INVALID),   # above 1024
+    (dict(maxb=3), _lib.FA_ERR_PARAM_INVALID),    # 3 x 64 rows < S_kv = 256
+    (dict(maxb=-1), _lib.FA_ERR_PARAM_INVALID),
+    (dict(mask=3, S_q=128), _lib.FA_ERR_PARAM_INVALID),  # causal needs S_q == S_kv
+    (dict(mask=4), _lib.FA_ERR_PARAM_INVALID),    # the window has its own entry points
+    (dict(lens=[300, 1]), _lib.FA_ERR_PARAM_INVALID),  # past S_kv
+    (dict(D=96), _lib.FA_ERR_UNSUPPORTED),
+    (dict(ws_bytes=16), _lib.FA_ERR_WORKSPACE_TOO_SMALL),
+])
+def test_forward_paged_rejects_before_any_cuda_call(lib, kw, expect):
+    assert _fwd_paged(lib, **kw) == expect
+
+
+def test_forward_paged_zero_batch_is_noop(lib):
+    assert _fwd_paged(lib, B=0, bt=None) == _lib.FA_OK
+
+
 def _fwd_varlen(lib, cq, ckv, **kw):
     args = dict(q=P, k=P, v=P, mask=0, Hq=4, Hkv=2, D=128, scale=0.1, out=P, lse=None, ws=WS,
                 ws_bytes=1 << 22, stream=None)

@@ -57,7 +57,7 @@ class Workload:
     max_pad: int | None = None
     # prefill: sliding window (win_left, win_right), -1 = no limit on that side
     window: tuple | None = None
-    # decode: paged cache of blocks of this many rows (PA_BBND), or None
+    # paged K/V cache of blocks of this many rows (PA_BBND, shuffled), or None
     block_size: int | None = None
     # prefill: B packed sequences (TND) of lengths drawn uniform in
     # [len_lo, len_hi] (equal q and kv lengths), S_q = S_kv = len_hi
@@ -109,6 +109,14 @@ WORKLOADS: dict[str, Workload] = {
         "varlen_prefill", "prefill", B=16, Hq=32, Hkv=8, S_q=8192, S_kv=8192, D=128,
         layout="TND", causal=True, seed=108, len_lo=512, len_hi=8192, packed=True,
         note="16 packed sequences (TND), lengths ~U[512,8192], Hq=32 Hkv=8 D=128, causal"),
+    # Beyond the five: the causal prefill workload with its K/V in a paged
+    # cache (FlashAttn guide §1.2, layout_kv PA_BBND beside q in BSND; 128-row
+    # blocks in shuffled order).
+    "paged_prefill": Workload(
+        "paged_prefill", "prefill", B=4, Hq=32, Hkv=32, S_q=4096, S_kv=4096, D=128,
+        layout="BSND", causal=True, seed=112, block_size=128,
+        note="B=4 H=32 S=4096 D=128 causal, q BSND, K/V paged (PA_BBND, 128-row blocks, "
+             "shuffled)"),
     # Beyond the five: the GQA decode workload with head dim 256 (FlashAttn
     # guide §3 tiling for D = 256).
     "d256_decode": Workload(
