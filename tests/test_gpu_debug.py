@@ -3,7 +3,8 @@ device-side index checks, which record FA_ERR_DEVICE_CHECK in the workspace
 status word and skip the access instead of trapping. On valid inputs no check
 may fire and the results must match the oracle as the release build's do:
 prefill (padded causal with a key mask, D=256, packed sequences with seqused
-and a key mask) and decode (split sequences, forced splits, paged)."""
+and a key mask, a paged cache) and decode (split sequences, forced splits,
+paged)."""
 import math
 
 import numpy as np
@@ -43,6 +44,23 @@ def test_debug_prefill_checks_pass_and_match(debug_build):
         ro, rl = oracle.attention(x["q"], x["k"], x["v"], scale=1 / math.sqrt(D), causal=True,
                                   key_mask=x["key_mask"])
         compare(out, lse, ro, rl, "BNSD")
+
+
+def test_debug_paged_prefill_checks_pass_and_match(debug_build):
+    from test_gpu_paged_prefill import _case
+    B, Hq, Hkv, S, D, bs = 2, 8, 2, 300, 128, 48
+    q, k, v, kp, vp, table = _case(B, Hq, Hkv, S, S, D, bs, "PA_BNBD", seed=63, lens=[300, 211],
+                                   table_fill="other")
+    ws = torch.empty(F.fa_forward_workspace_size(B, S, S, Hq, Hkv, D), dtype=torch.uint8,
+                     device="cuda")
+    out, lse = F.fa_forward_paged(q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), bs, S,
+                                  kv_layout="PA_BNBD", mask_mode="causal",
+                                  actual_seq_lengths=[300, 211], scale=1 / math.sqrt(D),
+                                  workspace=ws)
+    assert F.fa_workspace_status(ws) == _lib.FA_OK
+    ro, rl = oracle.attention(q, k, v, scale=1 / math.sqrt(D), causal=True,
+                              actual_seq_lengths=[300, 211])
+    compare(out, lse, ro, rl, "BNSD")
 
 
 def test_debug_packed_prefill_checks_pass_and_match(debug_build):
