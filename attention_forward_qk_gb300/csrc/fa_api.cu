@@ -360,10 +360,13 @@ fa_status decode_plan_impl(int64_t B, int64_t S_kv_max, int64_t num_heads, int64
   const int64_t g = num_heads / num_kv_heads;
   const int64_t KH = num_kv_heads * (g / decode_heads_per_cta(g, D));
   const int64_t total = KH * sum;
-  // With more (non-empty) units than SMs a share holds several unit starts,
-  // each a piece end to pay for: the shares are then cut by cost, where a row
-  // costs 1 and every unit after the first adds pc (FlashAttn guide §4: split
-  // the work into sections of equal cost). Forced splits cut rows.
+  // A share holding a unit start pays a piece end: the shares are cut by
+  // cost, where a row costs 1 and every unit after the first adds pc
+  // (FlashAttn guide §4: split the work into sections of equal cost), when
+  // the (non-empty) units outnumber the SMs (a share then holds several unit
+  // starts), and when a CTA carries four or more query heads (whose piece
+  // end, with its warps' park and combine of every head, costs the most;
+  // charged as more rows). Forced splits cut rows.
   int64_t units = 0, last_unit = -1;
   for (int64_t b = 0; b < B; ++b)
     if (lens[b] > 0) {
@@ -371,8 +374,12 @@ fa_status decode_plan_impl(int64_t B, int64_t S_kv_max, int64_t num_heads, int64
       last_unit = b * KH + KH - 1;
     }
   int64_t pc = 0;
-  if (num_splits == 0 && units > num_sms)
-    pc = std::max<int64_t>(kDecodePieceCostRows128 * 128 / D / rc_align, 1) * rc_align;
+  if (num_splits == 0 && units > 1) {
+    const int64_t rows128 = units > num_sms                           ? kDecodePieceCostRows128
+                            : decode_heads_per_cta(g, D) >= 4 ? kDecodePieceCostRows128Heads
+                                                              : 0;
+    if (rows128 > 0) pc = std::max<int64_t>(rows128 * 128 / D / rc_align, 1) * rc_align;
+  }
   const int64_t cost = total + pc * std::max<int64_t>(last_unit, 0);
   int64_t rc;
   if (num_splits > 0) {

@@ -307,162 +307,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   }
   __syncthreads();
 
-  if (warp == kDecWarps) {
-    // ================================================================ producer
-    // The shares are equal in cost: a row costs 1 and, when piece_cost > 0,
-    // the start of every unit after the first costs piece_cost more (the
-    // piece end it brings), so that a share holding unit starts takes fewer
-    // rows. Row x of unit k costs x + piece_cost * k; CTA c holds the rows of
-    // cost [c Rc, (c+1) Rc).
-    const long long Rc = a.rows_per_cta;
-    constexpr bool kWeighted = kShares == kSharesCost;
-    const long long pc = kWeighted ? a.piece_cost : 0;
-    // the first row whose cost is at least T
-    auto row_at_cost = [&](long long T) -> long long {
-      const int b = find_batch(a.prefix, a.B, KH, pc, T);
-      const long long L = a.prefix[b + 1] - a.prefix[b];
-      const long long cb = KH * (a.prefix[b] + pc * b);  // cost of the batch's first row
-      const long long kh = min(KH - 1, div_nn(T - cb, L + pc));  // L + pc > 0 here
-      const long long off = T - cb - kh * (L + pc);
-      const long long u0 = KH * a.prefix[b] + kh * L;
-      return off < L ? u0 + off : u0 + L;  // in the gap before the next unit: its first row
-    };
-    const long long T0 = static_cast<long long>(blockIdx.x) * Rc;
-    long long r = T0;
-    long long r1 = min(T0 + Rc, a.total);
-    long long v = blockIdx.x;  // the share being planned
-    if constexpr (kWeighted) {
-      if (a.share_off >= 0) {
-        r = a.prefix.local[a.share_off + blockIdx.x];
-        r1 = a.prefix.local[a.share_off + blockIdx.x + 1];
-      } else {
-        if (T0 > 0) r = row_at_cost(T0);
-        r1 = blockIdx.x + 1 == gridDim.x ? a.total : min(row_at_cost(T0 + Rc), a.total);
-      }
-    }
-    // the next piece of this CTA's range [r, r1): its unit, rows and stages
-    auto plan = [&](int piece, SlotHeader& h, int& kvh, int& hg) {
-      h = SlotHeader{-1, 0, 1, 0, 0, 0, 0, 0, 0, 0};
-      if (r >= r1) return;
-      const int b = find_batch(a.prefix, a.B, KH, 0, r);
-      const long long base = KH * a.prefix[b];
-      const long long L = a.prefix[b + 1] - a.prefix[b];
-      const long long kh = div_nn(r - base, L);
-      const long long u0 = base + kh * L;  // the unit's first row in the work space
-      const long long u1 = u0 + L;
-      const long long rows = min(u1, r1) - r;
-      h.piece = piece;
-      h.b = b;
-      h.kh = static_cast<int>(kh);
-      h.row0 = static_cast<int>(r - u0);
-      h.rows = static_cast<int>(rows);
-      const long long cu = kWeighted ? u0 + pc * (b * KH + kh) : u0;  // cost of its first row
-      const long long c0 = div_nn(cu, Rc);  // the CTA holding the unit's first row
-      h.slot = static_cast<int>(v - c0);
-      h.nsp = static_cast<int>(div_nn(cu + L - 1, Rc) - c0 + 1);
-      h.nstage = static_cast<int>((rows + C::R - 1) / C::R);
-      h.vend = h.rows;
-      if (a.block_table != nullptr) {
-        const long long real = a.real_len != nullptr ? __ldg(a.real_len + b) : L - a.pad16[b];
-        h.vend = static_cast<int>(max(0ll, min(static_cast<long long>(h.rows), real - h.row0)));
-      }
-      kvh = h.kh / a.head_groups;
-      hg = h.kh % a.head_groups;
-      r += rows;
-      if (!FA_CHECK(b >= 0 && b < a.B && kh >= 0 && kh < KH && h.row0 >= 0 && rows > 0 &&
-                        h.row0 + rows <= L && h.slot >= 0 && h.slot < h.nsp,
-                    a.status, kDevCheckDecodePiece))
-        h.piece = -1;  // stop: nothing of this piece is loaded
-    };
-    SlotHeader h{};
-    int kvh = 0, hg = 0;
-    // the first piece needs only the launch parameters (unless the prefix
-    // sums or the paged lengths sit in the workspace): plan it while the
-    // work before this kernel may still be running
-    const bool early = a.prefix.global == nullptr && a.real_len == nullptr;
-    if (lane == 0) {
-      tma_prefetch_map(&tm_k);
-      tma_prefetch_map(&tm_v);
-      tma_prefetch_map(&tm_k16);
-      tma_prefetch_map(&tm_v16);
-      if (early) plan(0, h, kvh, hg);
-    }
-    // launched with programmatic dependent launch: wait until the work that
-    // precedes this kernel on the stream (which may produce q, K, V) is done
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (lane == 0) {
-      int st = 0;  // stages issued by this CTA
-      bool ok = true;
-      for (int piece = 0; ok; ++piece) {
-        if (piece > 0 || !early) plan(piece, h, kvh, hg);
-        const bool done = h.piece < 0;
-        for (int s = 0; s < h.nstage; ++s, ++st) {
-          const int slot = st % NST;
-          const int use = st / NST;
-          if (use > 0 && !mbar_wait_polled(empty0 + 8 * slot, (use - 1) & 1, a.timeout_ns, a.status,
-                                    kDevTimeoutDecodeEmpty, abort_flag)) {
-            ok = false;
-            break;
-          }
-          h.stage = s;
-          hdr[slot] = h;
-          if (done) {
-            mbar_arrive(full0 + 8 * slot);  // end marker: no data
-            ok = false;
-            ++st;
-            break;
-          }
-          const uint32_t dst = smem_u32(smem + slot * C::STAGE_BYTES);
-          const int row = h.row0 + s * C::R;
-          const int rows_here = min(C::R, h.rows - s * C::R);
-          const uint32_t q_bytes = s == 0 ? G * D * 2 : 0;
-          if (a.block_table != nullptr) {
-            // paged: 16-row boxes (pieces and lengths are multiples of 16 rows in
-            // the work space, blocks are multiples of 16 rows), each from its block
-            const int nb = (rows_here + C::TAIL - 1) / C::TAIL;
-            mbar_expect_tx(full0 + 8 * slot, 2 * nb * C::TAIL * D * 2 + q_bytes);
-            const int32_t* bt = a.block_table + static_cast<size_t>(h.b) * a.max_blocks;
-            for (int t = 0; t < nb; ++t) {
-              const int lr = row + t * C::TAIL;
-              const int blk = __ldg(bt + lr / a.block_size);
-              const int in_blk = lr % a.block_size;
-              tma_load_4d(dst + t * C::TAIL * D * 2, &tm_k16, full0 + 8 * slot, 0, in_blk, kvh,
-                          blk);
-              tma_load_4d(dst + C::TILE_BYTES + t * C::TAIL * D * 2, &tm_v16, full0 + 8 * slot,
-                          0, in_blk, kvh, blk);
-            }
-          } else if (rows_here == C::R) {
-            mbar_expect_tx(full0 + 8 * slot, C::STAGE_BYTES + q_bytes);
-            tma_load_4d(dst, &tm_k, full0 + 8 * slot, 0, row, kvh, h.b);
-            tma_load_4d(dst + C::TILE_BYTES, &tm_v, full0 + 8 * slot, 0, row, kvh, h.b);
-          } else {
-            // partial last stage: 16-row boxes, only as many as the piece needs
-            const int nb = (rows_here + C::TAIL - 1) / C::TAIL;
-            mbar_expect_tx(full0 + 8 * slot, 2 * nb * C::TAIL * D * 2 + q_bytes);
-            for (int t = 0; t < nb; ++t) {
-              tma_load_4d(dst + t * C::TAIL * D * 2, &tm_k16, full0 + 8 * slot, 0,
-                          row + t * C::TAIL, kvh, h.b);
-              tma_load_4d(dst + C::TILE_BYTES + t * C::TAIL * D * 2, &tm_v16, full0 + 8 * slot,
-                          0, row + t * C::TAIL, kvh, h.b);
-            }
-          }
-          if (s == 0) {
-            const __nv_bfloat16* qsrc =
-                a.q + (static_cast<size_t>(h.b) * a.Hq + kvh * g_total + hg * G) * D;
-            bulk_load(smem_u32(qbuf + slot * C::QB), qsrc, q_bytes, full0 + 8 * slot);
-          }
-        }
-      }
-      if (*abort_flag) {
-        // let every copy this CTA started land before shared memory is released
-        const uint64_t drain_ns = a.timeout_ns > kDrainFloorNs ? a.timeout_ns : kDrainFloorNs;
-        for (int s = max(0, st - NST); s < st; ++s)
-          mbar_wait_polled(full0 + 8 * (s % NST), (s / NST) & 1, drain_ns, a.status,
-                    kDevTimeoutDrain, nullptr);
-      }
-    }
-  } else {
+  // The consumers' code comes first and the producer's after: a consumer's
+  // first stage runs code no warp has run yet (from L2 or HBM when the caches
+  // are cold), and this keeps that code where it is whatever the producer's
+  // planning code holds (with the producer first, the cost-cut plan's extra
+  // code before it made the first stage ≈2.5 µs slower).
+  if (warp != kDecWarps) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // (the status word was cleared on the stream before this kernel)
     // work queued after this kernel may be scheduled as soon as SMs free up
@@ -791,6 +641,161 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           else
             record_error(a.status, kDevPendingOverflow);  // the host plan prevents this
         }
+      }
+    }
+  } else {
+    // ================================================================ producer
+    // The shares are equal in cost: a row costs 1 and, when piece_cost > 0,
+    // the start of every unit after the first costs piece_cost more (the
+    // piece end it brings), so that a share holding unit starts takes fewer
+    // rows. Row x of unit k costs x + piece_cost * k; CTA c holds the rows of
+    // cost [c Rc, (c+1) Rc).
+    const long long Rc = a.rows_per_cta;
+    constexpr bool kWeighted = kShares == kSharesCost;
+    const long long pc = kWeighted ? a.piece_cost : 0;
+    // the first row whose cost is at least T
+    auto row_at_cost = [&](long long T) -> long long {
+      const int b = find_batch(a.prefix, a.B, KH, pc, T);
+      const long long L = a.prefix[b + 1] - a.prefix[b];
+      const long long cb = KH * (a.prefix[b] + pc * b);  // cost of the batch's first row
+      const long long kh = min(KH - 1, div_nn(T - cb, L + pc));  // L + pc > 0 here
+      const long long off = T - cb - kh * (L + pc);
+      const long long u0 = KH * a.prefix[b] + kh * L;
+      return off < L ? u0 + off : u0 + L;  // in the gap before the next unit: its first row
+    };
+    const long long T0 = static_cast<long long>(blockIdx.x) * Rc;
+    long long r = T0;
+    long long r1 = min(T0 + Rc, a.total);
+    long long v = blockIdx.x;  // the share being planned
+    if constexpr (kWeighted) {
+      if (a.share_off >= 0) {
+        r = a.prefix.local[a.share_off + blockIdx.x];
+        r1 = a.prefix.local[a.share_off + blockIdx.x + 1];
+      } else {
+        if (T0 > 0) r = row_at_cost(T0);
+        r1 = blockIdx.x + 1 == gridDim.x ? a.total : min(row_at_cost(T0 + Rc), a.total);
+      }
+    }
+    // the next piece of this CTA's range [r, r1): its unit, rows and stages
+    auto plan = [&](int piece, SlotHeader& h, int& kvh, int& hg) {
+      h = SlotHeader{-1, 0, 1, 0, 0, 0, 0, 0, 0, 0};
+      if (r >= r1) return;
+      const int b = find_batch(a.prefix, a.B, KH, 0, r);
+      const long long base = KH * a.prefix[b];
+      const long long L = a.prefix[b + 1] - a.prefix[b];
+      const long long kh = div_nn(r - base, L);
+      const long long u0 = base + kh * L;  // the unit's first row in the work space
+      const long long u1 = u0 + L;
+      const long long rows = min(u1, r1) - r;
+      h.piece = piece;
+      h.b = b;
+      h.kh = static_cast<int>(kh);
+      h.row0 = static_cast<int>(r - u0);
+      h.rows = static_cast<int>(rows);
+      const long long cu = kWeighted ? u0 + pc * (b * KH + kh) : u0;  // cost of its first row
+      const long long c0 = div_nn(cu, Rc);  // the CTA holding the unit's first row
+      h.slot = static_cast<int>(v - c0);
+      h.nsp = static_cast<int>(div_nn(cu + L - 1, Rc) - c0 + 1);
+      h.nstage = static_cast<int>((rows + C::R - 1) / C::R);
+      h.vend = h.rows;
+      if (a.block_table != nullptr) {
+        const long long real = a.real_len != nullptr ? __ldg(a.real_len + b) : L - a.pad16[b];
+        h.vend = static_cast<int>(max(0ll, min(static_cast<long long>(h.rows), real - h.row0)));
+      }
+      kvh = h.kh / a.head_groups;
+      hg = h.kh % a.head_groups;
+      r += rows;
+      if (!FA_CHECK(b >= 0 && b < a.B && kh >= 0 && kh < KH && h.row0 >= 0 && rows > 0 &&
+                        h.row0 + rows <= L && h.slot >= 0 && h.slot < h.nsp,
+                    a.status, kDevCheckDecodePiece))
+        h.piece = -1;  // stop: nothing of this piece is loaded
+    };
+    SlotHeader h{};
+    int kvh = 0, hg = 0;
+    // the first piece needs only the launch parameters (unless the prefix
+    // sums or the paged lengths sit in the workspace): plan it while the
+    // work before this kernel may still be running
+    const bool early = a.prefix.global == nullptr && a.real_len == nullptr;
+    if (lane == 0) {
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+      tma_prefetch_map(&tm_k16);
+      tma_prefetch_map(&tm_v16);
+      if (early) plan(0, h, kvh, hg);
+    }
+    // launched with programmatic dependent launch: wait until the work that
+    // precedes this kernel on the stream (which may produce q, K, V) is done
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (lane == 0) {
+      int st = 0;  // stages issued by this CTA
+      bool ok = true;
+      for (int piece = 0; ok; ++piece) {
+        if (piece > 0 || !early) plan(piece, h, kvh, hg);
+        const bool done = h.piece < 0;
+        for (int s = 0; s < h.nstage; ++s, ++st) {
+          const int slot = st % NST;
+          const int use = st / NST;
+          if (use > 0 && !mbar_wait_polled(empty0 + 8 * slot, (use - 1) & 1, a.timeout_ns, a.status,
+                                    kDevTimeoutDecodeEmpty, abort_flag)) {
+            ok = false;
+            break;
+          }
+          h.stage = s;
+          hdr[slot] = h;
+          if (done) {
+            mbar_arrive(full0 + 8 * slot);  // end marker: no data
+            ok = false;
+            ++st;
+            break;
+          }
+          const uint32_t dst = smem_u32(smem + slot * C::STAGE_BYTES);
+          const int row = h.row0 + s * C::R;
+          const int rows_here = min(C::R, h.rows - s * C::R);
+          const uint32_t q_bytes = s == 0 ? G * D * 2 : 0;
+          if (a.block_table != nullptr) {
+            // paged: 16-row boxes (pieces and lengths are multiples of 16 rows in
+            // the work space, blocks are multiples of 16 rows), each from its block
+            const int nb = (rows_here + C::TAIL - 1) / C::TAIL;
+            mbar_expect_tx(full0 + 8 * slot, 2 * nb * C::TAIL * D * 2 + q_bytes);
+            const int32_t* bt = a.block_table + static_cast<size_t>(h.b) * a.max_blocks;
+            for (int t = 0; t < nb; ++t) {
+              const int lr = row + t * C::TAIL;
+              const int blk = __ldg(bt + lr / a.block_size);
+              const int in_blk = lr % a.block_size;
+              tma_load_4d(dst + t * C::TAIL * D * 2, &tm_k16, full0 + 8 * slot, 0, in_blk, kvh,
+                          blk);
+              tma_load_4d(dst + C::TILE_BYTES + t * C::TAIL * D * 2, &tm_v16, full0 + 8 * slot,
+                          0, in_blk, kvh, blk);
+            }
+          } else if (rows_here == C::R) {
+            mbar_expect_tx(full0 + 8 * slot, C::STAGE_BYTES + q_bytes);
+            tma_load_4d(dst, &tm_k, full0 + 8 * slot, 0, row, kvh, h.b);
+            tma_load_4d(dst + C::TILE_BYTES, &tm_v, full0 + 8 * slot, 0, row, kvh, h.b);
+          } else {
+            // partial last stage: 16-row boxes, only as many as the piece needs
+            const int nb = (rows_here + C::TAIL - 1) / C::TAIL;
+            mbar_expect_tx(full0 + 8 * slot, 2 * nb * C::TAIL * D * 2 + q_bytes);
+            for (int t = 0; t < nb; ++t) {
+              tma_load_4d(dst + t * C::TAIL * D * 2, &tm_k16, full0 + 8 * slot, 0,
+                          row + t * C::TAIL, kvh, h.b);
+              tma_load_4d(dst + C::TILE_BYTES + t * C::TAIL * D * 2, &tm_v16, full0 + 8 * slot,
+                          0, row + t * C::TAIL, kvh, h.b);
+            }
+          }
+          if (s == 0) {
+            const __nv_bfloat16* qsrc =
+                a.q + (static_cast<size_t>(h.b) * a.Hq + kvh * g_total + hg * G) * D;
+            bulk_load(smem_u32(qbuf + slot * C::QB), qsrc, q_bytes, full0 + 8 * slot);
+          }
+        }
+      }
+      if (*abort_flag) {
+        // let every copy this CTA started land before shared memory is released
+        const uint64_t drain_ns = a.timeout_ns > kDrainFloorNs ? a.timeout_ns : kDrainFloorNs;
+        for (int s = max(0, st - NST); s < st; ++s)
+          mbar_wait_polled(full0 + 8 * (s % NST), (s / NST) & 1, drain_ns, a.status,
+                    kDevTimeoutDrain, nullptr);
       }
     }
   }

@@ -57,9 +57,11 @@ constexpr int kDecodeMergeGroup = 32;
 constexpr int kDecodeMinRowsPerCta = 224;
 // Cost of a piece end (the warps' park and combine, a partial stage, the
 // partial write) in K/V rows of D = 128 (scaled by 128 / D), charged when the
-// shares are cut by cost instead of by rows: only when there are more units
-// than SMs, so that a share holds several unit starts.
+// shares are cut by cost instead of by rows: when there are more units than
+// SMs, so that a share holds several unit starts, and (the second figure)
+// when there are fewer but a CTA carries four or more query heads.
 constexpr int kDecodePieceCostRows128 = 192;
+constexpr int kDecodePieceCostRows128Heads = 384;
 
 // Error codes written to the device status word (first one wins).
 enum DeviceError : uint32_t {

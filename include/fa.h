@@ -325,11 +325,13 @@ fa_status fa_decode_paged(const void* q, const void* k_cache, const void* v_cach
  * FlashAttn guide §4, SectionStreamK; splitting S2 when B*N2 is small,
  * aclnnIncreFlashAttention guide §8.2). A unit crossed by share boundaries
  * is computed in pieces that are merged by their log-sum-exp.
- * With num_splits = 0 the shares are equal in cost: a row costs 1 and, when
- * the non-empty units outnumber num_sms (so that a share holds several unit
- * starts), the start of every unit after the first costs 192 * 128 / D rows
- * more, the work of the piece end it brings; a share holding unit starts
- * then takes fewer rows. Row x of unit k costs x + that cost * k.
+ * With num_splits = 0 the shares are equal in cost: a row costs 1 and the
+ * start of every unit after the first costs c * 128 / D rows more, the work
+ * of the piece end it brings, with c = 192 when the non-empty units outnumber
+ * num_sms (so that a share holds several unit starts), c = 384 when they do
+ * not but a CTA handles four or more query heads (the most costly piece
+ * end), else 0; a share holding unit starts then takes fewer rows. Row x of
+ * unit k costs x + that cost * k.
  *   chunk_rows  cost of a share: with num_splits = 0, the total cost divided
  *               by num_sms (at least 224); with n > 0, ceil(S_kv_max / n)
  *               rounded up to a multiple of 64, and a row costs 1

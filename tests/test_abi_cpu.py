@@ -198,14 +198,21 @@ def _units(lens, Hq, Hkv, D):
     return Hkv * (g // _heads_per_cta(g, D))
 
 
-PC128 = 192  # rows a unit start costs at D = 128 when the shares are cut by cost
+PC128 = 192        # rows a unit start costs at D = 128 when units outnumber SMs
+PC128_HEADS = 384  # ... when they do not, and a CTA carries four or more query heads
 
 
 def _piece_cost(lens, Hq, Hkv, D, sms=152, splits=0):
-    """The extra cost of a unit start: charged only when the non-empty units
-    outnumber the SMs (PC128 rows at D = 128, scaled by 128 / D)."""
+    """The extra cost of a unit start (scaled by 128 / D): PC128 rows when the
+    non-empty units outnumber the SMs, PC128_HEADS when there are fewer (but
+    more than one) and a CTA carries four or more query heads, else none."""
     units = _units(lens, Hq, Hkv, D) * sum(1 for L in lens if L)
-    return PC128 * 128 // D if splits == 0 and units > sms else 0
+    if splits or units <= 1:
+        return 0
+    if units > sms:
+        return PC128 * 128 // D
+    g = Hq // Hkv
+    return PC128_HEADS * 128 // D if _heads_per_cta(g, D) >= 4 else 0
 
 
 def _pieces(lens, Hq, Hkv, D, rc, pc=0):
@@ -246,11 +253,16 @@ def test_plan_cuts_equal_shares(lib):
 
 
 def test_plan_one_share_per_sm():
-    # GQA decode workload shape: 8 batches x 8 KV heads, lengths ~U[1024, 8192]
+    # GQA decode workload shape: 8 batches x 8 KV heads, lengths ~U[1024, 8192];
+    # four heads per CTA: the shares are cut by cost
     lens = [1024, 8192, 4000, 6000, 3000, 7777, 2048, 5000]
     rc, n, mx = _plan(lens, 8192, 32, 8)
+    cost = 8 * sum(lens) + PC128_HEADS * (8 * 8 - 1)
+    assert n == 152 and rc * 152 >= cost > rc * 151
+    assert mx == max(_pieces(lens, 32, 8, 128, rc, PC128_HEADS)[0])
+    # one query head per KV head and fewer units than SMs: shares of rows
+    rc, n, mx = _plan(lens, 8192, 8, 8)
     assert n == 152 and rc * 152 >= 8 * sum(lens) > rc * 151
-    assert mx == max(_pieces(lens, 32, 8, 128, rc)[0])
     # one long sequence, 32 heads: every SM streams an equal share
     rc, n, mx = _plan([131072], 131072, 32, 32)
     assert n == 152 and mx == max(_pieces([131072], 32, 32, 128, rc)[0])
@@ -483,7 +495,9 @@ def test_header_is_plain_c_and_the_library_links_from_c(lib, tmp_path):
                     f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
     st, rc, n, mx, ws = out[0].split()
-    assert (int(st), int(rc), int(n), int(mx)) == (0, 224, 1, 1)
+    # 4 units (two sequences x two KV heads, four heads per CTA): cut by cost,
+    # 214 rows + 3 unit starts x 384 = 1366 over shares of 224, one unit each
+    assert (int(st), int(rc), int(n), int(mx)) == (0, 224, 7, 1)
     assert int(ws) == F.fa_decode_workspace_size(8, 8192, 32, 8, 128, 0)
     assert out[1] == lib.fa_status_string(_lib.FA_ERR_UNSUPPORTED).decode()
 
