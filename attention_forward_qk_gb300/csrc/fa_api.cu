@@ -851,9 +851,17 @@ fa_status decode_impl(const void* q, const void* k, const void* v, const PagedKv
   }
   // the status word, and the piece counters of the units cut into several
   // pieces, start at zero: one clear on the stream before the launch (a
-  // kernel-side clear could erase a timeout another CTA recorded first)
+  // clear inside the decode kernel could erase a timeout another CTA
+  // recorded first); for the default plan a kernel of its own rather than a
+  // memset, so that the decode kernel plans its first piece while it runs
+  // (split_kernel plans after its wait: a memset costs it less)
   const size_t clear_bytes = (total > 0 && max_slots > 1) ? ws.clear : sizeof(uint32_t);
-  if (cudaMemsetAsync(wsb, 0, clear_bytes, s) != cudaSuccess) return FA_ERR_RUNTIME;
+  if (num_splits > 0) {
+    if (cudaMemsetAsync(wsb, 0, clear_bytes, s) != cudaSuccess) return FA_ERR_RUNTIME;
+  } else {
+    if (launch_clear(wsb, clear_bytes, s) != cudaSuccess) return FA_ERR_RUNTIME;
+    count_launches(1);
+  }
 
   DecodeLaunch x;
   x.q = q;

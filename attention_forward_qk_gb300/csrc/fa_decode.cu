@@ -1577,6 +1577,27 @@ cudaError_t launch_decode_d(int G, int grid, bool loop, const CUtensorMap* m,
 
 }  // namespace
 
+// Zeroes the first n words of a decode workspace (the status word and the
+// piece counters) on the stream before the decode kernel. It lets that
+// kernel start at once (programmatic dependent launch), so the kernel plans
+// its first piece while this runs; the kernel reads the counters and the
+// status word only after its griddepcontrol.wait, which waits for this
+// kernel's writes. It is launched in stream order itself, after all earlier
+// work (a decode kernel before it may still use the same counters).
+__global__ void __launch_bounds__(256) clear_kernel(uint32_t* __restrict__ p, int n) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int i = static_cast<int>(blockIdx.x) * 256 + static_cast<int>(threadIdx.x); i < n;
+       i += static_cast<int>(gridDim.x) * 256)
+    p[i] = 0u;
+}
+
+cudaError_t launch_clear(void* workspace, size_t bytes, cudaStream_t stream) {
+  const int n = static_cast<int>(bytes / sizeof(uint32_t));
+  const int grid = std::max(1, std::min((n + 255) / 256, 128));
+  clear_kernel<<<grid, 256, 0, stream>>>(static_cast<uint32_t*>(workspace), n);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeLaunch& x, cudaStream_t stream) {
   const int g_total = x.Hq / x.Hkv;
   const int G = decode_heads_per_cta(g_total, x.D);

@@ -134,6 +134,10 @@ struct DecodeLaunch {
   uint64_t timeout_ns;
 };
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream);
+// Zero `bytes` (a multiple of 4) at the start of a decode workspace, before
+// launch_decode on the same stream (which may then start its set-up while
+// this runs).
+cudaError_t launch_clear(void* workspace, size_t bytes, cudaStream_t stream);
 
 struct PrefillLaunch {
   const void* q;
