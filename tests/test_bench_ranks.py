@@ -63,3 +63,17 @@ def test_reference_arm_other_ranks_exit_quietly():
                        text=True, timeout=120)
     assert p.returncode == 0, p.stderr
     assert p.stdout.strip() == ""
+
+
+@pytest.mark.parametrize("args", [
+    ["--workload", "causal_prefill", "--num-splits", "4"],   # a prefill workload
+    ["--workload", "paged_decode", "--num-splits", "4"],     # the paged decode: default plan only
+    ["--workload", "long_decode", "--num-splits", "-1"],
+    ["--warmup", "2"],
+])
+def test_bench_rejects_bad_options(args):
+    """Argument errors end the bench before any GPU work (exit status 2)."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 2, r.stderr
+    assert "error:" in r.stderr
