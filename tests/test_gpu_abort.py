@@ -48,6 +48,30 @@ def test_prefill_timeout_aborts_and_the_next_call_is_exact(cuda_device, D):
     compare(out, lse, ro, rl, "BSND")
 
 
+def test_paged_prefill_timeout_aborts_and_the_next_call_is_exact(cuda_device):
+    """The paged instantiation: a KV tile lands as several boxes on one
+    barrier, all issued after one byte count, so the drain after an abort
+    waits for whole tiles as with a contiguous cache."""
+    from test_gpu_paged_prefill import _case
+    B, H, S, D, bs = 1, 4, 1024, 128, 32
+    q, k, v, kp, vp, table = _case(B, H, H, S, S, D, bs, "PA_BBND", seed=33)
+    args = (q.cuda(), kp.cuda(), vp.cuda(), table.cuda(), bs, S)
+    kw = dict(kv_layout="PA_BBND", mask_mode="causal", scale=1 / math.sqrt(D))
+    ws = torch.empty(F.fa_forward_workspace_size(B, S, S, H, H, D), dtype=torch.uint8,
+                     device="cuda")
+    F.fa_set_wait_timeout_ns(SHORT_NS)
+    try:
+        F.fa_forward_paged(*args, workspace=ws, **kw)
+        assert F.fa_workspace_status(ws) == _lib.FA_ERR_DEVICE_TIMEOUT
+    finally:
+        F.fa_set_wait_timeout_ns(0)
+    out, lse = F.fa_forward_paged(*args, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    assert F.fa_workspace_status(ws) == _lib.FA_OK
+    ro, rl = oracle.attention(q, k, v, scale=1 / math.sqrt(D), causal=True)
+    compare(out, lse, ro, rl, "BNSD")
+
+
 def test_decode_timeout_aborts_and_the_next_call_is_exact(cuda_device):
     B, Hq, Hkv, S, D = 4, 16, 4, 3000, 128
     x = workloads.make_decode(B, Hq, Hkv, S, D, "BNSD", seed=41, len_lo=500, len_hi=S)
