@@ -730,10 +730,25 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (lane == 0) {
       int st = 0;  // stages issued by this CTA
       bool ok = true;
+      // the first stage, when it is a full stage of a contiguous cache, is
+      // issued here, next to the planning code, rather than from the loop
+      // below (whose code is then fetched while the stage is in flight)
+      bool first_issued = false;
+      if (early && h.piece >= 0 && a.block_table == nullptr && h.rows >= C::R) {
+        h.stage = 0;
+        hdr[0] = h;
+        mbar_expect_tx(full0, C::STAGE_BYTES + G * D * 2);
+        tma_load_4d(smem_u32(smem), &tm_k, full0, 0, h.row0, kvh, h.b);
+        tma_load_4d(smem_u32(smem + C::TILE_BYTES), &tm_v, full0, 0, h.row0, kvh, h.b);
+        bulk_load(smem_u32(qbuf), a.q + (static_cast<size_t>(h.b) * a.Hq + kvh * g_total + hg * G) * D,
+                  G * D * 2, full0);
+        first_issued = true;
+        st = 1;
+      }
       for (int piece = 0; ok; ++piece) {
         if (piece > 0 || !early) plan(piece, h, kvh, hg);
         const bool done = h.piece < 0;
-        for (int s = 0; s < h.nstage; ++s, ++st) {
+        for (int s = piece == 0 && first_issued ? 1 : 0; s < h.nstage; ++s, ++st) {
           const int slot = st % NST;
           const int use = st / NST;
           if (use > 0 && !mbar_wait_polled(empty0 + 8 * slot, (use - 1) & 1, a.timeout_ns, a.status,
@@ -806,12 +821,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   if (np == 0 || *abort_flag) return;
   volatile int* merge_mask = n_pending + 1;
   if (tid == 0) {
-    __threadfence();  // the partials of this CTA, written before the barrier, first
-    const unsigned c0 = atomicAdd(a.counters + pending[0].unit, 1u);
-    const unsigned c1 = np > 1 ? atomicAdd(a.counters + pending[1].unit, 1u) : 0u;
+    // release: the partials of this CTA, written before the barrier, before
+    // the count; acquire: the other pieces' partials after it (for the merge)
+    const unsigned c0 = atom_add_acq_rel_gpu(a.counters + pending[0].unit, 1u);
+    const unsigned c1 = np > 1 ? atom_add_acq_rel_gpu(a.counters + pending[1].unit, 1u) : 0u;
     int mm = c0 == static_cast<unsigned>(pending[0].nsp - 1) ? 1 : 0;
     if (np > 1 && c1 == static_cast<unsigned>(pending[1].nsp - 1)) mm |= 2;
-    if (mm) __threadfence();
     *merge_mask = mm;
   }
   __syncthreads();
